@@ -1,0 +1,272 @@
+/*
+ * Oracle for the quantized actor linear layer — TEST INFRASTRUCTURE ONLY.
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg may load
+ * this file's library.  The product path (the CUDA library) never does, and
+ * this file includes nothing from it.
+ *
+ * What it computes (plain, slow, obviously correct; OpenMP over independent
+ * groups only, no blocking or reordering inside a group):
+ *
+ *  - FP8 E4M3 ("fn" variant: max 448, no infinities, 0x7F/0xFF are NaN) decode
+ *    and round-to-nearest-even, saturating encode.  The pages name FP8 for the
+ *    GEMMs (Jet-RL notes, "细粒度 GEMM 量化方案") and E4M3 only as the NVFP4
+ *    block-scale format (QeRL news article, key takeaways); the sub-format,
+ *    the rounding and the saturation are the readings recorded in the design doc.
+ *  - Fine-grained quantization (Jet-RL notes, "细粒度 GEMM 量化方案", Fig. 6):
+ *      * 1x128 groups along K for activations / gradients,
+ *      * 128x1 groups along the token dimension for the second WGrad operand,
+ *      * 128x128 blocks for weights.
+ *    Per group: amax = max |x|, s = fl32(amax / 448) (1.0 when amax == 0),
+ *    q = encode(fl32(x / s)) with IEEE fp32 division.  Scales are dequant
+ *    multipliers: x ~= decode(q) * s.
+ *  - The UAQ invariant-scaling fold WX = (W/s)(sX) (QuRL notes, 关键设计 §1):
+ *    W'[n,k] = bf16_RN(fl32(W[n,k] / s_k)),  P'[r,k] = bf16_RN(fl32(P[r,k] * s_k)).
+ *
+ * The fp64 GEMMs over dequantized operands live in oracle.py (NumPy).
+ *
+ * Build: gcc -O2 -fopenmp -ffp-contract=off -shared -fPIC (no -ffast-math:
+ * subnormals and IEEE division must be honoured).
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#if !defined(FLT_EVAL_METHOD) || FLT_EVAL_METHOD != 0
+#error "the oracle needs fp32 expressions evaluated in fp32 (FLT_EVAL_METHOD == 0)"
+#endif
+
+#define GRP 128
+
+/* ---------------------------------------------------------------- bf16 --- */
+
+static float bf16_bits_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* fp32 -> bf16, round to nearest, ties to even.  bf16 keeps the upper 16 bits
+ * of the fp32 pattern, so rounding looks only at the 16 discarded bits. */
+uint16_t orc_f32_to_bf16_rn(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u); /* quiet NaN, outside the contract */
+    uint32_t upper = u >> 16, lower = u & 0xFFFFu;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1; /* may carry into the exponent, up to infinity: that is RN */
+    return (uint16_t)upper;
+}
+
+/* ---------------------------------------------------------------- E4M3 --- */
+
+/* Value of an E4M3 code: sign bit 7, exponent bits 6..3 (bias 7), mantissa
+ * bits 2..0.  Exponent 0 is subnormal (m * 2^-9).  Exponent 15 with mantissa 7
+ * is NaN; every other pattern is finite. */
+double orc_e4m3_decode(uint8_t c)
+{
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double mag = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Round a non-negative exact double to an integer, ties to even. */
+static double round_half_even(double t)
+{
+    double f = floor(t), r = t - f;
+    if (r > 0.5)
+        return f + 1.0;
+    if (r < 0.5)
+        return f;
+    return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+}
+
+/* fp32 -> E4M3: nearest representable value, ties to the even mantissa, and
+ * magnitudes at or above 448 clamp to 448 (satfinite).  The sign of zero is
+ * kept.  NaN maps to 0x7F (outside the contract). */
+uint8_t orc_e4m3_encode(float v)
+{
+    if (isnan(v))
+        return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    if (a < 0x1p-6) {
+        /* subnormal grid: multiples of 2^-9; m == 8 is the first normal 2^-6,
+         * whose code 0x08 is exactly the integer 8. */
+        double m = round_half_even(a * 512.0);
+        return sign | (uint8_t)m;
+    }
+    int e;
+    (void)frexp(a, &e);
+    e -= 1; /* a = 2^e * [1, 2) */
+    double t = (ldexp(a, -e) - 1.0) * 8.0; /* exact: a has <= 24 significant bits */
+    double m = round_half_even(t);
+    if (m == 8.0) {
+        m = 0.0;
+        e += 1;
+    }
+    /* a < 448 keeps (e, m) at or below (8, 6): no NaN pattern can result. */
+    return sign | (uint8_t)(((e + 7) << 3) | (int)m);
+}
+
+/* --------------------------------------------------------- group quant --- */
+
+/* Scale of a group from its amax: fl32(amax / 448), or 1.0 for an all-zero
+ * group. */
+static float group_scale(float amax)
+{
+    return (amax == 0.0f) ? 1.0f : amax / 448.0f;
+}
+
+float orc_group_scale(float amax) { return group_scale(amax); }
+
+/* One element of a group: encode(fl32(x / s)). */
+uint8_t orc_quant_element(float x, float s) { return orc_e4m3_encode(x / s); }
+
+/* 1x128 groups along K (row-wise).  x bf16 [M,K] (row pitch ldx elements);
+ * q u8 [M,K] (pitch ldq); s f32, s[kb*lds + m]. */
+void orc_quant_rows_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                          uint8_t *q, int64_t ldq, float *s, int64_t lds)
+{
+    int64_t KB = K / GRP;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            const uint16_t *g = x + m * ldx + kb * GRP;
+            float amax = 0.0f;
+            for (int i = 0; i < GRP; ++i) {
+                float a = fabsf(bf16_bits_to_f32(g[i]));
+                if (a > amax)
+                    amax = a;
+            }
+            float sc = group_scale(amax);
+            s[kb * lds + m] = sc;
+            for (int i = 0; i < GRP; ++i)
+                q[m * ldq + kb * GRP + i] = orc_e4m3_encode(bf16_bits_to_f32(g[i]) / sc);
+        }
+    }
+}
+
+/* 128x1 groups along M (column-wise), codes written transposed.
+ * x bf16 [M,K]; qT u8, qT[k*ldqT + m] for m < M; sc f32, sc[mb*ldsc + k].
+ * The last group of a column covers rows mb*128 .. M-1 only. */
+void orc_quant_cols_128x1(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                          uint8_t *qT, int64_t ldqT, float *sc, int64_t ldsc)
+{
+    int64_t MB = (M + GRP - 1) / GRP;
+#pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < K; ++k) {
+        for (int64_t mb = 0; mb < MB; ++mb) {
+            int64_t m0 = mb * GRP, m1 = (m0 + GRP < M) ? m0 + GRP : M;
+            float amax = 0.0f;
+            for (int64_t m = m0; m < m1; ++m) {
+                float a = fabsf(bf16_bits_to_f32(x[m * ldx + k]));
+                if (a > amax)
+                    amax = a;
+            }
+            float s = group_scale(amax);
+            sc[mb * ldsc + k] = s;
+            for (int64_t m = m0; m < m1; ++m)
+                qT[k * ldqT + m] = orc_e4m3_encode(bf16_bits_to_f32(x[m * ldx + k]) / s);
+        }
+    }
+}
+
+/* 128x128 blocks (weights).  w bf16 [N,K]; q u8 [N,K]; s[nb*lds + kb];
+ * optional qT u8 [K,N] (qT[k*ldqT + n]) holding the same codes transposed. */
+void orc_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
+                              uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                              uint8_t *qT, int64_t ldqT)
+{
+    int64_t NB = N / GRP, KB = K / GRP;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t nb = 0; nb < NB; ++nb) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            float amax = 0.0f;
+            for (int64_t n = nb * GRP; n < (nb + 1) * GRP; ++n)
+                for (int64_t k = kb * GRP; k < (kb + 1) * GRP; ++k) {
+                    float a = fabsf(bf16_bits_to_f32(w[n * ldw + k]));
+                    if (a > amax)
+                        amax = a;
+                }
+            float sc = group_scale(amax);
+            s[nb * lds + kb] = sc;
+            for (int64_t n = nb * GRP; n < (nb + 1) * GRP; ++n)
+                for (int64_t k = kb * GRP; k < (kb + 1) * GRP; ++k) {
+                    uint8_t c = orc_e4m3_encode(bf16_bits_to_f32(w[n * ldw + k]) / sc);
+                    q[n * ldq + k] = c;
+                    if (qT)
+                        qT[k * ldqT + n] = c;
+                }
+        }
+    }
+}
+
+/* ------------------------------------------------------------ UAQ fold --- */
+
+/* W [N,K] bf16 in place: column k divided by s[k]; prev [R,K] bf16 in place
+ * (nullable): column k multiplied by s[k].  Each result is rounded to bf16. */
+void orc_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, const float *s,
+                  uint16_t *prev, int64_t R, int64_t ldp)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            w[n * ldw + k] = orc_f32_to_bf16_rn(bf16_bits_to_f32(w[n * ldw + k]) / s[k]);
+    if (prev) {
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < R; ++r)
+            for (int64_t k = 0; k < K; ++k)
+                prev[r * ldp + k] =
+                    orc_f32_to_bf16_rn(bf16_bits_to_f32(prev[r * ldp + k]) * s[k]);
+    }
+}
+
+/* --------------------------------------------------------- bulk helpers --- */
+
+/* Element-wise encode / decode of arrays, for the pins. */
+void orc_e4m3_encode_array(const float *v, int64_t n, uint8_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_encode(v[i]);
+}
+
+void orc_e4m3_decode_array(const uint8_t *c, int64_t n, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_decode(c[i]);
+}
+
+void orc_f32_to_bf16_array(const float *v, int64_t n, uint16_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_f32_to_bf16_rn(v[i]);
+}
+
+/* Element map of the group quantizer for given (x, s) pairs. */
+void orc_quant_element_array(const float *x, const float *s, int64_t n, uint8_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_quant_element(x[i], s[i]);
+}
+
+int orc_num_threads(void);
+#ifdef _OPENMP
+#include <omp.h>
+int orc_num_threads(void) { return omp_get_max_threads(); }
+#else
+int orc_num_threads(void) { return 1; }
+#endif
