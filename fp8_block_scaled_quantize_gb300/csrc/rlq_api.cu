@@ -1,0 +1,301 @@
+// C ABI of librlq.so: host-side argument validation and dispatch to the
+// kernels.  Every check runs before any launch; a failing call launches
+// nothing and leaves a description for rlq_last_error().
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "rlq_internal.h"
+
+namespace rlq {
+
+namespace {
+thread_local char g_last_error[512] = "";
+}
+
+rlq_status fail(rlq_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+const char *last_error_text() { return g_last_error; }
+
+rlq_status cuda_status(cudaError_t err, const char *what)
+{
+    if (err == cudaSuccess)
+        return RLQ_OK;
+    return fail(RLQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+}  // namespace rlq
+
+using namespace rlq;
+
+namespace {
+
+constexpr int64_t G = 128;
+constexpr int64_t MAX_DIM = (int64_t)1 << 31;  // TMA coordinates and tile indices are 32-bit
+
+bool al(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+#define RLQ_REQUIRE(cond, code, ...)        \
+    do {                                    \
+        if (!(cond))                        \
+            return fail((code), __VA_ARGS__); \
+    } while (0)
+
+// Code matrix [rows][cols] with pitch ld (bytes): TMA-ready.
+rlq_status check_codes(const char *name, const void *p, int64_t ld, int64_t cols)
+{
+    RLQ_REQUIRE(p, RLQ_ERR_INVALID_ARG, "%s is NULL", name);
+    RLQ_REQUIRE(ld >= cols, RLQ_ERR_INVALID_ARG, "%s: pitch %lld < row length %lld", name, (long long)ld, (long long)cols);
+    RLQ_REQUIRE(al(p, 16), RLQ_ERR_MISALIGNED, "%s is not 16-byte aligned", name);
+    RLQ_REQUIRE(ld % 16 == 0, RLQ_ERR_MISALIGNED, "%s: pitch %lld bytes is not a multiple of 16", name, (long long)ld);
+    return RLQ_OK;
+}
+
+// bf16 matrix with pitch ld (elements).
+rlq_status check_bf16(const char *name, const void *p, int64_t ld, int64_t cols)
+{
+    RLQ_REQUIRE(p, RLQ_ERR_INVALID_ARG, "%s is NULL", name);
+    RLQ_REQUIRE(ld >= cols, RLQ_ERR_INVALID_ARG, "%s: pitch %lld < row length %lld", name, (long long)ld, (long long)cols);
+    RLQ_REQUIRE(al(p, 16), RLQ_ERR_MISALIGNED, "%s is not 16-byte aligned", name);
+    RLQ_REQUIRE(ld % 8 == 0, RLQ_ERR_MISALIGNED, "%s: pitch %lld elements is not a multiple of 8 (16 bytes)", name,
+                (long long)ld);
+    return RLQ_OK;
+}
+
+// fp32 scale array, s[b * ld + i] for i < extent.
+rlq_status check_scales(const char *name, const void *p, int64_t ld, int64_t extent)
+{
+    RLQ_REQUIRE(p, RLQ_ERR_INVALID_ARG, "%s is NULL", name);
+    RLQ_REQUIRE(ld >= extent, RLQ_ERR_INVALID_ARG, "%s: pitch %lld < %lld", name, (long long)ld, (long long)extent);
+    RLQ_REQUIRE(al(p, 4), RLQ_ERR_MISALIGNED, "%s is not 4-byte aligned", name);
+    return RLQ_OK;
+}
+
+#define RLQ_TRY(expr)                  \
+    do {                               \
+        const rlq_status _st = (expr); \
+        if (_st != RLQ_OK)             \
+            return _st;                \
+    } while (0)
+
+cudaStream_t cs(rlq_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+rlq_status rlq_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, int64_t ldq, float *s,
+                               int64_t lds, uint8_t *qT, int64_t ldqT, float *sc, int64_t ldsc, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(M >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size (M=%lld, K=%lld)", (long long)M, (long long)K);
+    RLQ_REQUIRE(K % G == 0, RLQ_ERR_UNSUPPORTED, "K=%lld is not a multiple of 128", (long long)K);
+    RLQ_REQUIRE((qT == nullptr) == (sc == nullptr), RLQ_ERR_INVALID_ARG,
+                "qT and sc must be both NULL (row-wise only) or both set (fused 128x1)");
+    RLQ_REQUIRE(M < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    if (M == 0 || K == 0)
+        return RLQ_OK;
+    RLQ_TRY(check_bf16("x", x, ldx, K));
+    RLQ_TRY(check_codes("q", q, ldq, K));
+    RLQ_TRY(check_scales("s", s, lds, M));
+    if (qT) {
+        RLQ_TRY(check_codes("qT", qT, ldqT, M));
+        RLQ_TRY(check_scales("sc", sc, ldsc, K));
+        return cuda_status(launch_quant_dual(x, M, K, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, cs(stream)),
+                           "1x128 + 128x1 quantizer launch");
+    }
+    return cuda_status(launch_quant_rows(x, M, K, ldx, q, ldq, s, lds, cs(stream)), "1x128 quantizer launch");
+}
+
+rlq_status rlq_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+                                    float *s, int64_t lds, uint8_t *qT, int64_t ldqT, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size (N=%lld, K=%lld)", (long long)N, (long long)K);
+    RLQ_REQUIRE(N % G == 0 && K % G == 0, RLQ_ERR_UNSUPPORTED, "N=%lld and K=%lld must be multiples of 128",
+                (long long)N, (long long)K);
+    RLQ_REQUIRE(N < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    if (N == 0 || K == 0)
+        return RLQ_OK;
+    RLQ_TRY(check_bf16("w", w, ldw, K));
+    RLQ_TRY(check_codes("q", q, ldq, K));
+    RLQ_TRY(check_scales("s", s, lds, K / G));
+    if (qT)
+        RLQ_TRY(check_codes("qT", qT, ldqT, N));
+    return cuda_status(launch_quant_weight(w, N, K, ldw, q, ldq, s, lds, qT, ldqT, cs(stream)),
+                       "128x128 quantizer launch");
+}
+
+rlq_status rlq_gemm_fprop(const uint8_t *xq, int64_t ldxq, const float *xs, int64_t ldxs, const uint8_t *wq,
+                          int64_t ldwq, const float *ws, int64_t ldws, uint16_t *y, int64_t ldy, int64_t M, int64_t N,
+                          int64_t K, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
+    RLQ_REQUIRE(N % G == 0 && K % G == 0, RLQ_ERR_UNSUPPORTED, "N=%lld and K=%lld must be multiples of 128",
+                (long long)N, (long long)K);
+    RLQ_REQUIRE(M < MAX_DIM && N < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    if (M == 0 || N == 0)
+        return RLQ_OK;
+    RLQ_TRY(check_bf16("y", y, ldy, N));
+    if (K > 0) {
+        RLQ_TRY(check_codes("xq", xq, ldxq, K));
+        RLQ_TRY(check_codes("wq", wq, ldwq, K));
+        RLQ_TRY(check_scales("xs", xs, ldxs, M));
+        RLQ_TRY(check_scales("ws", ws, ldws, K / G));
+    }
+    GemmArgs a{};
+    a.A = xq;
+    a.lda = ldxq;
+    a.B = wq;
+    a.ldb = ldwq;
+    a.sa = xs;
+    a.ld_sa = ldxs;
+    a.sb = ws;
+    a.sb_bstride = 1;      // contraction block kb
+    a.sb_cstride = ldws;   // output column block nb
+    a.per_col_sb = false;
+    a.out = y;
+    a.ldo = ldy;
+    a.R = M;
+    a.C = N;
+    a.L = K;
+    return launch_gemm(a, cs(stream));
+}
+
+rlq_status rlq_gemm_dgrad(const uint8_t *dyq, int64_t lddyq, const float *dys, int64_t lddys, const uint8_t *w,
+                          int64_t ldw, int wq_is_transposed, const float *ws, int64_t ldws, uint16_t *dx, int64_t lddx,
+                          int64_t M, int64_t N, int64_t K, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
+    RLQ_REQUIRE(N % G == 0 && K % G == 0, RLQ_ERR_UNSUPPORTED, "N=%lld and K=%lld must be multiples of 128",
+                (long long)N, (long long)K);
+    RLQ_REQUIRE(wq_is_transposed == 0 || wq_is_transposed == 1, RLQ_ERR_INVALID_ARG,
+                "wq_is_transposed must be 0 or 1");
+    RLQ_REQUIRE(M < MAX_DIM && N < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    if (M == 0 || K == 0)
+        return RLQ_OK;
+    RLQ_TRY(check_bf16("dx", dx, lddx, K));
+    if (N > 0) {
+        RLQ_TRY(check_codes("dyq", dyq, lddyq, N));
+        RLQ_TRY(check_scales("dys", dys, lddys, M));
+        RLQ_TRY(check_scales("ws", ws, ldws, K / G));
+        if (wq_is_transposed)
+            RLQ_TRY(check_codes("wqT", w, ldw, N));
+        else
+            RLQ_TRY(check_codes("wq", w, ldw, K));
+    }
+    RLQ_REQUIRE(wq_is_transposed == 1, RLQ_ERR_UNSUPPORTED,
+                "DGrad on the untransposed weight codes is not built in this version: "
+                "pass the transposed codes from rlq_quant_weight_128x128 (wq_is_transposed = 1)");
+    GemmArgs a{};
+    a.A = dyq;
+    a.lda = lddyq;
+    a.B = w;  // wqT [K rows][N]: output column k, contraction n
+    a.ldb = ldw;
+    a.sa = dys;
+    a.ld_sa = lddys;
+    a.sb = ws;             // scale of contraction block nb, output block kb: ws[nb * ldws + kb]
+    a.sb_bstride = ldws;
+    a.sb_cstride = 1;
+    a.per_col_sb = false;
+    a.out = dx;
+    a.ldo = lddx;
+    a.R = M;
+    a.C = K;
+    a.L = N;
+    return launch_gemm(a, cs(stream));
+}
+
+rlq_status rlq_gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, int64_t lddysc, const uint8_t *xqT,
+                          int64_t ldxqT, const float *xsc, int64_t ldxsc, uint16_t *dw, int64_t lddw, int64_t M,
+                          int64_t N, int64_t K, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
+    RLQ_REQUIRE(N % G == 0 && K % G == 0, RLQ_ERR_UNSUPPORTED, "N=%lld and K=%lld must be multiples of 128",
+                (long long)N, (long long)K);
+    RLQ_REQUIRE(M < MAX_DIM && N < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    if (N == 0 || K == 0)
+        return RLQ_OK;
+    RLQ_TRY(check_bf16("dw", dw, lddw, K));
+    if (M > 0) {
+        RLQ_TRY(check_codes("dyqT", dyqT, lddyqT, M));
+        RLQ_TRY(check_codes("xqT", xqT, ldxqT, M));
+        RLQ_TRY(check_scales("dysc", dysc, lddysc, N));
+        RLQ_TRY(check_scales("xsc", xsc, ldxsc, K));
+        RLQ_REQUIRE(al(xsc, 16) && ldxsc % 4 == 0, RLQ_ERR_MISALIGNED,
+                    "xsc rows must be 16-byte aligned (pointer 16-byte aligned, pitch a multiple of 4)");
+    }
+    GemmArgs a{};
+    a.A = dyqT;
+    a.lda = lddyqT;
+    a.B = xqT;
+    a.ldb = ldxqT;
+    a.sa = dysc;
+    a.ld_sa = lddysc;
+    a.sb = xsc;
+    a.sb_bstride = ldxsc;
+    a.sb_cstride = 0;
+    a.per_col_sb = true;
+    a.out = dw;
+    a.ldo = lddw;
+    a.R = N;
+    a.C = K;
+    a.L = M;
+    return launch_gemm(a, cs(stream));
+}
+
+rlq_status rlq_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, const float *s, uint16_t *prev, int64_t R,
+                        int64_t ldp, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(N >= 0 && K >= 0 && R >= 0, RLQ_ERR_INVALID_ARG, "negative size");
+    RLQ_REQUIRE(K % 8 == 0, RLQ_ERR_UNSUPPORTED, "K=%lld is not a multiple of 8", (long long)K);
+    if (K == 0 || (N == 0 && (prev == nullptr || R == 0)))
+        return RLQ_OK;
+    RLQ_REQUIRE(s, RLQ_ERR_INVALID_ARG, "s is NULL");
+    RLQ_REQUIRE(al(s, 16), RLQ_ERR_MISALIGNED, "s is not 16-byte aligned");
+    if (N > 0)
+        RLQ_TRY(check_bf16("w", w, ldw, K));
+    if (prev && R > 0)
+        RLQ_TRY(check_bf16("prev", prev, ldp, K));
+    return cuda_status(launch_uaq_fold(w, N, K, ldw, s, prev, R, ldp, cs(stream)), "UAQ fold launch");
+}
+
+rlq_status rlq_check(rlq_stream_t stream) { return check_device_errors(cs(stream)); }
+
+rlq_status rlq_diag_bounded_wait(int64_t timeout_us, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(timeout_us >= 1 && timeout_us <= 10000000, RLQ_ERR_INVALID_ARG, "timeout_us must be in 1 .. 10^7");
+    return launch_diag_wait(timeout_us, cs(stream));
+}
+
+const char *rlq_status_string(rlq_status status)
+{
+    switch (status) {
+    case RLQ_OK:
+        return "RLQ_OK";
+    case RLQ_ERR_INVALID_ARG:
+        return "RLQ_ERR_INVALID_ARG: invalid argument";
+    case RLQ_ERR_UNSUPPORTED:
+        return "RLQ_ERR_UNSUPPORTED: unsupported shape";
+    case RLQ_ERR_MISALIGNED:
+        return "RLQ_ERR_MISALIGNED: pointer or pitch breaks the alignment rules";
+    case RLQ_ERR_CUDA:
+        return "RLQ_ERR_CUDA: CUDA call or launch failed";
+    case RLQ_ERR_TIMEOUT:
+        return "RLQ_ERR_TIMEOUT: a bounded device-side wait ran out";
+    }
+    return "unknown rlq_status";
+}
+
+const char *rlq_last_error(void) { return last_error_text(); }
+
+const char *rlq_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Internal declarations shared by the translation units of librlq.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rlq.h"
+
+namespace rlq {
+
+// Records a failure description for rlq_last_error() and returns `st`.
+rlq_status fail(rlq_status st, const char *fmt, ...);
+
+// Text of the latest failure in the calling thread.
+const char *last_error_text();
+
+// Maps a CUDA error (if any) to RLQ_ERR_CUDA with a description.
+rlq_status cuda_status(cudaError_t err, const char *what);
+
+// ---- quantizers and fold (rlq_quant.cu); arguments already validated ----
+cudaError_t launch_quant_rows(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
+                              int64_t ldq, float *s, int64_t lds, cudaStream_t st);
+cudaError_t launch_quant_dual(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
+                              int64_t ldq, float *s, int64_t lds, uint8_t *qT, int64_t ldqT,
+                              float *sc, int64_t ldsc, cudaStream_t st);
+cudaError_t launch_quant_weight(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q,
+                                int64_t ldq, float *s, int64_t lds, uint8_t *qT, int64_t ldqT,
+                                cudaStream_t st);
+cudaError_t launch_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, const float *s,
+                            uint16_t *prev, int64_t R, int64_t ldp, cudaStream_t st);
+
+// ---- block-scaled GEMM (rlq_gemm.cu) ----
+//
+// out[r, c] = bf16( sum_b sa(b, r) * sb(b, c) * sum_{j in block b} A[r, j] * B[c, j] )
+// A: E4M3 [R rows][L contraction], pitch lda bytes; B: E4M3 [C rows][L], pitch ldb.
+// sa(b, r) = sa[b * ld_sa + r].
+// Block-scaled B (per_col_sb == false): sb(b, c) = sb[b * sb_bstride + (c / 128) * sb_cstride].
+// Column-scaled B (per_col_sb == true):  sb(b, c) = sb[b * sb_bstride + c], rows 16-byte aligned.
+struct GemmArgs {
+    const uint8_t *A;
+    int64_t lda;
+    const uint8_t *B;
+    int64_t ldb;
+    const float *sa;
+    int64_t ld_sa;
+    const float *sb;
+    int64_t sb_bstride;
+    int64_t sb_cstride;
+    bool per_col_sb;
+    uint16_t *out;
+    int64_t ldo;
+    int64_t R, C, L;
+};
+rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st);
+
+// Reads and clears the device error word of the current device (after syncing st).
+rlq_status check_device_errors(cudaStream_t st);
+rlq_status launch_diag_wait(int64_t timeout_us, cudaStream_t st);
+
+}  // namespace rlq

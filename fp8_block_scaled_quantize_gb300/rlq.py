@@ -1,0 +1,244 @@
+"""Thin ctypes binding of librlq.so (include/rlq.h).
+
+The functions named ``rlq_*`` mirror the C entry points one to one: plain
+integers for device pointers, sizes and the stream, and an ``RlqError`` raised
+for a non-OK status.  The lower-case helpers below them take torch tensors,
+allocate outputs with torch (device memory is PyTorch's plumbing here) and call
+the same entry points; every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if the library is missing or cannot be
+loaded, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+GRP = 128
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+
+_SIGS = {
+    "rlq_quant_act_1x128": [_P, _I, _I, _I, _P, _I, _P, _I, _P, _I, _P, _I, _P],
+    "rlq_quant_weight_128x128": [_P, _I, _I, _I, _P, _I, _P, _I, _P, _I, _P],
+    "rlq_gemm_fprop": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
+    "rlq_gemm_dgrad": [_P, _I, _P, _I, _P, _I, ctypes.c_int, _P, _I, _P, _I, _I, _I, _I, _P],
+    "rlq_gemm_wgrad": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
+    "rlq_uaq_fold": [_P, _I, _I, _I, _P, _P, _I, _I, _P],
+    "rlq_check": [_P],
+    "rlq_diag_bounded_wait": [_I, _P],
+}
+
+STATUS = {0: "RLQ_OK", 1: "RLQ_ERR_INVALID_ARG", 2: "RLQ_ERR_UNSUPPORTED", 3: "RLQ_ERR_MISALIGNED",
+          4: "RLQ_ERR_CUDA", 5: "RLQ_ERR_TIMEOUT"}
+
+
+class RlqError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load librlq.so (building it first if its sources are newer)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path) or _build._stale():
+                _build.build()
+            L = ctypes.CDLL(path)
+            for name, args in _SIGS.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            L.rlq_status_string.argtypes = [ctypes.c_int]
+            L.rlq_status_string.restype = ctypes.c_char_p
+            L.rlq_last_error.argtypes = []
+            L.rlq_last_error.restype = ctypes.c_char_p
+            L.rlq_version.argtypes = []
+            L.rlq_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _call(name: str, *args) -> int:
+    L = lib()
+    st = getattr(L, name)(*args)
+    if st != 0:
+        raise RlqError(st, L.rlq_last_error().decode(errors="replace"))
+    return st
+
+
+# ------------------------------------------------- raw C-ABI mirrors ---
+
+def rlq_quant_act_1x128(x, M, K, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, stream):
+    return _call("rlq_quant_act_1x128", x, M, K, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, stream)
+
+
+def rlq_quant_weight_128x128(w, N, K, ldw, q, ldq, s, lds, qT, ldqT, stream):
+    return _call("rlq_quant_weight_128x128", w, N, K, ldw, q, ldq, s, lds, qT, ldqT, stream)
+
+
+def rlq_gemm_fprop(xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, stream):
+    return _call("rlq_gemm_fprop", xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, stream)
+
+
+def rlq_gemm_dgrad(dyq, lddyq, dys, lddys, w, ldw, wq_is_transposed, ws, ldws, dx, lddx, M, N, K, stream):
+    return _call("rlq_gemm_dgrad", dyq, lddyq, dys, lddys, w, ldw, wq_is_transposed, ws, ldws, dx, lddx,
+                 M, N, K, stream)
+
+
+def rlq_gemm_wgrad(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K, stream):
+    return _call("rlq_gemm_wgrad", dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K, stream)
+
+
+def rlq_uaq_fold(w, N, K, ldw, s, prev, R, ldp, stream):
+    return _call("rlq_uaq_fold", w, N, K, ldw, s, prev, R, ldp, stream)
+
+
+def rlq_check(stream):
+    return _call("rlq_check", stream)
+
+
+def rlq_diag_bounded_wait(timeout_us, stream):
+    return _call("rlq_diag_bounded_wait", timeout_us, stream)
+
+
+def rlq_status_string(status: int) -> str:
+    return lib().rlq_status_string(status).decode()
+
+
+def rlq_last_error() -> str:
+    return lib().rlq_last_error().decode(errors="replace")
+
+
+def rlq_version() -> str:
+    return lib().rlq_version().decode()
+
+
+# ------------------------------------------------------ torch helpers ---
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _ld(t) -> int:
+    """Row pitch in elements of a 2-D tensor whose rows are contiguous."""
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with contiguous rows")
+    return t.stride(0)
+
+
+def _round_up(v: int, m: int) -> int:
+    return (v + m - 1) // m * m
+
+
+def empty_codes_T(K: int, M: int, device) -> torch.Tensor:
+    """[K, M] uint8 view of a [K, round_up(M, 16)] buffer (TMA-ready pitch)."""
+    return torch.empty((K, _round_up(max(M, 1), 16)), dtype=torch.uint8, device=device)[:, :M]
+
+
+def quant_act_1x128(x: torch.Tensor, colwise: bool = False, stream=None):
+    """1x128 quantization of bf16 x [M, K]; with ``colwise`` also the fused
+    128x1 codes (transposed) and scales.
+
+    Returns (q [M,K] u8, s [K/128, M] f32, qT [K, M] u8 or None, sc [ceil(M/128), K] f32 or None).
+    """
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    M, K = x.shape
+    dev = x.device
+    q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((K // GRP, M), dtype=torch.float32, device=dev)
+    qT = sc = None
+    if colwise:
+        qT = empty_codes_T(K, M, dev)
+        sc = torch.empty(((M + GRP - 1) // GRP, K), dtype=torch.float32, device=dev)
+    rlq_quant_act_1x128(x.data_ptr(), M, K, _ld(x), q.data_ptr(), K, s.data_ptr(), max(M, 1),
+                        _ptr(qT), _ld(qT) if qT is not None else 0, _ptr(sc), K if sc is not None else 0,
+                        _stream(stream))
+    return q, s, qT, sc
+
+
+def quant_weight_128x128(w: torch.Tensor, transposed: bool = False, stream=None):
+    """128x128 block quantization of bf16 w [N, K].
+
+    Returns (q [N,K] u8, s [N/128, K/128] f32, qT [K,N] u8 or None).
+    """
+    if w.dtype != torch.bfloat16:
+        raise TypeError("w must be bfloat16")
+    N, K = w.shape
+    dev = w.device
+    q = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((N // GRP, K // GRP), dtype=torch.float32, device=dev)
+    qT = torch.empty((K, N), dtype=torch.uint8, device=dev) if transposed else None
+    rlq_quant_weight_128x128(w.data_ptr(), N, K, _ld(w), q.data_ptr(), K, s.data_ptr(), max(K // GRP, 1),
+                             _ptr(qT), N if qT is not None else 0, _stream(stream))
+    return q, s, qT
+
+
+def gemm_fprop(xq, xs, wq, ws, out=None, stream=None):
+    """Y [M, N] bf16 = X W^T from 1x128 X codes and 128x128 W codes."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    rlq_gemm_fprop(xq.data_ptr(), _ld(xq), xs.data_ptr(), _ld(xs), wq.data_ptr(), _ld(wq), ws.data_ptr(), _ld(ws),
+                   y.data_ptr(), _ld(y), M, N, K, _stream(stream))
+    return y
+
+
+def gemm_dgrad(dyq, dys, w, ws, transposed: bool = True, out=None, stream=None):
+    """dX [M, K] bf16 = dY W.  ``w`` is the transposed weight codes [K, N]
+    (``transposed=True``) or the FProp codes [N, K]."""
+    M, N = dyq.shape
+    K = w.shape[0] if transposed else w.shape[1]
+    dx = out if out is not None else torch.empty((M, K), dtype=torch.bfloat16, device=dyq.device)
+    rlq_gemm_dgrad(dyq.data_ptr(), _ld(dyq), dys.data_ptr(), _ld(dys), w.data_ptr(), _ld(w), 1 if transposed else 0,
+                   ws.data_ptr(), _ld(ws), dx.data_ptr(), _ld(dx), M, N, K, _stream(stream))
+    return dx
+
+
+def gemm_wgrad(dyqT, dysc, xqT, xsc, out=None, stream=None):
+    """dW [N, K] bf16 = dY^T X from the 128x1 (transposed) codes of dY and X."""
+    N, M = dyqT.shape
+    K = xqT.shape[0]
+    dw = out if out is not None else torch.empty((N, K), dtype=torch.bfloat16, device=dyqT.device)
+    rlq_gemm_wgrad(dyqT.data_ptr(), _ld(dyqT), dysc.data_ptr(), _ld(dysc), xqT.data_ptr(), _ld(xqT),
+                   xsc.data_ptr(), _ld(xsc), dw.data_ptr(), _ld(dw), M, N, K, _stream(stream))
+    return dw
+
+
+def uaq_fold_(w: torch.Tensor, s: torch.Tensor, prev: torch.Tensor | None = None, stream=None):
+    """In-place UAQ fold: w[:, k] /= s[k], prev[:, k] *= s[k] (bf16, fp32 math)."""
+    N, K = w.shape
+    R = prev.shape[0] if prev is not None else 0
+    rlq_uaq_fold(w.data_ptr(), N, K, _ld(w), s.data_ptr(), _ptr(prev), R, _ld(prev) if prev is not None else 0,
+                 _stream(stream))
+    return w, prev
+
+
+def check(stream=None):
+    """Synchronise the stream and raise RlqError on a recorded device-side timeout."""
+    return rlq_check(_stream(stream))

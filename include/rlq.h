@@ -1,0 +1,202 @@
+/*
+ * rlq.h — C ABI of librlq.so, the GB300 (sm_103a) FP8 quantized actor linear layer.
+ *
+ * The layer, as the pages on quantized RL rollout describe it:
+ *   - fine-grained FP8 quantization: 1x128 per-group scales for activations and
+ *     gradients, 128x128 per-block scales for weights, and a 128x1 grouping of
+ *     the second WGrad operand fused with the first (Jet-RL notes, section
+ *     "细粒度 GEMM 量化方案", Fig. 6);
+ *   - FP8 GEMMs for the three training passes FProp, DGrad and WGrad on those
+ *     operands (same section; DGrad "equivalent to FProp, same configuration");
+ *   - the one-time UAQ invariant-scaling fold WX = (W/s)(sX), s applied per
+ *     column of W and per row of the previous activation (QuRL notes,
+ *     关键设计 §1).
+ *
+ * Conventions for every call
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The library
+ *     never allocates, frees or keeps a pointer after the call returns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and never synchronises, except rlq_check.
+ *   - Row-major storage: element (r, c) of a matrix with row pitch ld sits at
+ *     base[r * ld + c].  All ld arguments count elements, not bytes.
+ *   - bf16 tensors are passed as uint16_t bit patterns (IEEE bfloat16).
+ *   - "Codes" are FP8 E4M3 bytes (OCP "fn" variant: max 448, no infinities).
+ *     Scales are fp32 dequantization multipliers: value ~= decode(code) * scale.
+ *     A group's scale is fl32(amax / 448), or 1.0 when the group is all zero;
+ *     a code is the round-to-nearest-even, saturating E4M3 encoding of
+ *     fl32(x / scale) with IEEE fp32 division.
+ *   - Alignment: every code and bf16 base pointer 16-byte aligned and every
+ *     code / bf16 row pitch a multiple of 16 bytes; fp32 scale pointers 4-byte
+ *     aligned.  Violations return RLQ_ERR_MISALIGNED.
+ *   - Shapes: dimensions that carry 128-groups (K for activations, N and K for
+ *     weights) must be multiples of 128, else RLQ_ERR_UNSUPPORTED.  The token
+ *     dimension M may be any value >= 0.  A call with an empty extent returns
+ *     RLQ_OK and launches nothing.
+ *   - Errors: arguments are validated on the host before any launch (NULL
+ *     pointers, negative sizes, ld smaller than the row, misalignment); on
+ *     failure nothing is launched.  A failed launch returns RLQ_ERR_CUDA.  The
+ *     GEMM kernels bound every wait on the GPU: a wait that runs out records
+ *     an error word on the device, and the next rlq_check on that device
+ *     returns RLQ_ERR_TIMEOUT.  rlq_last_error() describes the latest failure.
+ *   - Inputs must be finite; NaN / Inf inputs are outside the contract.
+ */
+#ifndef RLQ_H
+#define RLQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *rlq_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    RLQ_OK = 0,
+    RLQ_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, ld too small, bad flag */
+    RLQ_ERR_UNSUPPORTED = 2, /* a 128-grouped dimension is not a multiple of 128 */
+    RLQ_ERR_MISALIGNED = 3,  /* pointer or row pitch breaks the alignment rules */
+    RLQ_ERR_CUDA = 4,        /* a CUDA call or launch failed */
+    RLQ_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out (rlq_check) */
+} rlq_status;
+
+/*
+ * Activation / gradient quantization, 1x128 groups along K, with an optional
+ * fused 128x1 grouping along M written transposed (one read of x).
+ * Jet-RL notes, "细粒度 GEMM 量化方案": activations and gradients 1x128 per
+ * group; the second WGrad operand 128x1, fused with the first to avoid
+ * quantizing twice.
+ *
+ *   x   bf16 [M, K], pitch ldx >= K                      (input)
+ *   q   E4M3 [M, K], pitch ldq >= K                      (output) row-wise codes
+ *   s   f32, s[kb * lds + m], kb < K/128, lds >= M       (output) row-wise scales
+ *   qT  E4M3, qT[k * ldqT + m] for k < K, m < M, ldqT >= M  (output, optional)
+ *       column-wise codes: group (mb, k) = rows 128*mb .. min(M, 128*mb+128)-1
+ *       of column k; positions m >= M are not written
+ *   sc  f32, sc[mb * ldsc + k], mb < ceil(M/128), ldsc >= K (output; required
+ *       exactly when qT is non-NULL)
+ * K % 128 == 0.  Either both qT and sc are NULL (row-wise only) or neither.
+ */
+rlq_status rlq_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                               uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                               uint8_t *qT, int64_t ldqT, float *sc, int64_t ldsc,
+                               rlq_stream_t stream);
+
+/*
+ * Weight quantization, 128x128 blocks.  Jet-RL notes, "细粒度 GEMM 量化方案":
+ * weights 128x128 per block; "系统实现": weights are quantized at the
+ * parameter-update step.
+ *
+ *   w   bf16 [N, K], pitch ldw >= K                      (input)
+ *   q   E4M3 [N, K], pitch ldq >= K                      (output)
+ *   s   f32, s[nb * lds + kb], lds >= K/128              (output) block scales
+ *   qT  E4M3 [K, N], pitch ldqT >= N                     (output, optional)
+ *       the same codes transposed, the B operand of DGrad
+ * N % 128 == 0 and K % 128 == 0.
+ */
+rlq_status rlq_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
+                                    uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                                    uint8_t *qT, int64_t ldqT, rlq_stream_t stream);
+
+/*
+ * FProp: Y = X W^T with 1x128 X codes and 128x128 W codes.  Jet-RL notes,
+ * "细粒度 GEMM 量化方案": the FProp input activation is 1x128-quantized
+ * (row-major) and the weight 128x128-quantized.
+ *
+ *   Y[m, n] = bf16_RN( sum_kb xs[kb, m] * ws[n/128, kb] * sum_{k in kb} x[m,k] w[n,k] )
+ *
+ *   xq  E4M3 [M, K], pitch ldxq;   xs f32, xs[kb * ldxs + m], ldxs >= M
+ *   wq  E4M3 [N, K], pitch ldwq;   ws f32, ws[nb * ldws + kb], ldws >= K/128
+ *   y   bf16 [M, N], pitch ldy >= N (output, overwritten)
+ * N % 128 == 0, K % 128 == 0.  Accumulation is fp32 (tensor-core partial sums
+ * of each 128-K block, then the scale product applied in fp32).
+ */
+rlq_status rlq_gemm_fprop(const uint8_t *xq, int64_t ldxq, const float *xs, int64_t ldxs,
+                          const uint8_t *wq, int64_t ldwq, const float *ws, int64_t ldws,
+                          uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                          rlq_stream_t stream);
+
+/*
+ * DGrad: dX = dY W with 1x128 dY codes (groups along N) and the FProp weight
+ * blocks.  Jet-RL notes, "细粒度 GEMM 量化方案": DGrad is equivalent to FProp
+ * and reuses its configuration.
+ *
+ *   dX[m, k] = bf16_RN( sum_nb dys[nb, m] * ws[nb, k/128] * sum_{n in nb} dy[m,n] w[n,k] )
+ *
+ *   dyq  E4M3 [M, N], pitch lddyq; dys f32, dys[nb * lddys + m], lddys >= M
+ *   w    wq_is_transposed = 1: wqT E4M3 [K, N], pitch ldw >= N (from
+ *        rlq_quant_weight_128x128's qT); wq_is_transposed = 0: wq E4M3 [N, K],
+ *        pitch ldw >= K (the FProp operand itself)
+ *   ws   f32 block scales of W as in FProp: ws[nb * ldws + kb], ldws >= K/128
+ *   dx   bf16 [M, K], pitch lddx >= K (output, overwritten)
+ * N % 128 == 0, K % 128 == 0.
+ */
+rlq_status rlq_gemm_dgrad(const uint8_t *dyq, int64_t lddyq, const float *dys, int64_t lddys,
+                          const uint8_t *w, int64_t ldw, int wq_is_transposed,
+                          const float *ws, int64_t ldws, uint16_t *dx, int64_t lddx,
+                          int64_t M, int64_t N, int64_t K, rlq_stream_t stream);
+
+/*
+ * WGrad: dW = dY^T X with 128x1 groups along the M tokens on both operands
+ * (the transposed outputs of rlq_quant_act_1x128).  Jet-RL notes,
+ * "细粒度 GEMM 量化方案": WGrad takes a 1x128 first operand and a 128x1 second
+ * operand; here both are grouped along the contraction (token) dimension,
+ * which is what a 128-block promotion over the contraction needs.
+ *
+ *   dW[n, k] = bf16_RN( sum_mb dysc[mb, n] * xsc[mb, k] * sum_{m in mb} dy[m,n] x[m,k] )
+ *
+ *   dyqT E4M3, dyqT[n * lddyqT + m], lddyqT >= M; dysc f32, dysc[mb * lddysc + n], lddysc >= N
+ *   xqT  E4M3, xqT[k * ldxqT + m],  ldxqT >= M;  xsc f32, xsc[mb * ldxsc + k],  ldxsc >= K,
+ *        xsc 16-byte aligned and ldxsc % 4 == 0 (its rows are copied to shared memory in bulk)
+ *   dw   bf16 [N, K], pitch lddw >= K (output, overwritten; M == 0 writes zeros)
+ * N % 128 == 0, K % 128 == 0; the last token block may be partial.
+ */
+rlq_status rlq_gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, int64_t lddysc,
+                          const uint8_t *xqT, int64_t ldxqT, const float *xsc, int64_t ldxsc,
+                          uint16_t *dw, int64_t lddw, int64_t M, int64_t N, int64_t K,
+                          rlq_stream_t stream);
+
+/*
+ * UAQ invariant-scaling fold, in place.  QuRL notes, 关键设计 §1: WX = (W/s)(sX)
+ * with s > 1 applied per column of W and per row of the previous activation
+ * (foldable into a LayerNorm / RMSNorm scale); run once before RL.
+ *
+ *   w     bf16 [N, K], pitch ldw >= K: w[n,k] <- bf16_RN(fl32(w[n,k] / s[k]))
+ *   s     f32 [K], 16-byte aligned, every entry > 0 and finite (not checked on the device)
+ *   prev  bf16 [R, K], pitch ldp >= K, nullable: prev[r,k] <- bf16_RN(fl32(prev[r,k] * s[k]))
+ *         (the previous activation, R = M rows, or a norm weight, R = 1)
+ * K % 8 == 0 (16-byte vectors); w / prev 16-byte aligned with pitches % 8 == 0.
+ */
+rlq_status rlq_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, const float *s,
+                        uint16_t *prev, int64_t R, int64_t ldp, rlq_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns RLQ_ERR_TIMEOUT if a bounded wait ran out in an
+ * earlier launch, RLQ_ERR_CUDA if CUDA reports an error, else RLQ_OK.
+ */
+rlq_status rlq_check(rlq_stream_t stream);
+
+/*
+ * Diagnostic for the bounded-wait machinery: launches one CTA that waits on a
+ * barrier nothing will ever arrive on, for at most timeout_us microseconds
+ * (1 .. 10^7), then records a timeout and exits.  The following rlq_check
+ * returns RLQ_ERR_TIMEOUT and the context stays usable.
+ */
+rlq_status rlq_diag_bounded_wait(int64_t timeout_us, rlq_stream_t stream);
+
+/* Static description of a status code. */
+const char *rlq_status_string(rlq_status status);
+
+/* Description of the latest failure in the calling thread ("" if none). */
+const char *rlq_last_error(void);
+
+/* Library version, "major.minor.patch". */
+const char *rlq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLQ_H */

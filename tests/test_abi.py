@@ -1,0 +1,103 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+entry point that include/rlq.h declares, and host-side validation returns the
+documented status codes before anything is launched (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp8_block_scaled_quantize_gb300 import rlq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rlq.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rlq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for n in ("rlq_quant_act_1x128", "rlq_quant_weight_128x128", "rlq_gemm_fprop", "rlq_gemm_dgrad",
+              "rlq_gemm_wgrad", "rlq_uaq_fold", "rlq_check", "rlq_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = rlq.lib()
+    for n in declared_functions():
+        assert hasattr(L, n), f"librlq.so does not export {n}"
+    assert rlq.rlq_version().count(".") == 2
+
+
+def test_status_strings():
+    for code, name in rlq.STATUS.items():
+        assert rlq.rlq_status_string(code).startswith(name)
+    assert "unknown" in rlq.rlq_status_string(99)
+
+
+FAKE = 0x10000  # an aligned fake device address: validation never dereferences it
+
+
+def _status(fn, *args):
+    try:
+        fn(*args)
+        return 0
+    except rlq.RlqError as e:
+        return e.status
+
+
+def test_quant_act_validation():
+    q = rlq.rlq_quant_act_1x128
+    assert _status(q, FAKE, 4, 100, 128, FAKE, 128, FAKE, 4, None, 0, None, 0, None) == 2  # K % 128
+    assert _status(q, FAKE, -1, 128, 128, FAKE, 128, FAKE, 4, None, 0, None, 0, None) == 1
+    assert _status(q, None, 4, 128, 128, FAKE, 128, FAKE, 4, None, 0, None, 0, None) == 1  # NULL x
+    assert _status(q, FAKE, 4, 128, 64, FAKE, 128, FAKE, 4, None, 0, None, 0, None) == 1   # ldx < K
+    assert _status(q, FAKE, 4, 128, 128, FAKE, 128, FAKE, 3, None, 0, None, 0, None) == 1  # lds < M
+    assert _status(q, FAKE + 8, 4, 128, 128, FAKE, 128, FAKE, 4, None, 0, None, 0, None) == 3
+    assert _status(q, FAKE, 4, 128, 132, FAKE, 128, FAKE, 4, None, 0, None, 0, None) == 3  # ldx % 8
+    assert _status(q, FAKE, 4, 128, 128, FAKE, 136, FAKE, 4, None, 0, None, 0, None) == 3  # ldq % 16
+    assert _status(q, FAKE, 4, 128, 128, FAKE, 128, FAKE, 4, FAKE, 16, None, 0, None) == 1  # qT without sc
+    assert _status(q, FAKE, 4, 128, 128, FAKE, 128, FAKE, 4, FAKE, 8, FAKE, 128, None) == 3  # ldqT % 16
+    assert "qT" in rlq.rlq_last_error()
+    assert _status(q, FAKE, 40, 128, 128, FAKE, 128, FAKE, 40, FAKE, 32, FAKE, 128, None) == 1  # ldqT < M
+    assert _status(q, FAKE, 4, 128, 128, FAKE, 128, FAKE, 4, FAKE, 16, FAKE, 64, None) == 1  # ldsc < K
+    # empty extents are a no-op success without touching the pointers
+    assert _status(q, None, 0, 128, 128, None, 128, None, 0, None, 0, None, 0, None) == 0
+    assert _status(q, None, 5, 0, 0, None, 0, None, 0, None, 0, None, 0, None) == 0
+
+
+def test_weight_and_fold_validation():
+    w = rlq.rlq_quant_weight_128x128
+    assert _status(w, FAKE, 100, 128, 128, FAKE, 128, FAKE, 1, None, 0, None) == 2
+    assert _status(w, FAKE, 128, 256, 256, FAKE, 256, FAKE, 1, None, 0, None) == 1  # lds < K/128
+    assert _status(w, FAKE, 128, 128, 128, FAKE, 128, FAKE, 1, FAKE, 64, None) == 1  # ldqT < N
+    f = rlq.rlq_uaq_fold
+    assert _status(f, FAKE, 4, 12, 16, FAKE, None, 0, 0, None) == 2  # K % 8
+    assert _status(f, FAKE, 4, 16, 16, None, None, 0, 0, None) == 1  # s NULL
+    assert _status(f, FAKE, 4, 16, 16, FAKE + 4, None, 0, 0, None) == 3  # s alignment
+    assert _status(f, None, 0, 16, 16, None, None, 0, 0, None) == 0
+
+
+def test_gemm_validation():
+    fp = rlq.rlq_gemm_fprop
+    assert _status(fp, FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 1, FAKE, 136, 4, 130, 128, None) == 2  # N % 128
+    assert _status(fp, FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 1, FAKE, 128, 4, 128, 100, None) == 2  # K % 128
+    assert _status(fp, FAKE, 120, FAKE, 4, FAKE, 128, FAKE, 1, FAKE, 128, 4, 128, 128, None) == 1  # ldxq < K
+    assert _status(fp, FAKE, 144, FAKE, 4, FAKE + 1, 128, FAKE, 1, FAKE, 128, 4, 128, 128, None) == 3
+    assert _status(fp, FAKE, 128, FAKE, 3, FAKE, 128, FAKE, 1, FAKE, 128, 4, 128, 128, None) == 1  # ldxs < M
+    assert _status(fp, None, 0, None, 0, None, 0, None, 0, None, 0, 0, 128, 128, None) == 0  # M == 0
+    dg = rlq.rlq_gemm_dgrad
+    assert _status(dg, FAKE, 128, FAKE, 4, FAKE, 128, 2, FAKE, 1, FAKE, 128, 4, 128, 128, None) == 1
+    wg = rlq.rlq_gemm_wgrad
+    # column scales of X must be 16-byte aligned rows
+    assert _status(wg, FAKE, 16, FAKE, 128, FAKE, 16, FAKE + 4, 128, FAKE, 128, 4, 128, 128, None) == 3
+    assert _status(wg, FAKE, 16, FAKE, 128, FAKE, 16, FAKE, 130, FAKE, 128, 4, 128, 128, None) == 3
+
+
+def test_diag_validation():
+    assert _status(rlq.rlq_diag_bounded_wait, 0, None) == 1
+    assert _status(rlq.rlq_diag_bounded_wait, 10 ** 8, None) == 1
