@@ -1,0 +1,473 @@
+"""Benchmark of the FP8 quantized actor linear layer on GB300.
+
+One step = one pass of the whole hot path over the 8B-shaped training
+workload (X bf16 [8192, 4096], W bf16 [14336, 4096], dY bf16 [8192, 14336]):
+
+  1. UAQ fold of W and of a norm weight (R = 1), in place
+     (the channel scale alternates between s and 1/s so W stays stationary)
+  2. fused 1x128 + 128x1 quantization of X
+  3. fused 1x128 + 128x1 quantization of dY
+  4. 128x128 quantization of W, with the transposed copy for DGrad
+  5. FProp  Y  = X W^T
+  6. DGrad  dX = dY W
+  7. WGrad  dW = dY^T X
+
+Every step launches only this library's kernels (8 launches).  L2 is flushed
+(a 256 MB device write, outside the timed events) before every step; each
+step is timed with CUDA events on the launching stream, per kernel and whole.
+
+``value`` is the step's GEMM throughput, 3 * 2*M*N*K FLOP / step time, so the
+quantizers and the fold count against it.  Per-kernel TFLOP/s and GB/s, each
+against its roofline, are in ``kernels``.  ``e2e`` repeats the step through
+host buffers (pinned host -> device copies of X, W, dY; device -> host copies of
+Y, dX, dW inside the timed region).  ``cpu_baseline`` and ``--impl reference``
+time the test oracle (plain C + NumPy fp64) on the host cores over a bounded
+sample of the same workload.
+
+Multi-GPU: the path has no exchange step, so N GPUs run N independent replicas
+("weak" scaling): value = total FLOP over all ranks / max step time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+M_, N_, K_ = 8192, 14336, 4096
+WORKLOAD = "8B-shaped training step (Llama-3.1-8B MLP up-proj): fold + quant X/dY/W + FProp/DGrad/WGrad"
+METRIC = "FP8 block-scaled GEMM TFLOPS & % FP8 peak; quantizer GB/s & % of HBM BW"
+UAQ_S = 1.5  # QuRL's recommended fold factor
+
+# algorithmic bytes per element
+B_DUAL = 2 + 1 + 1 + 4 / 128 + 4 / 128
+B_WEIGHT_T = 2 + 1 + 1 + 4 / 16384
+B_FOLD_W = 4  # read + write bf16 per weight element
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_burst": p["bf16_tflops"],
+                "bf16_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_burst": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- dist ---
+
+def _dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return dist, rank, world, local
+    return None, 0, 1, local
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- step ---
+
+class Step:
+    """Device buffers and the launch sequence of one step."""
+
+    def __init__(self, dev, host):
+        from fp8_block_scaled_quantize_gb300 import rlq
+        self.rlq = rlq
+        M, N, K = M_, N_, K_
+        self.dev = dev
+        bf = torch.bfloat16
+        self.x = torch.empty((M, K), dtype=bf, device=dev)
+        self.w = torch.empty((N, K), dtype=bf, device=dev)
+        self.dy = torch.empty((M, N), dtype=bf, device=dev)
+        self.gamma = torch.ones((1, K), dtype=bf, device=dev)
+        self.s_fwd = torch.full((K,), UAQ_S, dtype=torch.float32, device=dev)
+        self.s_bwd = torch.full((K,), 1.0 / UAQ_S, dtype=torch.float32, device=dev)
+        u8, f32 = torch.uint8, torch.float32
+        self.qx = torch.empty((M, K), dtype=u8, device=dev)
+        self.sx = torch.empty((K // 128, M), dtype=f32, device=dev)
+        self.qxT = torch.empty((K, M), dtype=u8, device=dev)
+        self.sxc = torch.empty((M // 128, K), dtype=f32, device=dev)
+        self.qdy = torch.empty((M, N), dtype=u8, device=dev)
+        self.sdy = torch.empty((N // 128, M), dtype=f32, device=dev)
+        self.qdyT = torch.empty((N, M), dtype=u8, device=dev)
+        self.sdyc = torch.empty((M // 128, N), dtype=f32, device=dev)
+        self.qw = torch.empty((N, K), dtype=u8, device=dev)
+        self.sw = torch.empty((N // 128, K // 128), dtype=f32, device=dev)
+        self.qwT = torch.empty((K, N), dtype=u8, device=dev)
+        self.y = torch.empty((M, N), dtype=bf, device=dev)
+        self.dx = torch.empty((M, K), dtype=bf, device=dev)
+        self.dw = torch.empty((N, K), dtype=bf, device=dev)
+        self.x.copy_(host["x"])
+        self.w.copy_(host["w"])
+        self.dy.copy_(host["dy"])
+        self.parity = 0
+        self.launches_per_step = 8
+
+    def run(self, stream: int, events=None):
+        """Launch the step; if `events` (8 CUDA events) is given, record them
+        around the kernels."""
+        r = self.rlq
+        M, N, K = M_, N_, K_
+        s = self.s_fwd if self.parity == 0 else self.s_bwd
+        self.parity ^= 1
+        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
+        rec(0)
+        r.rlq_uaq_fold(self.w.data_ptr(), N, K, K, s.data_ptr(), self.gamma.data_ptr(), 1, K, stream)
+        rec(1)
+        r.rlq_quant_act_1x128(self.x.data_ptr(), M, K, K, self.qx.data_ptr(), K, self.sx.data_ptr(), M,
+                              self.qxT.data_ptr(), M, self.sxc.data_ptr(), K, stream)
+        rec(2)
+        r.rlq_quant_act_1x128(self.dy.data_ptr(), M, N, N, self.qdy.data_ptr(), N, self.sdy.data_ptr(), M,
+                              self.qdyT.data_ptr(), M, self.sdyc.data_ptr(), N, stream)
+        rec(3)
+        r.rlq_quant_weight_128x128(self.w.data_ptr(), N, K, K, self.qw.data_ptr(), K, self.sw.data_ptr(), K // 128,
+                                   self.qwT.data_ptr(), N, stream)
+        rec(4)
+        r.rlq_gemm_fprop(self.qx.data_ptr(), K, self.sx.data_ptr(), M, self.qw.data_ptr(), K, self.sw.data_ptr(),
+                         K // 128, self.y.data_ptr(), N, M, N, K, stream)
+        rec(5)
+        r.rlq_gemm_dgrad(self.qdy.data_ptr(), N, self.sdy.data_ptr(), M, self.qwT.data_ptr(), N, 1,
+                         self.sw.data_ptr(), K // 128, self.dx.data_ptr(), K, M, N, K, stream)
+        rec(6)
+        r.rlq_gemm_wgrad(self.qdyT.data_ptr(), M, self.sdyc.data_ptr(), N, self.qxT.data_ptr(), M,
+                         self.sxc.data_ptr(), K, self.dw.data_ptr(), K, M, N, K, stream)
+        rec(7)
+
+
+KERNELS = ["uaq_fold", "quant_dual_x", "quant_dual_dy", "quant_weight_128x128", "gemm_fprop", "gemm_dgrad",
+           "gemm_wgrad"]
+
+
+def kernel_work():
+    """Algorithmic work per launch: ("bytes", B) or ("flop", F)."""
+    M, N, K = M_, N_, K_
+    return {
+        "uaq_fold": ("bytes", B_FOLD_W * N * K + 4 * K + 4 * K),
+        "quant_dual_x": ("bytes", B_DUAL * M * K),
+        "quant_dual_dy": ("bytes", B_DUAL * M * N),
+        "quant_weight_128x128": ("bytes", B_WEIGHT_T * N * K),
+        "gemm_fprop": ("flop", 2.0 * M * N * K),
+        "gemm_dgrad": ("flop", 2.0 * M * N * K),
+        "gemm_wgrad": ("flop", 2.0 * M * N * K),
+    }
+
+
+def make_host_inputs():
+    from fp8_block_scaled_quantize_gb300 import inputs as I
+    d = I.train_step_8b()
+    return {k: I.to_torch(v) for k, v in d.items()}
+
+
+def run_ours(args):
+    from fp8_block_scaled_quantize_gb300 import rlq
+
+    dist, rank, world, local = _dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rlq.lib()
+    peaks = _peaks()
+    host = make_host_inputs()
+    st = Step(dev, host)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size if hasattr(torch.cuda.get_device_properties(dev), "L2_cache_size") else 128 << 20
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        st.run(sh)
+    rlq.check(sh)
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    _barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()  # outside the timed events
+            st.run(sh, evs[i])
+        torch.cuda.synchronize()
+    _barrier(dist)
+    rlq.check(sh)
+
+    per_kernel = {k: [] for k in KERNELS}
+    step_ms = []
+    for e in evs:
+        for j, k in enumerate(KERNELS):
+            per_kernel[k].append(e[j].elapsed_time(e[j + 1]))
+        step_ms.append(e[0].elapsed_time(e[7]))
+    ms = statistics.mean(step_ms)
+    ms_max = _max_over_ranks(dist, ms)
+    flop_step = 3 * 2.0 * M_ * N_ * K_
+    value = world * flop_step / (ms_max * 1e-3) / 1e12
+
+    fp8_peak = 2.0 * peaks["bf16_sustained"]  # dense FP8 = 2 x dense bf16 (nominal 4.5 / 2.25 PF)
+    kern = {}
+    for k, (kind, amount) in kernel_work().items():
+        t = statistics.mean(per_kernel[k])
+        if kind == "flop":
+            a = amount / (t * 1e-3) / 1e12
+            kern[k] = {"ms": round(t, 4), "tflops": round(a, 1), "frac_fp8_peak": round(a / fp8_peak, 3)}
+        else:
+            a = amount / (t * 1e-3) / 1e9
+            kern[k] = {"ms": round(t, 4), "gbs": round(a, 1), "frac_hbm": round(a / peaks["hbm_gbs"], 3)}
+    dom = max(KERNELS, key=lambda k: statistics.mean(per_kernel[k]))
+    dkind, damount = kernel_work()[dom]
+    dt = statistics.mean(per_kernel[dom])
+    traffic = _load_traffic(dom)
+    if dkind == "flop":
+        ach = damount / (dt * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 3), "traffic": traffic,
+                "peak_source": f"{peaks['source']}: 2 x bf16 sustained {peaks['bf16_sustained']} TFLOP/s"}
+    else:
+        ach = damount / (dt * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 3), "traffic": traffic, "peak_source": peaks["source"]}
+
+    e2e = run_e2e(st, host, args, dist, world, flop_step)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_rows, args.cpu_cols, {k: v.view(torch.int16).numpy().view(np.uint16)
+                                                          for k, v in host.items()})
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 (bf16 in/out)", "data": "synthetic (seeded N(0,1) X, "
+            "N(0,0.02) W, N(0,1e-3) dY; no weights or datasets)",
+            "config": {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "uaq_s": UAQ_S,
+                       "l2": "flushed before every step (256 MB device write outside the timed events)",
+                       "parallelism": f"{world} independent replica(s)"},
+            "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": st.launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _load_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel version (else null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    v = t.get(kernel)
+    return v.get("dram_bytes_per_launch") if isinstance(v, dict) and v.get("current", False) else None
+
+
+def run_e2e(st: Step, host, args, dist, world, flop_step):
+    """The same step through host buffers: H2D of X, W, dY from pinned memory,
+    the step, D2H of Y, dX, dW into pinned memory, all inside the timed region."""
+    pin = {k: v.pin_memory() for k, v in host.items()}
+    outs = {"y": torch.empty(st.y.shape, dtype=torch.bfloat16).pin_memory(),
+            "dx": torch.empty(st.dx.shape, dtype=torch.bfloat16).pin_memory(),
+            "dw": torch.empty(st.dw.shape, dtype=torch.bfloat16).pin_memory()}
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def one():
+        st.x.copy_(pin["x"], non_blocking=True)
+        st.w.copy_(pin["w"], non_blocking=True)
+        st.dy.copy_(pin["dy"], non_blocking=True)
+        st.run(sh)
+        outs["y"].copy_(st.y, non_blocking=True)
+        outs["dx"].copy_(st.dx, non_blocking=True)
+        outs["dw"].copy_(st.dw, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        one()
+    torch.cuda.synchronize()
+    n = max(2, args.steps // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(dist)
+    e0.record()
+    for _ in range(n):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = _max_over_ranks(dist, e0.elapsed_time(e1) / n)
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    return {"value": round(world * flop_step / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+# ------------------------------------------------------------------ CPU ---
+
+def cpu_baseline(rows: int, cols: int, data=None):
+    """The oracle as it stands, on a bounded sample of the same workload: the
+    sub-problem of `rows` tokens and `cols` output channels.  It folds and
+    128x128-quantizes W[:cols], quantizes X[:rows] and dY[:rows, :cols]
+    (1x128 and 128x1), and computes Y[:rows, :cols], the dX[:rows] contribution
+    of those channels, and dW[:cols] over those tokens: 6 * rows * cols * K FLOP.
+    Returns throughput in the GPU line's unit (GEMM TFLOP/s over the sample,
+    quantization and dequantization time included)."""
+    import oracle
+    from fp8_block_scaled_quantize_gb300 import inputs as I
+
+    oracle.build()
+    K = K_
+    rows = max(128, rows // 128 * 128)
+    cols = max(128, cols // 128 * 128)
+    d = data if data is not None else I.train_step_8b()
+    x = np.ascontiguousarray(d["x"][:rows])
+    w = np.ascontiguousarray(d["w"][:cols])
+    dy = np.ascontiguousarray(d["dy"][:rows, :cols])
+    s = np.full(K, UAQ_S, np.float32)
+    t0 = time.perf_counter()
+    w_f, _ = oracle.uaq_fold(w, s)
+    qw, sw, _ = oracle.quant_weight_128x128(w_f)
+    qx, sx = oracle.quant_rows_1x128(x)
+    qdy, sdy = oracle.quant_rows_1x128(dy)
+    qxT, sxc = oracle.quant_cols_128x1(x)
+    qdyT, sdyc = oracle.quant_cols_128x1(dy)
+    oracle.gemm_fprop(qx, sx, qw, sw)
+    oracle.gemm_dgrad(qdy, sdy, qw, sw)
+    oracle.gemm_wgrad(qdyT, sdyc, qxT, sxc)
+    dt = time.perf_counter() - t0
+    flop = 6.0 * rows * cols * K
+    return {"value": round(flop / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"sub-problem of {rows} tokens x {cols} output channels of the [{M_},{N_},{K_}] step: fold and "
+                      f"128x128 quant of W[:{cols}], 1x128 + 128x1 quant of X[:{rows}] and dY[:{rows},:{cols}], "
+                      f"FProp / DGrad / WGrad restricted to it (C with OpenMP + NumPy fp64)"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle timed on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from fp8_block_scaled_quantize_gb300 import inputs as I
+    data = I.train_step_8b()
+    steps = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(args.ref_rows, args.ref_cols, data)
+        if i >= args.warmup:
+            steps.append(r)
+    val = statistics.mean(r["value"] for r in steps)
+    sec = statistics.mean(r["seconds"] for r in steps)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "sample_rows": args.ref_rows,
+                       "sample_cols": args.ref_cols},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": steps[-1]["cores"], "kind": "oracle",
+                             "sample": steps[-1]["sample"]},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--cpu-cols", type=int, default=14336)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--ref-cols", type=int, default=1024)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -20,6 +20,13 @@
 //     by sa * sb and accumulate into fp32 registers (packed f32x2 FMA), release
 //     the TMEM buffer, and after the last block round to bf16 and store.
 //
+// The scales are read by the epilogue straight from global memory, two blocks
+// ahead of use (per-row / per-block scales into registers; WGrad's per-column
+// scale rows through an L1 prefetch and broadcast loads).  They are not staged
+// through the shared-memory ring: generic-proxy reads of a buffer that the
+// async proxy (TMA) rewrites are not ordered by the stage barriers alone, and
+// a ring-staged variant measured non-deterministic.
+//
 // Tiles are 128 x 256; the kernel is persistent (one CTA per SM) and walks
 // the tile list with the smaller operand resident in L2.  Every mbarrier wait
 // is bounded: on timeout the waiting thread records an error word that
@@ -59,9 +66,8 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int REGS_PRODUCER = 40;
 constexpr int REGS_EPILOGUE = 232;
 constexpr int TMEM_COLS = 2 * BN;          // two partial buffers
-constexpr int SBCOL_BYTES = STAGES * BN * 4;
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + SBCOL_BYTES + NUM_BARS * 8 + 16;
+constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1),
 // A and B E4M3 (format 0 in bits 7-9 / 10-12), both K-major (bits 15/16 = 0),
@@ -158,11 +164,9 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+__device__ __forceinline__ void prefetch_l1(const void *p)
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
@@ -188,20 +192,34 @@ __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes, waited for.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+// Issues a load of 32 consecutive fp32 columns of this warp's 32 TMEM lanes
+// into r; the registers are valid only after tmem_wait32(r).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32])
 {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
+}
+
+// Waits for the outstanding TMEM loads.  The registers of r are tied to the
+// wait as in/out operands so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_wait32(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
@@ -237,6 +255,31 @@ __device__ __forceinline__ void reg_fence16(uint64_t *a)
     asm volatile(""
                  : "+l"(a[0]), "+l"(a[1]), "+l"(a[2]), "+l"(a[3]), "+l"(a[4]), "+l"(a[5]), "+l"(a[6]), "+l"(a[7]),
                    "+l"(a[8]), "+l"(a[9]), "+l"(a[10]), "+l"(a[11]), "+l"(a[12]), "+l"(a[13]), "+l"(a[14]), "+l"(a[15]));
+}
+
+// acc[0..15] += chunk * scale (one scale for the whole chunk).
+__device__ __forceinline__ void promote_chunk(uint64_t *acc, const uint32_t (&r)[32], uint64_t scl2)
+{
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        ffma2(acc[j], f2_bits(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), scl2);
+    reg_fence16(acc);
+}
+
+// acc[0..15] += chunk * sa * sb[column]; sb is 32 consecutive column scales in
+// global memory, read by every lane (broadcast).
+__device__ __forceinline__ void promote_chunk_cols(uint64_t *acc, const uint32_t (&r)[32], uint64_t sa2,
+                                                   const float4 *sbs)
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float4 sb4 = __ldg(sbs + j);
+        const uint64_t s01 = fmul2(sa2, f2_bits(sb4.x, sb4.y));
+        const uint64_t s23 = fmul2(sa2, f2_bits(sb4.z, sb4.w));
+        ffma2(acc[2 * j], f2_bits(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), s01);
+        ffma2(acc[2 * j + 1], f2_bits(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), s23);
+    }
+    reg_fence16(acc);
 }
 
 __device__ __forceinline__ uint32_t bf16x2_rn(uint64_t v)
@@ -279,8 +322,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *sbcol = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + SBCOL_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -297,9 +339,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            // the stage is free once its MMAs completed and, when B carries
-            // per-column scales, once every epilogue warp has read them
-            mbar_init(empty_bar(s), 1 + (kColScaleB ? NUM_EPI_WARPS : 0));
+            mbar_init(empty_bar(s), 1);  // the stage is free once its MMAs completed
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -335,11 +375,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 int mt, nt;
                 tile_coords(p, tile, mt, nt);
-                uint32_t sb_bytes = 0;
-                if (kColScaleB) {
-                    const int cols = p.C - nt * BN;
-                    sb_bytes = (uint32_t)((cols < BN ? cols : BN) * 4);
-                }
                 for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
@@ -347,12 +382,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES + sb_bytes);
+                    mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
                     tma_load_2d(a_stage(s), &tmA, full_bar(s), kb * BK, mt * BM);
                     tma_load_2d(b_stage(s), &tmB, full_bar(s), kb * BK, nt * BN);
-                    if (kColScaleB)
-                        bulk_load(smem_u32(sbcol + s * BN), p.sb + (int64_t)kb * p.sb_bstride + (int64_t)nt * BN,
-                                  sb_bytes, full_bar(s));
                 }
             }
             if (!ok) {
@@ -399,9 +431,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp >= FIRST_EPI_WARP) {
         // --------------------------------------------------- epilogue ---
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPILOGUE));
-        const int q = warp & 3;              // TMEM lane quarter this warp may access
+        const int q = warp & 3;                      // TMEM lane quarter this warp may access
         const int h = (warp - FIRST_EPI_WARP) >> 2;  // column half of the tile
-        const int row = q * 32 + lane;       // tile row = TMEM lane
+        const int row = q * 32 + lane;               // tile row = TMEM lane
+
+        // The block scales are fetched two contraction blocks ahead (crossing
+        // tile boundaries) so that their global-memory latency stays hidden.
+        int pf_tile = blockIdx.x, pf_kb = 0;
+        auto fetch = [&](float &sa_o, float &sb_o) {
+            sa_o = 0.0f;
+            sb_o = 0.0f;
+            if (pf_tile < p.num_tiles) {
+                int mt, nt;
+                tile_coords(p, pf_tile, mt, nt);
+                const int grow = mt * BM + row;
+                if (grow < p.R)
+                    sa_o = __ldg(p.sa + (int64_t)pf_kb * p.ld_sa + grow);
+                const int col0 = nt * BN + h * 128;
+                if (!kColScaleB) {
+                    if (col0 < p.C)
+                        sb_o = __ldg(p.sb + (int64_t)pf_kb * p.sb_bstride + (int64_t)(col0 >> 7) * p.sb_cstride);
+                } else if (col0 < p.C && lane < 4) {
+                    // the warp's 128 column scales: four 128-byte lines
+                    prefetch_l1(p.sb + (int64_t)pf_kb * p.sb_bstride + col0 + lane * 32);
+                }
+                if (++pf_kb == p.kblocks) {
+                    pf_kb = 0;
+                    pf_tile += gridDim.x;
+                }
+            }
+        };
+        float sa0, sb0, sa1, sb1, sa2, sb2;
+        fetch(sa0, sb0);
+        fetch(sa1, sb1);
+
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
@@ -418,59 +481,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                 const int buf = it & 1;
                 const uint32_t bph = (uint32_t)(it >> 1) & 1u;
-                const float sa = row_ok ? __ldg(p.sa + (int64_t)kb * p.ld_sa + grow) : 0.0f;
-                float sbk = 0.0f;
-                if (!kColScaleB && half_ok)
-                    sbk = __ldg(p.sb + (int64_t)kb * p.sb_bstride + (int64_t)(col0 >> 7) * p.sb_cstride);
-                // one lane waits; the decision must be warp-uniform because
-                // tcgen05.ld below is a .sync.aligned warp instruction
-                int waited = 1;
-                if (lane == 0)
-                    waited = mbar_wait(tfull_bar(buf), bph, abort_flag, p.timeout_ns, SITE_EPI_TMEM_FULL) ? 1 : 0;
-                if (!__shfl_sync(0xFFFFFFFFu, waited, 0)) {
+                fetch(sa2, sb2);
+                // every lane acquires the partial itself; the decision is made
+                // warp-uniform because tcgen05.ld is a .sync.aligned instruction
+                const bool w = mbar_wait(tfull_bar(buf), bph, abort_flag, p.timeout_ns, SITE_EPI_TMEM_FULL);
+                if (!__all_sync(0xFFFFFFFFu, w)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
+                uint32_t ra[32], rb[32];
                 if (!kColScaleB) {
-                    const float scl = sa * sbk;
+                    const float scl = sa0 * sb0;
                     const uint64_t scl2 = f2_bits(scl, scl);
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t r[32];
-                        tmem_ld32(taddr + ch * 32, r);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            ffma2(acc[ch * 16 + j], f2_bits(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), scl2);
-                        reg_fence16(&acc[ch * 16]);
-                    }
+                    tmem_ld32_async(taddr, ra);
+                    tmem_wait32(ra);
+                    tmem_ld32_async(taddr + 32, rb);
+                    promote_chunk(&acc[0], ra, scl2);
+                    tmem_wait32(rb);
+                    tmem_ld32_async(taddr + 64, ra);
+                    promote_chunk(&acc[16], rb, scl2);
+                    tmem_wait32(ra);
+                    tmem_ld32_async(taddr + 96, rb);
+                    promote_chunk(&acc[32], ra, scl2);
+                    tmem_wait32(rb);
+                    promote_chunk(&acc[48], rb, scl2);
                 } else {
-                    const int s = it % STAGES;
-                    const float4 *sbs = reinterpret_cast<const float4 *>(sbcol + s * BN + h * 128);
-                    const uint64_t sa2 = f2_bits(sa, sa);
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t r[32];
-                        tmem_ld32(taddr + ch * 32, r);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 sb4 = sbs[ch * 8 + j];
-                            const uint64_t s01 = fmul2(sa2, f2_bits(sb4.x, sb4.y));
-                            const uint64_t s23 = fmul2(sa2, f2_bits(sb4.z, sb4.w));
-                            ffma2(acc[ch * 16 + 2 * j], f2_bits(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), s01);
-                            ffma2(acc[ch * 16 + 2 * j + 1], f2_bits(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), s23);
-                        }
-                        reg_fence16(&acc[ch * 16]);
-                    }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(empty_bar(s));
+                    const float4 *sbs = reinterpret_cast<const float4 *>(
+                        p.sb + (int64_t)kb * p.sb_bstride + (half_ok ? col0 : 0));
+                    const uint64_t sa2v = f2_bits(sa0, sa0);
+                    tmem_ld32_async(taddr, ra);
+                    tmem_wait32(ra);
+                    tmem_ld32_async(taddr + 32, rb);
+                    promote_chunk_cols(&acc[0], ra, sa2v, sbs);
+                    tmem_wait32(rb);
+                    tmem_ld32_async(taddr + 64, ra);
+                    promote_chunk_cols(&acc[16], rb, sa2v, sbs + 8);
+                    tmem_wait32(ra);
+                    tmem_ld32_async(taddr + 96, rb);
+                    promote_chunk_cols(&acc[32], ra, sa2v, sbs + 16);
+                    tmem_wait32(rb);
+                    promote_chunk_cols(&acc[48], rb, sa2v, sbs + 24);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(tempty_bar(buf));
+                sa0 = sa1;
+                sb0 = sb1;
+                sa1 = sa2;
+                sb1 = sb2;
             }
             if (ok && row_ok && half_ok) {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.out + (int64_t)grow * p.ldo + col0);
