@@ -191,14 +191,12 @@ rlq_status rlq_gemm_dgrad(const uint8_t *dyq, int64_t lddyq, const float *dys, i
         else
             RLQ_TRY(check_codes("wq", w, ldw, K));
     }
-    RLQ_REQUIRE(wq_is_transposed == 1, RLQ_ERR_UNSUPPORTED,
-                "DGrad on the untransposed weight codes is not built in this version: "
-                "pass the transposed codes from rlq_quant_weight_128x128 (wq_is_transposed = 1)");
     GemmArgs a{};
     a.A = dyq;
     a.lda = lddyq;
-    a.B = w;  // wqT [K rows][N]: output column k, contraction n
+    a.B = w;  // wqT [K rows][N] (output column k, contraction n), or wq [N rows][K] read MN-major
     a.ldb = ldw;
+    a.b_mn_major = (wq_is_transposed == 0);
     a.sa = dys;
     a.ld_sa = lddys;
     a.sb = ws;             // scale of contraction block nb, output block kb: ws[nb * ldws + kb]

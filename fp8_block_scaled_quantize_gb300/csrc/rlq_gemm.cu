@@ -12,20 +12,24 @@
 // per-128 scales, so the scaling ("promotion") is done in software:
 //
 //   * a TMA warp streams 128x128 A tiles and 256x128 B tiles (128-byte swizzle)
-//     into a 4-stage shared-memory ring guarded by mbarriers;
+//     into a 3-stage shared-memory ring guarded by mbarriers;
 //   * an MMA warp issues, per contraction block, four tcgen05.mma
 //     (kind::f8f6f4, M=128, N=256, K=32) into one of two TMEM partial buffers
 //     (2 x 256 fp32 columns = the whole 512-column TMEM), then commits;
 //   * eight epilogue warps read the finished partial with tcgen05.ld, multiply
 //     by sa * sb and accumulate into fp32 registers (packed f32x2 FMA), release
-//     the TMEM buffer, and after the last block round to bf16 and store.
+//     the TMEM buffer, and after the last block round to bf16, stage the tile
+//     in shared memory (128-byte swizzle) and hand it to asynchronous TMA
+//     stores, so the next tile's promotion starts at once.
 //
-// The scales are read by the epilogue straight from global memory, two blocks
-// ahead of use (per-row / per-block scales into registers; WGrad's per-column
-// scale rows through an L1 prefetch and broadcast loads).  They are not staged
-// through the shared-memory ring: generic-proxy reads of a buffer that the
-// async proxy (TMA) rewrites are not ordered by the stage barriers alone, and
-// a ring-staged variant measured non-deterministic.
+//   * a scale warp streams each block's scales (128 row scales, and the block
+//     or per-column scales of the tile's columns) into an 8-slot shared-memory
+//     ring with cp.async, up to 8 blocks ahead of the epilogue, so that their
+//     global-memory latency never reaches the promotion.  These copies use the
+//     generic proxy (cp.async + cp.async.mbarrier.arrive), not TMA: the
+//     epilogue reads the ring with ordinary loads, and generic reads of a
+//     buffer that the async proxy rewrites are not ordered by mbarriers alone
+//     (a TMA-staged variant measured non-deterministic).
 //
 // Tiles are 128 x 256; the kernel is persistent (one CTA per SM) and walks
 // the tile list with the smaller operand resident in L2.  Every mbarrier wait
@@ -53,26 +57,33 @@ constexpr int BM = 128;                    // tile rows (TMEM lanes)
 constexpr int BN = 256;                    // tile columns (MMA N)
 constexpr int BK = 128;                    // contraction block = scale granularity = 128 bytes of E4M3
 constexpr int UMMA_K = 32;                 // K of one kind::f8f6f4 MMA
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BK;           // 16 KB
 constexpr int B_BYTES = BN * BK;           // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-// Warpgroup 0: warp 0 TMA, warp 1 MMA (and TMEM owner), warps 2-3 idle.
+// Warpgroup 0: warp 0 TMA, warp 1 MMA (and TMEM owner), warp 2 scales, warp 3 idle.
 // Warpgroups 1-2: eight epilogue warps.  Registers are rebalanced with
 // setmaxnreg: 128 x 40 + 256 x 232 = 384 x 168, the launch allocation.
 constexpr int NUM_THREADS = 384;
 constexpr int FIRST_EPI_WARP = 4;
 constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_EPI_WARPS_C = NUM_EPI_WARPS;
 constexpr int REGS_PRODUCER = 40;
 constexpr int REGS_EPILOGUE = 232;
 constexpr int TMEM_COLS = 2 * BN;          // two partial buffers
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+constexpr int STG_BYTES = NUM_EPI_WARPS_C * 2 * 32 * 128;  // output staging: per warp two 32x64 bf16 boxes
+constexpr int SCALE_SLOTS = 8;             // scale ring depth (contraction blocks)
+constexpr int SLOT_FLOATS = BM + BN;       // 128 row scales + up to 256 column scales
+constexpr int RING_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 2 * SCALE_SLOTS;
+constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + STG_BYTES + RING_BYTES + NUM_BARS * 8 + 16;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1),
-// A and B E4M3 (format 0 in bits 7-9 / 10-12), both K-major (bits 15/16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// A and B E4M3 (format 0 in bits 7-9 / 10-12), A K-major (bit 15 = 0), B K-major
+// (bit 16 = 0) or MN-major (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t IDESC_BK = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t IDESC_BMN = IDESC_BK | (1u << 16);
 
 // Error sites (reported by rlq_check / rlq_last_error).
 enum : uint32_t {
@@ -82,6 +93,8 @@ enum : uint32_t {
     SITE_EPI_TMEM_FULL = 4,
     SITE_TEARDOWN = 5,
     SITE_DRAIN = 6,
+    SITE_SCALE_EMPTY = 7,
+    SITE_EPI_SCALE_FULL = 8,
     SITE_DIAG = 99,
 };
 
@@ -164,9 +177,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l1(const void *p)
+// 4-byte global -> shared copy; src_bytes = 0 writes zero without reading.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes)
 {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// TMA store of a box from shared memory, tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"((uint64_t)map), "r"(src), "r"(x), "r"(y)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
@@ -182,13 +210,14 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate)
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(IDESC), "r"(accumulate)
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -230,62 +259,48 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-__device__ __forceinline__ uint64_t f2_bits(float lo, float hi)
+// MN-major operand (the MN index contiguous), 128-byte swizzle: each atom is
+// 128 MN elements (bytes) x 8 contraction rows (1024 bytes); contraction rows
+// are 128 bytes apart, 8-row groups 1024 bytes apart (SBO), and the second
+// 128-wide MN atom of a 256-wide tile sits 16 KB further (LBO).
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr)
 {
-    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(16384 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// acc += p * scale, two lanes at a time.
-__device__ __forceinline__ void ffma2(uint64_t &acc, uint64_t p, uint64_t scale)
+__device__ __forceinline__ float2 f2_of(uint32_t lo, uint32_t hi)
 {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(p), "l"(scale));
+    return make_float2(__uint_as_float(lo), __uint_as_float(hi));
 }
 
-__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// Keeps the compiler from sinking the FMAs of one TMEM chunk below the next
-// chunk's load (which would hold several chunks in registers at once).
-__device__ __forceinline__ void reg_fence16(uint64_t *a)
-{
-    asm volatile(""
-                 : "+l"(a[0]), "+l"(a[1]), "+l"(a[2]), "+l"(a[3]), "+l"(a[4]), "+l"(a[5]), "+l"(a[6]), "+l"(a[7]),
-                   "+l"(a[8]), "+l"(a[9]), "+l"(a[10]), "+l"(a[11]), "+l"(a[12]), "+l"(a[13]), "+l"(a[14]), "+l"(a[15]));
-}
-
-// acc[0..15] += chunk * scale (one scale for the whole chunk).
-__device__ __forceinline__ void promote_chunk(uint64_t *acc, const uint32_t (&r)[32], uint64_t scl2)
+// acc[0..15] += chunk * scale, two columns per packed fp32 FMA.
+__device__ __forceinline__ void promote_chunk(float2 *acc, const uint32_t (&r)[32], float2 scl)
 {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-        ffma2(acc[j], f2_bits(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), scl2);
-    reg_fence16(acc);
+        acc[j] = __ffma2_rn(f2_of(r[2 * j], r[2 * j + 1]), scl, acc[j]);
 }
 
 // acc[0..15] += chunk * sa * sb[column]; sb is 32 consecutive column scales in
-// global memory, read by every lane (broadcast).
-__device__ __forceinline__ void promote_chunk_cols(uint64_t *acc, const uint32_t (&r)[32], uint64_t sa2,
+// shared memory, read by every lane (broadcast).
+__device__ __forceinline__ void promote_chunk_cols(float2 *acc, const uint32_t (&r)[32], float2 sa2,
                                                    const float4 *sbs)
 {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float4 sb4 = __ldg(sbs + j);
-        const uint64_t s01 = fmul2(sa2, f2_bits(sb4.x, sb4.y));
-        const uint64_t s23 = fmul2(sa2, f2_bits(sb4.z, sb4.w));
-        ffma2(acc[2 * j], f2_bits(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), s01);
-        ffma2(acc[2 * j + 1], f2_bits(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), s23);
+        const float4 sb4 = sbs[j];
+        const float2 s01 = __fmul2_rn(sa2, make_float2(sb4.x, sb4.y));
+        const float2 s23 = __fmul2_rn(sa2, make_float2(sb4.z, sb4.w));
+        acc[2 * j] = __ffma2_rn(f2_of(r[4 * j], r[4 * j + 1]), s01, acc[2 * j]);
+        acc[2 * j + 1] = __ffma2_rn(f2_of(r[4 * j + 2], r[4 * j + 3]), s23, acc[2 * j + 1]);
     }
-    reg_fence16(acc);
 }
 
-__device__ __forceinline__ uint32_t bf16x2_rn(uint64_t v)
+__device__ __forceinline__ uint32_t bf16x2_rn(float2 v)
 {
     uint32_t d;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "r"((uint32_t)(v >> 32)), "r"((uint32_t)v));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(v.y), "f"(v.x));
     return d;
 }
 
@@ -315,14 +330,16 @@ __device__ __forceinline__ void tile_coords(const Params &p, int tile, int &mt, 
     }
 }
 
-template <bool kColScaleB>
+template <bool kColScaleB, bool kBMajorMN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_block_scaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const Params p)
+                        const __grid_constant__ CUtensorMap tmOut, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint8_t *staging = smem + STAGES * STAGE_BYTES;
+    float *ring = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES + STG_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + STG_BYTES + RING_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -335,6 +352,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto tfull_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + b]); };
     auto tempty_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + 2 + b]); };
     const uint32_t teardown_bar = smem_u32(&bars[2 * STAGES + 4]);
+    auto sfull_bar = [&](int k) { return smem_u32(&bars[2 * STAGES + 5 + k]); };
+    auto sempty_bar = [&](int k) { return smem_u32(&bars[2 * STAGES + 5 + SCALE_SLOTS + k]); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -346,6 +365,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(tempty_bar(b), NUM_EPI_WARPS);
         }
         mbar_init(teardown_bar, 1);
+        for (int k = 0; k < SCALE_SLOTS; ++k) {
+            mbar_init(sfull_bar(k), 32);              // one cp.async arrival per scale-warp lane
+            mbar_init(sempty_bar(k), NUM_EPI_WARPS);  // one arrival per epilogue warp
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -359,6 +382,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        prefetch_tmap(&tmOut);
     }
     tc_fence_before();
     __syncthreads();
@@ -384,7 +408,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
                     tma_load_2d(a_stage(s), &tmA, full_bar(s), kb * BK, mt * BM);
-                    tma_load_2d(b_stage(s), &tmB, full_bar(s), kb * BK, nt * BN);
+                    if (kBMajorMN) {
+                        // B stored [contraction][output]: two 128-column boxes of 128 rows
+                        tma_load_2d(b_stage(s), &tmB, full_bar(s), nt * BN, kb * BK);
+                        tma_load_2d(b_stage(s) + B_BYTES / 2, &tmB, full_bar(s), nt * BN + 128, kb * BK);
+                    } else {
+                        tma_load_2d(b_stage(s), &tmB, full_bar(s), kb * BK, nt * BN);
+                    }
                 }
             }
             if (!ok) {
@@ -415,10 +445,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_after();
                     const uint32_t d = tmem_base + (uint32_t)(buf * BN);
                     const uint64_t ad = sw128_desc(a_stage(s));
-                    const uint64_t bd = sw128_desc(b_stage(s));
+                    const uint64_t bd = kBMajorMN ? sw128_desc_mn(b_stage(s)) : sw128_desc(b_stage(s));
 #pragma unroll
-                    for (int j = 0; j < BK / UMMA_K; ++j)  // +32 bytes along K = +2 in the address field
-                        tc_mma_f8(d, ad + 2 * j, bd + 2 * j, j > 0 ? 1u : 0u);
+                    for (int j = 0; j < BK / UMMA_K; ++j) {
+                        // K-major: +32 bytes along K (+2 in the address field); MN-major:
+                        // +32 contraction rows of 128 bytes (+256)
+                        const uint64_t bj = kBMajorMN ? bd + (uint64_t)(256 * j) : bd + 2 * j;
+                        tc_mma_f8(d, ad + 2 * j, bj, kBMajorMN ? IDESC_BMN : IDESC_BK, j > 0 ? 1u : 0u);
+                    }
                     tc_commit(empty_bar(s));
                     tc_commit(tfull_bar(buf));
                 }
@@ -428,42 +462,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             volatile uint32_t never = 0;
             mbar_wait(teardown_bar, 0, &never, 20000000ull, SITE_TEARDOWN);
         }
+    } else if (warp == 2) {
+        // ------------------------------------------------ scale loader ---
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            int mt, nt;
+            tile_coords(p, tile, mt, nt);
+            for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                const int k = it % SCALE_SLOTS;
+                const uint32_t ph = (uint32_t)(it / SCALE_SLOTS) & 1u;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(sempty_bar(k), ph ^ 1u, abort_flag, p.timeout_ns,
+                                                       SITE_SCALE_EMPTY))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t slot = smem_u32(ring + k * SLOT_FLOATS);
+                const float *sa_row = p.sa + (int64_t)kb * p.ld_sa;
+#pragma unroll
+                for (int j = 0; j < BM / 32; ++j) {
+                    const int r = mt * BM + lane + 32 * j;
+                    cp_async4(slot + 4u * (lane + 32 * j), r < p.R ? sa_row + r : sa_row, r < p.R ? 4u : 0u);
+                }
+                if (kColScaleB) {
+                    const float *sb_row = p.sb + (int64_t)kb * p.sb_bstride;
+#pragma unroll
+                    for (int j = 0; j < BN / 32; ++j) {
+                        const int c = nt * BN + lane + 32 * j;
+                        cp_async4(slot + 4u * (BM + lane + 32 * j), c < p.C ? sb_row + c : sb_row, c < p.C ? 4u : 0u);
+                    }
+                } else if (lane < BN / 128) {
+                    const int c = nt * BN + lane * 128;
+                    const float *src = p.sb + (int64_t)kb * p.sb_bstride + (int64_t)(c >> 7) * p.sb_cstride;
+                    cp_async4(slot + 4u * (BM + lane), c < p.C ? src : p.sb, c < p.C ? 4u : 0u);
+                }
+                cp_async_arrive(sfull_bar(k));
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp >= FIRST_EPI_WARP) {
         // --------------------------------------------------- epilogue ---
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPILOGUE));
         const int q = warp & 3;                      // TMEM lane quarter this warp may access
         const int h = (warp - FIRST_EPI_WARP) >> 2;  // column half of the tile
         const int row = q * 32 + lane;               // tile row = TMEM lane
-
-        // The block scales are fetched two contraction blocks ahead (crossing
-        // tile boundaries) so that their global-memory latency stays hidden.
-        int pf_tile = blockIdx.x, pf_kb = 0;
-        auto fetch = [&](float &sa_o, float &sb_o) {
-            sa_o = 0.0f;
-            sb_o = 0.0f;
-            if (pf_tile < p.num_tiles) {
-                int mt, nt;
-                tile_coords(p, pf_tile, mt, nt);
-                const int grow = mt * BM + row;
-                if (grow < p.R)
-                    sa_o = __ldg(p.sa + (int64_t)pf_kb * p.ld_sa + grow);
-                const int col0 = nt * BN + h * 128;
-                if (!kColScaleB) {
-                    if (col0 < p.C)
-                        sb_o = __ldg(p.sb + (int64_t)pf_kb * p.sb_bstride + (int64_t)(col0 >> 7) * p.sb_cstride);
-                } else if (col0 < p.C && lane < 4) {
-                    // the warp's 128 column scales: four 128-byte lines
-                    prefetch_l1(p.sb + (int64_t)pf_kb * p.sb_bstride + col0 + lane * 32);
-                }
-                if (++pf_kb == p.kblocks) {
-                    pf_kb = 0;
-                    pf_tile += gridDim.x;
-                }
-            }
-        };
-        float sa0, sb0, sa1, sb1, sa2, sb2;
-        fetch(sa0, sb0);
-        fetch(sa1, sb1);
 
         int it = 0;
         bool ok = true;
@@ -474,27 +516,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool row_ok = grow < p.R;
             const int col0 = nt * BN + h * 128;
             const bool half_ok = col0 < p.C;
-            uint64_t acc[64];
+            float2 acc[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j)
-                acc[j] = 0;
+                acc[j] = make_float2(0.0f, 0.0f);
             for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                 const int buf = it & 1;
                 const uint32_t bph = (uint32_t)(it >> 1) & 1u;
-                fetch(sa2, sb2);
-                // every lane acquires the partial itself; the decision is made
-                // warp-uniform because tcgen05.ld is a .sync.aligned instruction
-                const bool w = mbar_wait(tfull_bar(buf), bph, abort_flag, p.timeout_ns, SITE_EPI_TMEM_FULL);
+                const int k = it % SCALE_SLOTS;
+                // every lane acquires the scales and the partial itself; the
+                // decision is warp-uniform because tcgen05.ld is .sync.aligned
+                const bool w = mbar_wait(sfull_bar(k), (uint32_t)(it / SCALE_SLOTS) & 1u, abort_flag, p.timeout_ns,
+                                         SITE_EPI_SCALE_FULL) &&
+                               mbar_wait(tfull_bar(buf), bph, abort_flag, p.timeout_ns, SITE_EPI_TMEM_FULL);
                 if (!__all_sync(0xFFFFFFFFu, w)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const float *slot = ring + k * SLOT_FLOATS;
+                const float sa = slot[row];
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
                 uint32_t ra[32], rb[32];
                 if (!kColScaleB) {
-                    const float scl = sa0 * sb0;
-                    const uint64_t scl2 = f2_bits(scl, scl);
+                    const float scl = sa * slot[BM + h];
+                    const float2 scl2 = make_float2(scl, scl);
                     tmem_ld32_async(taddr, ra);
                     tmem_wait32(ra);
                     tmem_ld32_async(taddr + 32, rb);
@@ -508,9 +554,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_wait32(rb);
                     promote_chunk(&acc[48], rb, scl2);
                 } else {
-                    const float4 *sbs = reinterpret_cast<const float4 *>(
-                        p.sb + (int64_t)kb * p.sb_bstride + (half_ok ? col0 : 0));
-                    const uint64_t sa2v = f2_bits(sa0, sa0);
+                    const float4 *sbs = reinterpret_cast<const float4 *>(slot + BM + h * 128);
+                    const float2 sa2v = make_float2(sa, sa);
                     tmem_ld32_async(taddr, ra);
                     tmem_wait32(ra);
                     tmem_ld32_async(taddr + 32, rb);
@@ -526,21 +571,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
+                if (lane == 0) {
                     mbar_arrive(tempty_bar(buf));
-                sa0 = sa1;
-                sb0 = sb1;
-                sa1 = sa2;
-                sb1 = sb2;
+                    mbar_arrive(sempty_bar(k));
+                }
             }
-            if (ok && row_ok && half_ok) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out + (int64_t)grow * p.ldo + col0);
+            if (ok) {
+                // this warp's 32 rows x 128 columns: two 32x64 boxes, rows of
+                // 128 bytes with the 16-byte chunks XOR-swizzled by (row % 8)
+                const uint32_t stg = smem_u32(staging) + (uint32_t)((warp - FIRST_EPI_WARP) * 2 * 32 * 128);
+                if (lane == 0)
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // previous tile's boxes read
+                __syncwarp();
 #pragma unroll
-                for (int v = 0; v < 16; ++v)
-                    dst[v] = make_uint4(bf16x2_rn(acc[4 * v]), bf16x2_rn(acc[4 * v + 1]), bf16x2_rn(acc[4 * v + 2]),
-                                        bf16x2_rn(acc[4 * v + 3]));
+                for (int v = 0; v < 16; ++v) {
+                    const uint32_t addr = stg + (uint32_t)((v >> 3) * 32 * 128 + lane * 128 +
+                                                           ((((v & 7) ^ (lane & 7))) << 4));
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                 "r"(bf16x2_rn(acc[4 * v])), "r"(bf16x2_rn(acc[4 * v + 1])),
+                                 "r"(bf16x2_rn(acc[4 * v + 2])), "r"(bf16x2_rn(acc[4 * v + 3]))
+                                 : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> TMA reads
+                __syncwarp();
+                if (lane == 0 && half_ok) {
+                    // rows beyond R are clipped by the tensor map
+                    tma_store_2d(&tmOut, stg, col0, mt * BM + q * 32);
+                    tma_store_2d(&tmOut, stg + 32 * 128, col0 + 64, mt * BM + q * 32);
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                }
             }
         }
+        if (lane == 0)
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // stores complete before exit
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -597,6 +661,25 @@ uint64_t wait_limit_ns()
     return ns;
 }
 
+// bf16 output [rows][cols], pitch ld elements; box 64 columns x 32 rows, 128-byte swizzle.
+rlq_status encode_out_map(CUtensorMap *map, uint16_t *base, int64_t cols, int64_t rows, int64_t ld)
+{
+    auto enc = get_encode_fn();
+    if (!enc)
+        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for the [%lld x %lld] output",
+                    (int)r, (long long)rows, (long long)cols);
+    return RLQ_OK;
+}
+
 // 2-D E4M3 tensor [rows][inner] with row pitch `ld` bytes; box 128 x box_rows.
 rlq_status encode_map(CUtensorMap *map, const uint8_t *base, int64_t inner, int64_t rows, int64_t ld, int box_rows)
 {
@@ -618,7 +701,7 @@ rlq_status encode_map(CUtensorMap *map, const uint8_t *base, int64_t inner, int6
 
 struct DevInfo {
     int sms = 0;
-    bool attr_set[2] = {false, false};
+    bool attr_set[4] = {false, false, false, false};
 };
 
 DevInfo &dev_info(int dev)
@@ -635,14 +718,18 @@ DevInfo &dev_info(int dev)
     return d;
 }
 
-template <bool kCol>
+template <bool kCol, bool kBMN>
 rlq_status launch_impl(const GemmArgs &a, cudaStream_t st)
 {
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmO;
     rlq_status rs = encode_map(&tmA, a.A, a.L, a.R, a.lda, BM);
     if (rs != RLQ_OK)
         return rs;
-    rs = encode_map(&tmB, a.B, a.L, a.C, a.ldb, BN);
+    // B is [C][L] (K-major) or [L][C] (MN-major, boxes of 128 columns x 128 rows)
+    rs = kBMN ? encode_map(&tmB, a.B, a.C, a.L, a.ldb, BK) : encode_map(&tmB, a.B, a.L, a.C, a.ldb, BN);
+    if (rs != RLQ_OK)
+        return rs;
+    rs = encode_out_map(&tmO, a.out, a.C, a.R, a.ldo);
     if (rs != RLQ_OK)
         return rs;
     int dev = 0;
@@ -650,11 +737,13 @@ rlq_status launch_impl(const GemmArgs &a, cudaStream_t st)
     if (e != cudaSuccess)
         return cuda_status(e, "cudaGetDevice");
     DevInfo &di = dev_info(dev);
-    if (!di.attr_set[kCol]) {
-        e = cudaFuncSetAttribute(k_gemm_block_scaled<kCol>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    const int variant = (kCol ? 1 : 0) + (kBMN ? 2 : 0);
+    if (!di.attr_set[variant]) {
+        e = cudaFuncSetAttribute(k_gemm_block_scaled<kCol, kBMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES);
         if (e != cudaSuccess)
             return cuda_status(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-        di.attr_set[kCol] = true;
+        di.attr_set[variant] = true;
     }
     Params p;
     p.sa = a.sa;
@@ -674,7 +763,7 @@ rlq_status launch_impl(const GemmArgs &a, cudaStream_t st)
     p.m_fastest = (a.R * a.L <= a.C * a.L) ? 1 : 0;
     p.timeout_ns = wait_limit_ns();
     const int grid = p.num_tiles < di.sms ? p.num_tiles : di.sms;
-    k_gemm_block_scaled<kCol><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+    k_gemm_block_scaled<kCol, kBMN><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, tmO, p);
     return cuda_status(cudaGetLastError(), "block-scaled GEMM launch");
 }
 
@@ -689,7 +778,9 @@ rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st)
         return cuda_status(cudaMemset2DAsync(a.out, (size_t)a.ldo * 2, 0, (size_t)a.C * 2, (size_t)a.R, st),
                            "cudaMemset2DAsync (empty contraction)");
     }
-    return a.per_col_sb ? launch_impl<true>(a, st) : launch_impl<false>(a, st);
+    if (a.per_col_sb)
+        return launch_impl<true, false>(a, st);
+    return a.b_mn_major ? launch_impl<false, true>(a, st) : launch_impl<false, false>(a, st);
 }
 
 rlq_status check_device_errors(cudaStream_t st)

@@ -34,6 +34,8 @@ cudaError_t launch_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, cons
 // out[r, c] = bf16( sum_b sa(b, r) * sb(b, c) * sum_{j in block b} A[r, j] * B[c, j] )
 // A: E4M3 [R rows][L contraction], pitch lda bytes; B: E4M3 [C rows][L], pitch ldb.
 // sa(b, r) = sa[b * ld_sa + r].
+// B is [C rows][L] (K-major) or, with b_mn_major, [L rows][C] (the FProp weight
+// codes read as DGrad's operand without a transposed copy); pitch ldb bytes.
 // Block-scaled B (per_col_sb == false): sb(b, c) = sb[b * sb_bstride + (c / 128) * sb_cstride].
 // Column-scaled B (per_col_sb == true):  sb(b, c) = sb[b * sb_bstride + c], rows 16-byte aligned.
 struct GemmArgs {
@@ -47,6 +49,7 @@ struct GemmArgs {
     int64_t sb_bstride;
     int64_t sb_cstride;
     bool per_col_sb;
+    bool b_mn_major;
     uint16_t *out;
     int64_t ldo;
     int64_t R, C, L;

@@ -53,9 +53,13 @@ def test_fprop_parity(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_dgrad_parity(M, N, K):
+@pytest.mark.parametrize("transposed", [True, False])
+def test_dgrad_parity(M, N, K, transposed):
+    """DGrad from the transposed weight codes, or from the FProp codes read
+    MN-major; both must match the oracle (and each other)."""
     g, o = _quantized_operands(M, N, K, 21)
-    dx = rlq.gemm_dgrad(g["qdy"], g["sdy"], g["qwT"], g["sw"], transposed=True)
+    w = g["qwT"] if transposed else g["qw"]
+    dx = rlq.gemm_dgrad(g["qdy"], g["sdy"], w, g["sw"], transposed=transposed)
     rlq.check()
     assert_gemm_close(dx, oracle.gemm_dgrad(o["qdy"], o["sdy"], o["qw"], o["sw"]), "DGrad")
 
@@ -93,6 +97,7 @@ def test_integer_gemms_bit_exact(M, N, K, scale):
     sdy = np.full((N // 128, M), scale, np.float32)
     y = rlq.gemm_fprop(_dev(qx), _dev(sx), _dev(qw), _dev(sw))
     dx = rlq.gemm_dgrad(_dev(qdy), _dev(sdy), _dev(np.ascontiguousarray(qw.T)), _dev(sw), transposed=True)
+    dx_mn = rlq.gemm_dgrad(_dev(qdy), _dev(sdy), _dev(qw), _dev(sw), transposed=False)
     # WGrad operands: 128x1 codes of dY and X, transposed, with a partial last token block
     MB = (M + 127) // 128
     ldm = (M + 15) // 16 * 16
@@ -109,6 +114,7 @@ def test_integer_gemms_bit_exact(M, N, K, scale):
     rdw = oracle.gemm_wgrad(qdyT[:, :M], sdyc, qxT[:, :M], sxc)
     assert np.array_equal(u16(y), _bf16_of(ry)), "FProp integer pin"
     assert np.array_equal(u16(dx), _bf16_of(rdx)), "DGrad integer pin"
+    assert np.array_equal(u16(dx_mn), _bf16_of(rdx)), "DGrad (untransposed weight codes) integer pin"
     assert np.array_equal(u16(dw), _bf16_of(rdw)), "WGrad integer pin"
 
 
