@@ -335,15 +335,23 @@ def run_ours(args):
 
 
 def _load_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel version (else null)."""
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when there is none or the kernel source changed since it was captured."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         t = json.load(f)
     v = t.get(kernel)
-    return v.get("dram_bytes_per_launch") if isinstance(v, dict) and v.get("current", False) else None
+    if not isinstance(v, dict):
+        return None
+    src = os.path.join(ROOT, v.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return v.get("dram_bytes_per_launch") if sha == v.get("source_sha256_16") else None
 
 
 def run_e2e(st: Step, host, args, dist, world, flop_step):
