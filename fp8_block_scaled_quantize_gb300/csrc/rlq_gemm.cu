@@ -133,6 +133,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended in hardware for up to
+// SUSPEND_NS while the phase is incomplete; it resumes as soon as the phase
+// completes.  Waiting warps then cost no issue slots.
+constexpr uint32_t SUSPEND_NS = 20000;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(SUSPEND_NS)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns()
 {
     uint64_t t;
@@ -155,9 +173,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_sleep(bar, parity))
             return true;
-        if ((i & 31) == 0) {
+        if ((i & 3) == 0) {
             if (*abort_flag)
                 return false;
             if (global_timer_ns() - t0 > limit_ns) {
@@ -486,7 +504,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (kColScaleB) {
                     const float *sb_row = p.sb + (int64_t)kb * p.sb_bstride;
-#pragma unroll
+#pragma unroll 1  // this warp runs on 40 registers
                     for (int j = 0; j < BN / 32; ++j) {
                         const int c = nt * BN + lane + 32 * j;
                         cp_async4(slot + 4u * (BM + lane + 32 * j), c < p.C ? sb_row + c : sb_row, c < p.C ? 4u : 0u);

@@ -11,8 +11,8 @@
 // All kernels are HBM-bound streaming kernels: 16-byte loads of 8 bf16 per
 // lane, a group of 128 spread over 16 lanes (warp-shuffle amax), packed code
 // stores.  The per-element quotient x / s uses the group's reciprocal
-// r = RN(1/s) plus one FMA residual correction, which costs 4 ALU ops instead
-// of an IEEE division sequence.  For bf16 x with |x| <= amax and
+// r = RN(1/s) plus one FMA residual correction (1.5 packed fp32x2 ops per
+// element) instead of an IEEE division sequence.  For bf16 x with |x| <= amax and
 // s = fl32(amax/448) this equals IEEE fp32 division wherever the E4M3 code can
 // depend on it (every (x, amax) bf16 pair was enumerated); groups with a scale
 // below 2^-100 are pre-scaled by 2^64, exactly, so that 1/s stays finite.
@@ -56,7 +56,8 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
     return d;
 }
 
-// Division context of one group.
+// Division context of one group (or of a pair of groups, one per lane of a
+// packed fp32x2 operation).
 struct Quot {
     float f;   // exact pre-scale: 1, or 2^64 for scales below 2^-100
     float sd;  // s * f (exact)
@@ -77,24 +78,60 @@ __device__ __forceinline__ Quot make_quot(float s)
     return q;
 }
 
-// fl32(x / s), as described at the top of this file; the sign is taken from x
-// so that -0 stays -0.
-__device__ __forceinline__ float quot(float x, const Quot &c)
+
+// fl32(x / s) for two elements at once, as described at the top of this file:
+// q0 = x*r, e = x - q0*s (one FMA, rounded toward -inf), q1 = q0 + e*r.  The
+// downward-rounded residual keeps the sign of a zero quotient (x = -0 gives -0);
+// every (x, amax) bf16 pair was enumerated: q1 equals the IEEE quotient wherever
+// the E4M3 code depends on it, sign included.  Each packed operation rounds
+// each lane exactly as its scalar IEEE counterpart does.  kPrescale applies the
+// exact 2^64 pre-scale of groups whose scale is below 2^-100.
+template <bool kPrescale>
+__device__ __forceinline__ float2 quot2(float2 x, float2 f, float2 r, float2 nsd)
 {
-    const float xs = __fmul_rn(x, c.f);
-    const float q0 = __fmul_rn(xs, c.r);
-    const float e = __fmaf_rn(-q0, c.sd, xs);
-    const float q1 = __fmaf_rn(e, c.r, q0);
-    return __uint_as_float((__float_as_uint(q1) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+    const float2 xs = kPrescale ? __fmul2_rn(x, f) : x;
+    const float2 q0 = __fmul2_rn(xs, r);
+    const float2 e = __ffma2_rd(q0, nsd, xs);  // xs - q0 * sd
+    return __ffma2_rn(e, r, q0);
 }
 
-// Codes of 8 consecutive elements, element 0 in the lowest byte.
-__device__ __forceinline__ uint2 encode8(const float (&f)[8], const Quot &c)
+// Codes of 8 consecutive elements of one group, element 0 in the lowest byte.
+template <bool kPrescale>
+__device__ __forceinline__ uint2 encode8_t(const float (&v)[8], const Quot &c)
 {
+    const float2 f = make_float2(c.f, c.f), r = make_float2(c.r, c.r), nsd = make_float2(-c.sd, -c.sd);
+    const float2 a = quot2<kPrescale>(make_float2(v[0], v[1]), f, r, nsd);
+    const float2 b = quot2<kPrescale>(make_float2(v[2], v[3]), f, r, nsd);
+    const float2 d = quot2<kPrescale>(make_float2(v[4], v[5]), f, r, nsd);
+    const float2 g = quot2<kPrescale>(make_float2(v[6], v[7]), f, r, nsd);
     uint2 out;
-    out.x = e4m3x2(quot(f[0], c), quot(f[1], c)) | (e4m3x2(quot(f[2], c), quot(f[3], c)) << 16);
-    out.y = e4m3x2(quot(f[4], c), quot(f[5], c)) | (e4m3x2(quot(f[6], c), quot(f[7], c)) << 16);
+    out.x = e4m3x2(a.x, a.y) | (e4m3x2(b.x, b.y) << 16);
+    out.y = e4m3x2(d.x, d.y) | (e4m3x2(g.x, g.y) << 16);
     return out;
+}
+
+__device__ __forceinline__ uint2 encode8(const float (&v)[8], const Quot &c)
+{
+    return c.f == 1.0f ? encode8_t<false>(v, c) : encode8_t<true>(v, c);
+}
+
+// Codes of 32 rows of two adjacent columns (packed lanes: even, odd column),
+// read from the staged tile; the words hold 4 rows each.
+template <bool kPrescale>
+__device__ __forceinline__ void encode_cols(const uint32_t *col, int rq, int tp2, float2 pf, float2 pr, float2 pn,
+                                            uint32_t (&e)[8], uint32_t (&o)[8])
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float2 qq[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t wv = col[(rq * 32 + 4 * j + u) * tp2];
+            qq[u] = quot2<kPrescale>(make_float2(bf_lo(wv), bf_hi(wv)), pf, pr, pn);
+        }
+        e[j] = e4m3x2(qq[0].x, qq[1].x) | (e4m3x2(qq[2].x, qq[3].x) << 16);
+        o[j] = e4m3x2(qq[0].y, qq[1].y) | (e4m3x2(qq[2].y, qq[3].y) << 16);
+    }
 }
 
 __device__ __forceinline__ float amax8(const float (&f)[8])
@@ -186,7 +223,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
                                                     float *__restrict__ sc, int64_t ldsc, int64_t MB)
 {
     __shared__ __align__(16) uint16_t tile[GRP * TP];
-    __shared__ float cam[4][GRP];
+    __shared__ float cam[4][GRP];  // column maxima of the four row quarters
     const int t = threadIdx.x, lane = t & 31, half = lane >> 4, l16 = lane & 15, warp = t >> 5;
     const int hw16 = warp * 2 + half;  // 0..15
     const int64_t kb = blockIdx.x;
@@ -196,7 +233,8 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
         const int64_t m0 = mb * GRP;
         const int rows = (int)((M - m0) < GRP ? (M - m0) : GRP);
 
-        // ---- row pass: half-warp hw16 owns rows hw16 + 16 i
+        // ---- row pass: half-warp hw16 owns rows hw16 + 16 i; lane l16 owns
+        // columns 8 l16 .. 8 l16 + 7.  Rows beyond M read as zero.
         uint4 v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -206,19 +244,30 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = hw16 + 16 * i;
-            row_group(v[i], r < rows, m0 + r, kb, l16, q, ldq, s, lds);
+            float f[8];
+            unpack8(v[i], f);
+            const float amax = halfwarp_max(amax8(f));
+            const float scl = group_scale(amax);
+            const Quot c = make_quot(scl);
+            const uint2 codes = encode8(f, c);
+            if (r < rows) {
+                *reinterpret_cast<uint2 *>(q + (m0 + r) * ldq + kb * GRP + l16 * 8) = codes;
+                if (l16 == 0)
+                    s[kb * lds + m0 + r] = scl;
+            }
             *reinterpret_cast<uint4 *>(&tile[r * TP + l16 * 8]) = v[i];
         }
         __syncthreads();
 
-        // ---- column pass: thread owns columns 2*c2, 2*c2+1 over rows rq*32 .. +31
+        // ---- column pass: thread owns columns 2*c2, 2*c2+1 over rows rq*32 .. +31;
+        // first the column maxima (four row quarters combined through smem)
         const uint32_t *col = reinterpret_cast<const uint32_t *>(tile) + c2;
         float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll 8
         for (int rr = 0; rr < 32; ++rr) {
-            const uint32_t w = col[(rq * 32 + rr) * (TP / 2)];
-            a0 = fmaxf(a0, fabsf(bf_lo(w)));
-            a1 = fmaxf(a1, fabsf(bf_hi(w)));
+            const uint32_t wv = col[(rq * 32 + rr) * (TP / 2)];
+            a0 = fmaxf(a0, fabsf(bf_lo(wv)));
+            a1 = fmaxf(a1, fabsf(bf_hi(wv)));
         }
         cam[rq][2 * c2] = a0;
         cam[rq][2 * c2 + 1] = a1;
@@ -227,18 +276,14 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
         a1 = fmaxf(fmaxf(cam[0][2 * c2 + 1], cam[1][2 * c2 + 1]), fmaxf(cam[2][2 * c2 + 1], cam[3][2 * c2 + 1]));
         const float s0 = group_scale(a0), s1 = group_scale(a1);
         const Quot c0 = make_quot(s0), c1 = make_quot(s1);
+        // one packed lane per column: (even column, odd column) of the same row
+        const float2 pf = make_float2(c0.f, c1.f), pr = make_float2(c0.r, c1.r), pn = make_float2(-c0.sd, -c1.sd);
+        const bool fast = (c0.f == 1.0f) && (c1.f == 1.0f);
         uint32_t e[8], o[8];  // 32 codes of each column, 4 per word
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t w0 = col[(rq * 32 + 4 * j + 0) * (TP / 2)];
-            const uint32_t w1 = col[(rq * 32 + 4 * j + 1) * (TP / 2)];
-            const uint32_t w2 = col[(rq * 32 + 4 * j + 2) * (TP / 2)];
-            const uint32_t w3 = col[(rq * 32 + 4 * j + 3) * (TP / 2)];
-            e[j] = e4m3x2(quot(bf_lo(w0), c0), quot(bf_lo(w1), c0)) |
-                   (e4m3x2(quot(bf_lo(w2), c0), quot(bf_lo(w3), c0)) << 16);
-            o[j] = e4m3x2(quot(bf_hi(w0), c1), quot(bf_hi(w1), c1)) |
-                   (e4m3x2(quot(bf_hi(w2), c1), quot(bf_hi(w3), c1)) << 16);
-        }
+        if (fast)
+            encode_cols<false>(col, rq, TP / 2, pf, pr, pn, e, o);
+        else
+            encode_cols<true>(col, rq, TP / 2, pf, pr, pn, e, o);
         const int64_t k = kb * GRP + 2 * c2;
         const int r0 = rq * 32;
         uint8_t *d0 = qT + k * ldqT + m0 + r0;
@@ -261,29 +306,33 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
             sc[mb * ldsc + k] = s0;
             sc[mb * ldsc + k + 1] = s1;
         }
-        __syncthreads();  // the tile and cam are reused by the next mb
+        __syncthreads();  // tile and cam are reused by the next mb
     }
 }
 
 // ---------------------------------------------------------------------------
-// 128x128 weight blocks: one CTA per block, block amax through registers
-// (one read of w), codes stored row-wise and, optionally, transposed through
-// a shared-memory staging tile.
-constexpr int CTP = GRP + 16;  // code staging row pitch (bytes)
+// 128x128 weight blocks: one CTA per block.  The block is read once (16-byte
+// loads), its amax reduced while the raw values are stashed in shared memory,
+// then quantized from shared memory; the same buffer is reused to transpose the
+// codes for the optional [K,N] copy.  32 KB of shared memory and few registers
+// per thread keep several blocks in flight per SM.
+constexpr int CTP = GRP + 16;  // code staging row pitch (bytes) for the transposed copy
 
-__global__ void __launch_bounds__(256, 2) k_quant_weight(const uint16_t *__restrict__ w, int64_t ldw,
-                                                      uint8_t *__restrict__ q, int64_t ldq,
-                                                      float *__restrict__ s, int64_t lds,
-                                                      uint8_t *__restrict__ qT, int64_t ldqT, int64_t NB)
+__global__ void __launch_bounds__(256, 4) k_quant_weight(const uint16_t *__restrict__ w, int64_t ldw,
+                                                         uint8_t *__restrict__ q, int64_t ldq,
+                                                         float *__restrict__ s, int64_t lds,
+                                                         uint8_t *__restrict__ qT, int64_t ldqT, int64_t NB)
 {
+    __shared__ __align__(16) uint16_t wt[GRP * GRP];  // raw block, row pitch 256 bytes
     __shared__ float red[8];
-    __shared__ __align__(16) uint8_t ct[GRP * CTP];
+    uint8_t *ct = reinterpret_cast<uint8_t *>(wt);     // code staging, reuses the raw buffer
     const int t = threadIdx.x, lane = t & 31, half = lane >> 4, l16 = lane & 15, warp = t >> 5;
     const int hw16 = warp * 2 + half;
     const int64_t kb = blockIdx.x;
 
     for (int64_t nb = blockIdx.y; nb < NB; nb += gridDim.y) {
         const int64_t n0 = nb * GRP;
+        // ---- read, amax, stash
         uint4 v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -294,6 +343,7 @@ __global__ void __launch_bounds__(256, 2) k_quant_weight(const uint16_t *__restr
             float f[8];
             unpack8(v[i], f);
             a = fmaxf(a, amax8(f));
+            *reinterpret_cast<uint4 *>(&wt[(hw16 + 16 * i) * GRP + l16 * 8]) = v[i];
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1)
@@ -309,17 +359,21 @@ __global__ void __launch_bounds__(256, 2) k_quant_weight(const uint16_t *__restr
         const Quot c = make_quot(sc);
         if (t == 0)
             s[nb * lds + kb] = sc;
+        // ---- quantize from shared memory
+        uint2 cd[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float f[8];
-            unpack8(v[i], f);
-            const uint2 codes = encode8(f, c);
             const int r = hw16 + 16 * i;
-            *reinterpret_cast<uint2 *>(q + (n0 + r) * ldq + kb * GRP + l16 * 8) = codes;
-            if (qT)
-                *reinterpret_cast<uint2 *>(&ct[r * CTP + l16 * 8]) = codes;
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4 *>(&wt[r * GRP + l16 * 8]), f);
+            cd[i] = encode8(f, c);
+            *reinterpret_cast<uint2 *>(q + (n0 + r) * ldq + kb * GRP + l16 * 8) = cd[i];
         }
         if (qT) {
+            __syncthreads();  // the raw block is no longer read: reuse it for the codes
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<uint2 *>(&ct[(hw16 + 16 * i) * CTP + l16 * 8]) = cd[i];
             __syncthreads();
             // thread -> output row k0 + cc of qT, 64 consecutive n (rows nh*64 .. +63 of the block)
             const int cc = t >> 1, nh = t & 1;
@@ -335,13 +389,17 @@ __global__ void __launch_bounds__(256, 2) k_quant_weight(const uint16_t *__restr
             for (int j = 0; j < 4; ++j)
                 dst[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
         }
-        __syncthreads();  // red / ct reused by the next nb
+        __syncthreads();  // wt / red are reused by the next block
     }
 }
 
 // ---------------------------------------------------------------------------
 // UAQ fold, in place: divide (w) or multiply (prev) column k by s[k] in fp32,
-// round to bf16.  8 elements per thread, rows over blockIdx.y (grid-stride).
+// round to bf16.  8 elements per thread and vector; each thread handles FOLD_ROWS
+// rows per iteration with all their loads issued first (bytes in flight hide
+// the memory latency); row groups over blockIdx.y (grid-stride).
+constexpr int FOLD_ROWS = 4;
+
 template <bool kDivide>
 __global__ void __launch_bounds__(256) k_uaq_fold(uint16_t *__restrict__ a, int64_t rows, int64_t K8,
                                                   int64_t lda, const float *__restrict__ s)
@@ -352,21 +410,29 @@ __global__ void __launch_bounds__(256) k_uaq_fold(uint16_t *__restrict__ a, int6
     const float4 s0 = __ldg(reinterpret_cast<const float4 *>(s) + 2 * v);
     const float4 s1 = __ldg(reinterpret_cast<const float4 *>(s) + 2 * v + 1);
     const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-        uint4 *p = reinterpret_cast<uint4 *>(a + r * lda) + v;
-        const uint4 in = *p;
-        float f[8];
-        unpack8(in, f);
-        uint32_t o[4];
+    for (int64_t r0 = (int64_t)blockIdx.y * FOLD_ROWS; r0 < rows; r0 += (int64_t)gridDim.y * FOLD_ROWS) {
+        uint4 in[FOLD_ROWS];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float x0 = kDivide ? __fdiv_rn(f[2 * i], sv[2 * i]) : __fmul_rn(f[2 * i], sv[2 * i]);
-            const float x1 = kDivide ? __fdiv_rn(f[2 * i + 1], sv[2 * i + 1]) : __fmul_rn(f[2 * i + 1], sv[2 * i + 1]);
-            uint32_t pk;
-            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(pk) : "f"(x1), "f"(x0));
-            o[i] = pk;
+        for (int i = 0; i < FOLD_ROWS; ++i)
+            if (r0 + i < rows)
+                in[i] = *(reinterpret_cast<const uint4 *>(a + (r0 + i) * lda) + v);
+#pragma unroll
+        for (int i = 0; i < FOLD_ROWS; ++i) {
+            if (r0 + i >= rows)
+                break;
+            float f[8];
+            unpack8(in[i], f);
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float x0 = kDivide ? __fdiv_rn(f[2 * j], sv[2 * j]) : __fmul_rn(f[2 * j], sv[2 * j]);
+                const float x1 = kDivide ? __fdiv_rn(f[2 * j + 1], sv[2 * j + 1]) : __fmul_rn(f[2 * j + 1], sv[2 * j + 1]);
+                uint32_t pk;
+                asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(pk) : "f"(x1), "f"(x0));
+                o[j] = pk;
+            }
+            *(reinterpret_cast<uint4 *>(a + (r0 + i) * lda) + v) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        *p = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -420,16 +486,18 @@ cudaError_t launch_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, cons
 {
     const int64_t K8 = K / 8;
     const unsigned gx = (unsigned)((K8 + 255) / 256);
+    auto gy = [](int64_t rows) {
+        const int64_t g = (rows + FOLD_ROWS - 1) / FOLD_ROWS;
+        return (unsigned)(g < 65535 ? g : 65535);
+    };
     if (N > 0) {
-        const dim3 grid(gx, (unsigned)(N < 65535 ? N : 65535));
-        k_uaq_fold<true><<<grid, 256, 0, st>>>(w, N, K8, ldw, s);
+        k_uaq_fold<true><<<dim3(gx, gy(N)), 256, 0, st>>>(w, N, K8, ldw, s);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
     }
     if (prev && R > 0) {
-        const dim3 grid(gx, (unsigned)(R < 65535 ? R : 65535));
-        k_uaq_fold<false><<<grid, 256, 0, st>>>(prev, R, K8, ldp, s);
+        k_uaq_fold<false><<<dim3(gx, gy(R)), 256, 0, st>>>(prev, R, K8, ldp, s);
         return cudaGetLastError();
     }
     return cudaSuccess;
