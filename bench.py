@@ -54,6 +54,8 @@ UAQ_S = 1.5  # QuRL's recommended fold factor
 B_DUAL = 2 + 1 + 1 + 4 / 128 + 4 / 128
 B_WEIGHT_T = 2 + 1 + 1 + 4 / 16384
 B_FOLD_W = 4  # read + write bf16 per weight element
+B_ROWS = 2 + 1 + 4 / 128
+B_WEIGHT = 2 + 1 + 4 / 16384
 
 
 def _peaks():
@@ -457,6 +459,181 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+# ----------------------------------------------------------------- sweep ---
+
+SWEEP_DOC = """Per-configuration report (--sweep): every kernel of each workload timed on
+its own (3 warm-ups, 10 repetitions, median; L2 flushed before each repetition),
+against its binding roofline.  For a GEMM that is max(FLOP / FP8 peak,
+algorithmic bytes / HBM bandwidth): at small M the weight read dominates and the
+kernel is bound by HBM, not by the tensor cores."""
+
+
+def _dev_normal(gen, shape, std, outlier_frac=0.0, factor=1.0, t_frac=0.0, dev="cuda"):
+    """Seeded device-side draw with the recipes of inputs.py (for timing only)."""
+    x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+    if std != 1.0:
+        x *= std
+    K = shape[1]
+    if outlier_frac:
+        idx = torch.randperm(K, generator=gen, device=dev)[: int(np.ceil(outlier_frac * K))]
+        x[:, idx] *= factor
+    if t_frac:
+        idx = torch.randperm(K, generator=gen, device=dev)[: int(np.ceil(t_frac * K))]
+        # Student-t(3) = N / sqrt(chi2_3 / 3)
+        z = torch.randn((shape[0], idx.numel()), generator=gen, device=dev)
+        c = torch.randn((shape[0], idx.numel(), 3), generator=gen, device=dev).pow(2).sum(-1) / 3
+        x[:, idx] = z / c.sqrt()
+    return x.to(torch.bfloat16)
+
+
+def _time_ms(fn, flush, reps=10, warm=3):
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
+def run_sweep(args):
+    from fp8_block_scaled_quantize_gb300 import rlq
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    rlq.lib()
+    peaks = _peaks()
+    bw = peaks["hbm_gbs"]
+    fp8 = 2.0 * peaks["bf16_sustained"]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    rows = []
+
+    def emit(cfg, kernel, ms, nbytes=None, flop=None):
+        r = {"sweep": True, "config": cfg, "kernel": kernel, "ms": round(ms, 4)}
+        if flop is None:
+            r["gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+            r["frac_hbm"] = round(r["gbs"] / bw, 3)
+            r["bound"] = "hbm"
+        else:
+            r["tflops"] = round(flop / (ms * 1e-3) / 1e12, 1)
+            t_roof = max(flop / (fp8 * 1e12), nbytes / (bw * 1e9)) * 1e3
+            r["bound"] = "tensor" if flop / (fp8 * 1e12) >= nbytes / (bw * 1e9) else "hbm"
+            r["frac_roofline"] = round(t_roof / ms, 3)
+            r["frac_fp8_peak"] = round(r["tflops"] / fp8, 3)
+        rows.append(r)
+        print(json.dumps(r), flush=True)
+
+    def _splitk_ws(kind, M, N, K):
+        """Workspace for the split-K plan of this GEMM, None when it runs one pass
+        (the split rows are then not reported)."""
+        nb = rlq.rlq_gemm_splitk_workspace_bytes(kind, M, N, K)
+        return torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+
+    def gemm_bytes(Mr, Nc, L):
+        return Mr * L + Nc * L + 2 * Mr * Nc + 4 * (Mr + Nc) * ((L + 127) // 128)
+
+    def linear(cfg, x, w, dy=None, s=None, full=False):
+        """Time the quantizers, fold and GEMMs of one linear layer."""
+        M, K = x.shape
+        N = w.shape[0]
+        if s is not None:
+            st = torch.from_numpy(s).to(dev)
+            inv = (1.0 / st).contiguous()
+            wf, xf = w.clone(), x.clone()
+            par = [0]
+
+            def fold():
+                # alternate s and 1/s so repeated folds keep the tensors stationary
+                rlq.uaq_fold_(wf, st if par[0] == 0 else inv, xf)
+                par[0] ^= 1
+            emit(cfg, "uaq_fold", _time_ms(fold, flush), nbytes=4 * (N * K + M * K))
+        emit(cfg, "quant_rows_x", _time_ms(lambda: rlq.quant_act_1x128(x), flush), nbytes=B_ROWS * M * K)
+        if full:
+            emit(cfg, "quant_dual_x", _time_ms(lambda: rlq.quant_act_1x128(x, colwise=True), flush),
+                 nbytes=B_DUAL * M * K)
+        emit(cfg, "quant_weight" + ("_t" if full else ""),
+             _time_ms(lambda: rlq.quant_weight_128x128(w, transposed=full), flush),
+             nbytes=(B_WEIGHT_T if full else B_WEIGHT) * N * K)
+        qx, sx, qxT, sxc = rlq.quant_act_1x128(x, colwise=full)
+        qw, sw, qwT = rlq.quant_weight_128x128(w, transposed=full)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        emit(cfg, "gemm_fprop", _time_ms(lambda: rlq.gemm_fprop(qx, sx, qw, sw, out=y), flush),
+             nbytes=gemm_bytes(M, N, K), flop=2.0 * M * N * K)
+        ws = _splitk_ws(rlq.GEMM_FPROP, M, N, K)
+        if ws is not None:
+            emit(cfg, "gemm_fprop_splitk",
+                 _time_ms(lambda: rlq.gemm_fprop(qx, sx, qw, sw, out=y, split_k=True, workspace=ws), flush),
+                 nbytes=gemm_bytes(M, N, K), flop=2.0 * M * N * K)
+        if full:
+            emit(cfg, "quant_dual_dy", _time_ms(lambda: rlq.quant_act_1x128(dy, colwise=True), flush),
+                 nbytes=B_DUAL * M * N)
+            qdy, sdy, qdyT, sdyc = rlq.quant_act_1x128(dy, colwise=True)
+            dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+            dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+            emit(cfg, "gemm_dgrad", _time_ms(lambda: rlq.gemm_dgrad(qdy, sdy, qwT, sw, out=dx), flush),
+                 nbytes=gemm_bytes(M, K, N), flop=2.0 * M * N * K)
+            ws = _splitk_ws(rlq.GEMM_DGRAD, M, N, K)
+            if ws is not None:
+                emit(cfg, "gemm_dgrad_splitk",
+                     _time_ms(lambda: rlq.gemm_dgrad(qdy, sdy, qwT, sw, out=dx, split_k=True, workspace=ws), flush),
+                     nbytes=gemm_bytes(M, K, N), flop=2.0 * M * N * K)
+            emit(cfg, "gemm_wgrad", _time_ms(lambda: rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc, out=dw), flush),
+                 nbytes=gemm_bytes(N, K, M), flop=2.0 * M * N * K)
+            ws = _splitk_ws(rlq.GEMM_WGRAD, M, N, K)
+            if ws is not None:
+                emit(cfg, "gemm_wgrad_splitk",
+                     _time_ms(lambda: rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc, out=dw, split_k=True, workspace=ws),
+                              flush),
+                     nbytes=gemm_bytes(N, K, M), flop=2.0 * M * N * K)
+        rlq.check()
+
+    from fp8_block_scaled_quantize_gb300 import inputs as I
+    gen = torch.Generator(device=dev)
+    # tiny single linear, fold with s = 4
+    d = I.tiny_single_linear()
+    linear("tiny_single_linear M=128 N=256 K=256", I.to_torch(d["x"], dev), I.to_torch(d["w"], dev), s=d["s"])
+    # decode up-projection, 8B shapes
+    gen.manual_seed(1)
+    linear("decode_upproj_8b M=256 N=14336 K=4096", _dev_normal(gen, (256, 4096), 1.0, 0.01, 20.0),
+           _dev_normal(gen, (14336, 4096), 0.02))
+    # 8B training step
+    gen.manual_seed(2)
+    linear("train_step_8b M=8192 N=14336 K=4096", _dev_normal(gen, (8192, 4096), 1.0),
+           _dev_normal(gen, (14336, 4096), 0.02), dy=_dev_normal(gen, (8192, 14336), 1e-3), full=True)
+    # Qwen2.5-7B layer set: fold + quant + FProp
+    gen.manual_seed(3)
+    for which, (N, K) in (("gate_up", (18944, 3584)), ("down", (3584, 18944))):
+        w = _dev_normal(gen, (N, K), 0.02)
+        s = np.random.default_rng(3).uniform(1.5, 4.0, K).astype(np.float32)
+        for M in I.QWEN7B_M:
+            linear(f"qwen7b_{which} M={M} N={N} K={K}", _dev_normal(gen, (M, K), 1.0, t_frac=0.01), w, s=s)
+        del w
+    # 32B sweep: all three passes per M
+    gen.manual_seed(4)
+    for orient, (N, K) in (("up", (27648, 5120)), ("down", (5120, 27648))):
+        w = _dev_normal(gen, (N, K), 0.015)
+        for M in I.SWEEP_32B_M:
+            x = _dev_normal(gen, (M, K), 1.0, 0.005, 50.0)
+            dy = _dev_normal(gen, (M, N), 1e-3)
+            linear(f"sweep_32b_{orient} M={M} N={N} K={K}", x, w, dy=dy, full=True)
+            del x, dy
+            torch.cuda.empty_cache()
+        del w
+    if args.sweep_md:
+        with open(args.sweep_md, "w") as f:
+            f.write("| Config | Kernel | ms | TFLOP/s | GB/s | bound | fraction of roofline |\n|---|---|---:|---:|---:|---|---:|\n")
+            for r in rows:
+                frac = r.get("frac_roofline", r.get("frac_hbm"))
+                f.write(f"| {r['config']} | {r['kernel']} | {r['ms']} | {r.get('tflops', '')} | {r.get('gbs', '')} | "
+                        f"{r['bound']} | {frac} |\n")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -468,10 +645,14 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--ref-cols", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help=SWEEP_DOC)
+    ap.add_argument("--sweep-md", default=None, help="also write the sweep as a markdown table to this path")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -133,9 +133,20 @@ rlq_status rlq_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int
                        "128x128 quantizer launch");
 }
 
-rlq_status rlq_gemm_fprop(const uint8_t *xq, int64_t ldxq, const float *xs, int64_t ldxs, const uint8_t *wq,
-                          int64_t ldwq, const float *ws, int64_t ldws, uint16_t *y, int64_t ldy, int64_t M, int64_t N,
-                          int64_t K, rlq_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+rlq_status check_workspace(const void *workspace, int64_t workspace_bytes)
+{
+    RLQ_REQUIRE(workspace_bytes >= 0, RLQ_ERR_INVALID_ARG, "workspace_bytes is negative");
+    RLQ_REQUIRE(al(workspace, 16), RLQ_ERR_MISALIGNED, "workspace is not 16-byte aligned");
+    return RLQ_OK;
+}
+
+rlq_status gemm_fprop(const uint8_t *xq, int64_t ldxq, const float *xs, int64_t ldxs, const uint8_t *wq, int64_t ldwq,
+                      const float *ws, int64_t ldws, uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                      void *workspace, int64_t workspace_bytes, rlq_stream_t stream)
 {
     RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
     RLQ_REQUIRE(N % G == 0 && K % G == 0, RLQ_ERR_UNSUPPORTED, "N=%lld and K=%lld must be multiples of 128",
@@ -166,12 +177,14 @@ rlq_status rlq_gemm_fprop(const uint8_t *xq, int64_t ldxq, const float *xs, int6
     a.R = M;
     a.C = N;
     a.L = K;
+    a.ws = static_cast<float *>(workspace);
+    a.ws_bytes = workspace_bytes;
     return launch_gemm(a, cs(stream));
 }
 
-rlq_status rlq_gemm_dgrad(const uint8_t *dyq, int64_t lddyq, const float *dys, int64_t lddys, const uint8_t *w,
-                          int64_t ldw, int wq_is_transposed, const float *ws, int64_t ldws, uint16_t *dx, int64_t lddx,
-                          int64_t M, int64_t N, int64_t K, rlq_stream_t stream)
+rlq_status gemm_dgrad(const uint8_t *dyq, int64_t lddyq, const float *dys, int64_t lddys, const uint8_t *w, int64_t ldw,
+                      int wq_is_transposed, const float *ws, int64_t ldws, uint16_t *dx, int64_t lddx, int64_t M,
+                      int64_t N, int64_t K, void *workspace, int64_t workspace_bytes, rlq_stream_t stream)
 {
     RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
     RLQ_REQUIRE(N % G == 0 && K % G == 0, RLQ_ERR_UNSUPPORTED, "N=%lld and K=%lld must be multiples of 128",
@@ -208,12 +221,14 @@ rlq_status rlq_gemm_dgrad(const uint8_t *dyq, int64_t lddyq, const float *dys, i
     a.R = M;
     a.C = K;
     a.L = N;
+    a.ws = static_cast<float *>(workspace);
+    a.ws_bytes = workspace_bytes;
     return launch_gemm(a, cs(stream));
 }
 
-rlq_status rlq_gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, int64_t lddysc, const uint8_t *xqT,
-                          int64_t ldxqT, const float *xsc, int64_t ldxsc, uint16_t *dw, int64_t lddw, int64_t M,
-                          int64_t N, int64_t K, rlq_stream_t stream)
+rlq_status gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, int64_t lddysc, const uint8_t *xqT,
+                      int64_t ldxqT, const float *xsc, int64_t ldxsc, uint16_t *dw, int64_t lddw, int64_t M, int64_t N,
+                      int64_t K, void *workspace, int64_t workspace_bytes, rlq_stream_t stream)
 {
     RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
     RLQ_REQUIRE(N % G == 0 && K % G == 0, RLQ_ERR_UNSUPPORTED, "N=%lld and K=%lld must be multiples of 128",
@@ -246,7 +261,86 @@ rlq_status rlq_gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc
     a.R = N;
     a.C = K;
     a.L = M;
+    a.ws = static_cast<float *>(workspace);
+    a.ws_bytes = workspace_bytes;
     return launch_gemm(a, cs(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+rlq_status rlq_gemm_fprop(const uint8_t *xq, int64_t ldxq, const float *xs, int64_t ldxs, const uint8_t *wq,
+                          int64_t ldwq, const float *ws, int64_t ldws, uint16_t *y, int64_t ldy, int64_t M, int64_t N,
+                          int64_t K, rlq_stream_t stream)
+{
+    return gemm_fprop(xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, nullptr, 0, stream);
+}
+
+rlq_status rlq_gemm_dgrad(const uint8_t *dyq, int64_t lddyq, const float *dys, int64_t lddys, const uint8_t *w,
+                          int64_t ldw, int wq_is_transposed, const float *ws, int64_t ldws, uint16_t *dx, int64_t lddx,
+                          int64_t M, int64_t N, int64_t K, rlq_stream_t stream)
+{
+    return gemm_dgrad(dyq, lddyq, dys, lddys, w, ldw, wq_is_transposed, ws, ldws, dx, lddx, M, N, K, nullptr, 0,
+                      stream);
+}
+
+rlq_status rlq_gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, int64_t lddysc, const uint8_t *xqT,
+                          int64_t ldxqT, const float *xsc, int64_t ldxsc, uint16_t *dw, int64_t lddw, int64_t M,
+                          int64_t N, int64_t K, rlq_stream_t stream)
+{
+    return gemm_wgrad(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K, nullptr, 0, stream);
+}
+
+rlq_status rlq_gemm_splitk_workspace_bytes(rlq_gemm_kind kind, int64_t M, int64_t N, int64_t K, int64_t *bytes)
+{
+    RLQ_REQUIRE(bytes, RLQ_ERR_INVALID_ARG, "bytes is NULL");
+    RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
+    RLQ_REQUIRE(M < MAX_DIM && N < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    int64_t R, C, L;
+    switch (kind) {
+    case RLQ_GEMM_FPROP:
+        R = M, C = N, L = K;
+        break;
+    case RLQ_GEMM_DGRAD:
+        R = M, C = K, L = N;
+        break;
+    case RLQ_GEMM_WGRAD:
+        R = N, C = K, L = M;
+        break;
+    default:
+        return fail(RLQ_ERR_INVALID_ARG, "unknown GEMM kind %d", (int)kind);
+    }
+    int splits = 1;
+    return plan_splitk(R, C, L, -1, &splits, bytes);
+}
+
+rlq_status rlq_gemm_fprop_splitk(const uint8_t *xq, int64_t ldxq, const float *xs, int64_t ldxs, const uint8_t *wq,
+                                 int64_t ldwq, const float *ws, int64_t ldws, uint16_t *y, int64_t ldy, int64_t M,
+                                 int64_t N, int64_t K, void *workspace, int64_t workspace_bytes, rlq_stream_t stream)
+{
+    RLQ_TRY(check_workspace(workspace, workspace_bytes));
+    return gemm_fprop(xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, workspace, workspace_bytes, stream);
+}
+
+rlq_status rlq_gemm_dgrad_splitk(const uint8_t *dyq, int64_t lddyq, const float *dys, int64_t lddys, const uint8_t *w,
+                                 int64_t ldw, int wq_is_transposed, const float *ws, int64_t ldws, uint16_t *dx,
+                                 int64_t lddx, int64_t M, int64_t N, int64_t K, void *workspace,
+                                 int64_t workspace_bytes, rlq_stream_t stream)
+{
+    RLQ_TRY(check_workspace(workspace, workspace_bytes));
+    return gemm_dgrad(dyq, lddyq, dys, lddys, w, ldw, wq_is_transposed, ws, ldws, dx, lddx, M, N, K, workspace,
+                      workspace_bytes, stream);
+}
+
+rlq_status rlq_gemm_wgrad_splitk(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, int64_t lddysc,
+                                 const uint8_t *xqT, int64_t ldxqT, const float *xsc, int64_t ldxsc, uint16_t *dw,
+                                 int64_t lddw, int64_t M, int64_t N, int64_t K, void *workspace,
+                                 int64_t workspace_bytes, rlq_stream_t stream)
+{
+    RLQ_TRY(check_workspace(workspace, workspace_bytes));
+    return gemm_wgrad(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K, workspace,
+                      workspace_bytes, stream);
 }
 
 rlq_status rlq_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, const float *s, uint16_t *prev, int64_t R,

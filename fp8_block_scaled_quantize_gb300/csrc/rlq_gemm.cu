@@ -215,6 +215,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"((uint64_t)map), "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
@@ -334,8 +341,17 @@ struct Params {
     int kblocks;
     int m_tiles, n_tiles, num_tiles;
     int m_fastest;
+    // split-K: unit u covers tile u / splits and contraction blocks
+    // [(u % splits) * kbps, min(kblocks, ... + kbps)); with splits > 1 the
+    // epilogue writes fp32 partials to the workspace [splits][R][C]
+    int splits, kbps, num_units;
     uint64_t timeout_ns;
 };
+
+struct Unit {
+    int mt, nt, split, kb0, kb1;
+};
+
 
 __device__ __forceinline__ void tile_coords(const Params &p, int tile, int &mt, int &nt)
 {
@@ -348,10 +364,22 @@ __device__ __forceinline__ void tile_coords(const Params &p, int tile, int &mt, 
     }
 }
 
+__device__ __forceinline__ Unit unit_of(const Params &p, int u)
+{
+    Unit w;
+    const int tile = u / p.splits;
+    w.split = u - tile * p.splits;
+    tile_coords(p, tile, w.mt, w.nt);
+    w.kb0 = w.split * p.kbps;
+    w.kb1 = min(p.kblocks, w.kb0 + p.kbps);
+    return w;
+}
+
 template <bool kColScaleB, bool kBMajorMN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_block_scaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmOut, const Params p)
+                        const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmWs,
+                        const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -401,6 +429,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmOut);
+        if (p.splits > 1)
+            prefetch_tmap(&tmWs);
     }
     tc_fence_before();
     __syncthreads();
@@ -414,10 +444,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                int mt, nt;
-                tile_coords(p, tile, mt, nt);
-                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const Unit w = unit_of(p, u);
+                const int mt = w.mt, nt = w.nt;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.timeout_ns, SITE_PRODUCER_EMPTY)) {
@@ -449,8 +479,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const Unit w = unit_of(p, u);
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     const int buf = it & 1;
@@ -484,10 +515,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------ scale loader ---
         int it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            int mt, nt;
-            tile_coords(p, tile, mt, nt);
-            for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const Unit w = unit_of(p, u);
+            const int mt = w.mt, nt = w.nt;
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                 const int k = it % SCALE_SLOTS;
                 const uint32_t ph = (uint32_t)(it / SCALE_SLOTS) & 1u;
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(sempty_bar(k), ph ^ 1u, abort_flag, p.timeout_ns,
@@ -527,9 +558,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         int it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            int mt, nt;
-            tile_coords(p, tile, mt, nt);
+        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const Unit wu = unit_of(p, u);
+            const int mt = wu.mt, nt = wu.nt;
             const int grow = mt * BM + row;
             const bool row_ok = grow < p.R;
             const int col0 = nt * BN + h * 128;
@@ -538,7 +569,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 64; ++j)
                 acc[j] = make_float2(0.0f, 0.0f);
-            for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+            for (int kb = wu.kb0; kb < wu.kb1; ++kb, ++it) {
                 const int buf = it & 1;
                 const uint32_t bph = (uint32_t)(it >> 1) & 1u;
                 const int k = it % SCALE_SLOTS;
@@ -594,7 +625,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_arrive(sempty_bar(k));
                 }
             }
-            if (ok) {
+            if (ok && p.splits > 1) {
+                // fp32 partial of this contraction range into plane `split` of the
+                // workspace [splits][R][C] (reduced by k_splitk_reduce): two rounds
+                // of two 32x32 boxes (rows of 128 bytes, swizzled as below)
+                const uint32_t stg = smem_u32(staging) + (uint32_t)((warp - FIRST_EPI_WARP) * 2 * 32 * 128);
+#pragma unroll
+                for (int rd = 0; rd < 2; ++rd) {
+                    if (lane == 0)
+                        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    __syncwarp();
+#pragma unroll
+                    for (int v = 0; v < 16; ++v) {
+                        const uint32_t addr = stg + (uint32_t)((v >> 3) * 32 * 128 + lane * 128 +
+                                                               ((((v & 7) ^ (lane & 7))) << 4));
+                        const int j = rd * 32 + 2 * v;  // columns 2j .. 2j+3 of this half
+                        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(acc[j].x), "f"(acc[j].y)
+                                     : "memory");
+                        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr + 8), "f"(acc[j + 1].x),
+                                     "f"(acc[j + 1].y)
+                                     : "memory");
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0 && half_ok) {
+                        tma_store_3d(&tmWs, stg, col0 + rd * 64, mt * BM + q * 32, wu.split);
+                        tma_store_3d(&tmWs, stg + 32 * 128, col0 + rd * 64 + 32, mt * BM + q * 32, wu.split);
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    }
+                }
+            } else if (ok) {
                 // this warp's 32 rows x 128 columns: two 32x64 boxes, rows of
                 // 128 bytes with the 16-byte chunks XOR-swizzled by (row % 8)
                 const uint32_t stg = smem_u32(staging) + (uint32_t)((warp - FIRST_EPI_WARP) * 2 * 32 * 128);
@@ -649,6 +709,30 @@ __global__ void k_diag_wait(uint64_t limit_ns)
         mbar_wait(smem_u32(&bar), 0, &abort_flag, limit_ns, SITE_DIAG);
 }
 
+// Split-K reduction: out[r, c] = bf16_RN(sum over splits s, in order, of
+// ws[(s * R + r) * C + c]); eight columns per thread (C % 128 == 0).
+__global__ void __launch_bounds__(256) k_splitk_reduce(const float *__restrict__ ws, int splits, int R, int C,
+                                                       uint16_t *__restrict__ out, int64_t ldo)
+{
+    const int64_t per_row = C / 8;
+    const int64_t total = (int64_t)R * per_row;
+    const int64_t plane = (int64_t)R * C;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / per_row, c = (i - r * per_row) * 8;
+        const float4 *src = reinterpret_cast<const float4 *>(ws + r * C + c);
+        float4 a = src[0], b = src[1];
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4 *t = reinterpret_cast<const float4 *>(ws + sp * plane + r * C + c);
+            const float4 x = t[0], y = t[1];
+            a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+            b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+        }
+        *reinterpret_cast<uint4 *>(out + r * ldo + c) =
+            make_uint4(bf16x2_rn(make_float2(a.x, a.y)), bf16x2_rn(make_float2(a.z, a.w)),
+                       bf16x2_rn(make_float2(b.x, b.y)), bf16x2_rn(make_float2(b.z, b.w)));
+    }
+}
+
 // ---------------------------------------------------------------- host ---
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
@@ -698,6 +782,24 @@ rlq_status encode_out_map(CUtensorMap *map, uint16_t *base, int64_t cols, int64_
     return RLQ_OK;
 }
 
+// fp32 split-K workspace [splits][rows][cols], dense; box 32 columns x 32 rows x 1, 128-byte swizzle.
+rlq_status encode_ws_map(CUtensorMap *map, float *base, int64_t cols, int64_t rows, int splits)
+{
+    auto enc = get_encode_fn();
+    if (!enc)
+        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)splits};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)(cols * rows * 4)};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for the split-K workspace", (int)r);
+    return RLQ_OK;
+}
+
 // 2-D E4M3 tensor [rows][inner] with row pitch `ld` bytes; box 128 x box_rows.
 rlq_status encode_map(CUtensorMap *map, const uint8_t *base, int64_t inner, int64_t rows, int64_t ld, int box_rows)
 {
@@ -736,8 +838,52 @@ DevInfo &dev_info(int dev)
     return d;
 }
 
+// ---- split-K planning ----
+//
+// Estimated time of an R x C x L GEMM cut into S contraction splits: the
+// persistent grid runs ceil(tiles * S / SMs) waves of units, each unit streams
+// ceil(kblocks / S) blocks of 128 x 256 x 128 plus a fixed fill/drain cost;
+// splitting adds the fp32 partial planes (written once, read once) and the
+// reduction launch.  Figures are per-SM steady-state rates of this kernel.
+constexpr double SPLIT_T_BLOCK_US = 0.55;   // one 128x256x128 block on one SM
+constexpr double SPLIT_T_UNIT_US = 1.5;     // pipeline fill + epilogue drain per unit
+constexpr double SPLIT_T_REDUCE_US = 3.0;   // reduction launch and tail
+constexpr double SPLIT_HBM_BYTES_US = 6.0e6;
+constexpr int SPLIT_MAX = 16;
+constexpr int SPLIT_MIN_BLOCKS = 4;         // contraction blocks per unit, at least
+
+int plan_splits(int64_t R, int64_t C, int64_t L, int sms, int64_t ws_cap)
+{
+    const int64_t kblocks = (L + BK - 1) / BK;
+    const int64_t tiles = ((R + BM - 1) / BM) * ((C + BN - 1) / BN);
+    if (tiles == 0 || kblocks < 2 * SPLIT_MIN_BLOCKS)
+        return 1;
+    const double plane = (double)R * (double)C * 4.0;
+    int best = 1;
+    double best_t = 0.0;
+    int prev_splits = 0;
+    for (int s = 1; s <= SPLIT_MAX && s * SPLIT_MIN_BLOCKS <= kblocks; ++s) {
+        const int64_t kbps = (kblocks + s - 1) / s;
+        const int splits = (int)((kblocks + kbps - 1) / kbps);  // every split non-empty
+        if (splits == prev_splits)
+            continue;
+        prev_splits = splits;
+        if (splits > 1 && ws_cap >= 0 && (double)splits * plane > (double)ws_cap)
+            break;
+        const int64_t waves = (tiles * splits + sms - 1) / sms;
+        double t = (double)waves * ((double)kbps * SPLIT_T_BLOCK_US + SPLIT_T_UNIT_US);
+        if (splits > 1)
+            t += (2.0 * splits * plane + (double)R * C * 2.0) / SPLIT_HBM_BYTES_US + SPLIT_T_REDUCE_US;
+        if (splits == 1 || t < 0.97 * best_t) {  // a split must pay for itself clearly
+            best = splits;
+            best_t = t;
+        }
+    }
+    return best;
+}
+
 template <bool kCol, bool kBMN>
-rlq_status launch_impl(const GemmArgs &a, cudaStream_t st)
+rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
 {
     CUtensorMap tmA, tmB, tmO;
     rlq_status rs = encode_map(&tmA, a.A, a.L, a.R, a.lda, BM);
@@ -780,9 +926,36 @@ rlq_status launch_impl(const GemmArgs &a, cudaStream_t st)
     // keep the smaller operand resident in L2: sweep the tiles along it
     p.m_fastest = (a.R * a.L <= a.C * a.L) ? 1 : 0;
     p.timeout_ns = wait_limit_ns();
-    const int grid = p.num_tiles < di.sms ? p.num_tiles : di.sms;
-    k_gemm_block_scaled<kCol, kBMN><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, tmO, p);
-    return cuda_status(cudaGetLastError(), "block-scaled GEMM launch");
+    p.kbps = (p.kblocks + splits - 1) / splits;
+    p.splits = (p.kblocks + p.kbps - 1) / p.kbps;
+    p.num_units = p.num_tiles * p.splits;
+    CUtensorMap tmW = tmO;  // not read with one split
+    if (p.splits > 1) {
+        rs = encode_ws_map(&tmW, a.ws, a.C, a.R, p.splits);
+        if (rs != RLQ_OK)
+            return rs;
+    }
+    const int grid = p.num_units < di.sms ? p.num_units : di.sms;
+    k_gemm_block_scaled<kCol, kBMN><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, tmO, tmW, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.splits == 1)
+        return cuda_status(e, "block-scaled GEMM launch");
+    const int64_t total = a.R * (a.C / 8);
+    int64_t rgrid = (total + 255) / 256;
+    if (rgrid > (int64_t)di.sms * 8)
+        rgrid = (int64_t)di.sms * 8;
+    k_splitk_reduce<<<(int)rgrid, 256, 0, st>>>(a.ws, p.splits, p.R, p.C, a.out, a.ldo);
+    return cuda_status(cudaGetLastError(), "split-K reduction launch");
+}
+
+rlq_status current_sms(int *sms)
+{
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_status(e, "cudaGetDevice");
+    *sms = dev_info(dev).sms;
+    return RLQ_OK;
 }
 
 }  // namespace
@@ -796,9 +969,28 @@ rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st)
         return cuda_status(cudaMemset2DAsync(a.out, (size_t)a.ldo * 2, 0, (size_t)a.C * 2, (size_t)a.R, st),
                            "cudaMemset2DAsync (empty contraction)");
     }
+    int splits = 1;
+    if (a.ws) {
+        int64_t bytes = 0;
+        const rlq_status rs = plan_splitk(a.R, a.C, a.L, a.ws_bytes, &splits, &bytes);
+        if (rs != RLQ_OK)
+            return rs;
+    }
     if (a.per_col_sb)
-        return launch_impl<true, false>(a, st);
-    return a.b_mn_major ? launch_impl<false, true>(a, st) : launch_impl<false, false>(a, st);
+        return launch_impl<true, false>(a, splits, st);
+    return a.b_mn_major ? launch_impl<false, true>(a, splits, st) : launch_impl<false, false>(a, splits, st);
+}
+
+rlq_status plan_splitk(int64_t R, int64_t C, int64_t L, int64_t ws_cap, int *splits, int64_t *ws_bytes)
+{
+    int sms = 0;
+    const rlq_status rs = current_sms(&sms);
+    if (rs != RLQ_OK)
+        return rs;
+    int s = (R > 0 && C > 0 && L > 0) ? plan_splits(R, C, L, sms, ws_cap) : 1;
+    *splits = s;
+    *ws_bytes = s > 1 ? (int64_t)s * R * C * 4 : 0;
+    return RLQ_OK;
 }
 
 rlq_status check_device_errors(cudaStream_t st)

@@ -53,8 +53,17 @@ struct GemmArgs {
     uint16_t *out;
     int64_t ldo;
     int64_t R, C, L;
+    // split-K workspace (16-byte aligned fp32), or NULL for the single-pass GEMM
+    float *ws;
+    int64_t ws_bytes;
 };
 rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st);
+
+// Number of contraction splits the split-K GEMM uses for an [R x C] output
+// with contraction length L on the current device, and the workspace bytes
+// (splits * R * C * 4, or 0 for one split) it needs.  ws_cap limits the
+// workspace (-1: no limit).
+rlq_status plan_splitk(int64_t R, int64_t C, int64_t L, int64_t ws_cap, int *splits, int64_t *ws_bytes);
 
 // Reads and clears the device error word of the current device (after syncing st).
 rlq_status check_device_errors(cudaStream_t st);

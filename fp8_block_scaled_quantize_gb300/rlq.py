@@ -29,6 +29,10 @@ _SIGS = {
     "rlq_gemm_fprop": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
     "rlq_gemm_dgrad": [_P, _I, _P, _I, _P, _I, ctypes.c_int, _P, _I, _P, _I, _I, _I, _I, _P],
     "rlq_gemm_wgrad": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
+    "rlq_gemm_splitk_workspace_bytes": [ctypes.c_int, _I, _I, _I, ctypes.POINTER(_I)],
+    "rlq_gemm_fprop_splitk": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
+    "rlq_gemm_dgrad_splitk": [_P, _I, _P, _I, _P, _I, ctypes.c_int, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
+    "rlq_gemm_wgrad_splitk": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_uaq_fold": [_P, _I, _I, _I, _P, _P, _I, _I, _P],
     "rlq_check": [_P],
     "rlq_diag_bounded_wait": [_I, _P],
@@ -104,6 +108,33 @@ def rlq_gemm_dgrad(dyq, lddyq, dys, lddys, w, ldw, wq_is_transposed, ws, ldws, d
 
 def rlq_gemm_wgrad(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K, stream):
     return _call("rlq_gemm_wgrad", dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K, stream)
+
+
+GEMM_FPROP, GEMM_DGRAD, GEMM_WGRAD = 0, 1, 2
+
+
+def rlq_gemm_splitk_workspace_bytes(kind, M, N, K) -> int:
+    out = _I(0)
+    _call("rlq_gemm_splitk_workspace_bytes", kind, M, N, K, ctypes.byref(out))
+    return out.value
+
+
+def rlq_gemm_fprop_splitk(xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, workspace, workspace_bytes,
+                          stream):
+    return _call("rlq_gemm_fprop_splitk", xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, workspace,
+                 workspace_bytes, stream)
+
+
+def rlq_gemm_dgrad_splitk(dyq, lddyq, dys, lddys, w, ldw, wq_is_transposed, ws, ldws, dx, lddx, M, N, K, workspace,
+                          workspace_bytes, stream):
+    return _call("rlq_gemm_dgrad_splitk", dyq, lddyq, dys, lddys, w, ldw, wq_is_transposed, ws, ldws, dx, lddx,
+                 M, N, K, workspace, workspace_bytes, stream)
+
+
+def rlq_gemm_wgrad_splitk(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K, workspace,
+                          workspace_bytes, stream):
+    return _call("rlq_gemm_wgrad_splitk", dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K,
+                 workspace, workspace_bytes, stream)
 
 
 def rlq_uaq_fold(w, N, K, ldw, s, prev, R, ldp, stream):
@@ -199,34 +230,61 @@ def quant_weight_128x128(w: torch.Tensor, transposed: bool = False, stream=None)
     return q, s, qT
 
 
-def gemm_fprop(xq, xs, wq, ws, out=None, stream=None):
-    """Y [M, N] bf16 = X W^T from 1x128 X codes and 128x128 W codes."""
+def _workspace(kind: int, M: int, N: int, K: int, workspace, device):
+    """(pointer, bytes) of the split-K workspace: the caller's uint8 tensor, or
+    one allocated with torch for the library's plan (None when it is one pass)."""
+    if workspace is None:
+        nbytes = rlq_gemm_splitk_workspace_bytes(kind, M, N, K)
+        if nbytes == 0:
+            return None, 0
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def gemm_fprop(xq, xs, wq, ws, out=None, stream=None, split_k: bool = False, workspace=None):
+    """Y [M, N] bf16 = X W^T from 1x128 X codes and 128x128 W codes.
+
+    ``split_k`` runs the split-K form with ``workspace`` (a device tensor) or
+    a workspace allocated here for the library's plan."""
     M, K = xq.shape
     N = wq.shape[0]
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
-    rlq_gemm_fprop(xq.data_ptr(), _ld(xq), xs.data_ptr(), _ld(xs), wq.data_ptr(), _ld(wq), ws.data_ptr(), _ld(ws),
-                   y.data_ptr(), _ld(y), M, N, K, _stream(stream))
+    args = (xq.data_ptr(), _ld(xq), xs.data_ptr(), _ld(xs), wq.data_ptr(), _ld(wq), ws.data_ptr(), _ld(ws),
+            y.data_ptr(), _ld(y), M, N, K)
+    if split_k:
+        rlq_gemm_fprop_splitk(*args, *_workspace(GEMM_FPROP, M, N, K, workspace, xq.device), _stream(stream))
+    else:
+        rlq_gemm_fprop(*args, _stream(stream))
     return y
 
 
-def gemm_dgrad(dyq, dys, w, ws, transposed: bool = True, out=None, stream=None):
+def gemm_dgrad(dyq, dys, w, ws, transposed: bool = True, out=None, stream=None, split_k: bool = False,
+               workspace=None):
     """dX [M, K] bf16 = dY W.  ``w`` is the transposed weight codes [K, N]
     (``transposed=True``) or the FProp codes [N, K]."""
     M, N = dyq.shape
     K = w.shape[0] if transposed else w.shape[1]
     dx = out if out is not None else torch.empty((M, K), dtype=torch.bfloat16, device=dyq.device)
-    rlq_gemm_dgrad(dyq.data_ptr(), _ld(dyq), dys.data_ptr(), _ld(dys), w.data_ptr(), _ld(w), 1 if transposed else 0,
-                   ws.data_ptr(), _ld(ws), dx.data_ptr(), _ld(dx), M, N, K, _stream(stream))
+    args = (dyq.data_ptr(), _ld(dyq), dys.data_ptr(), _ld(dys), w.data_ptr(), _ld(w), 1 if transposed else 0,
+            ws.data_ptr(), _ld(ws), dx.data_ptr(), _ld(dx), M, N, K)
+    if split_k:
+        rlq_gemm_dgrad_splitk(*args, *_workspace(GEMM_DGRAD, M, N, K, workspace, dyq.device), _stream(stream))
+    else:
+        rlq_gemm_dgrad(*args, _stream(stream))
     return dx
 
 
-def gemm_wgrad(dyqT, dysc, xqT, xsc, out=None, stream=None):
+def gemm_wgrad(dyqT, dysc, xqT, xsc, out=None, stream=None, split_k: bool = False, workspace=None):
     """dW [N, K] bf16 = dY^T X from the 128x1 (transposed) codes of dY and X."""
     N, M = dyqT.shape
     K = xqT.shape[0]
     dw = out if out is not None else torch.empty((N, K), dtype=torch.bfloat16, device=dyqT.device)
-    rlq_gemm_wgrad(dyqT.data_ptr(), _ld(dyqT), dysc.data_ptr(), _ld(dysc), xqT.data_ptr(), _ld(xqT),
-                   xsc.data_ptr(), _ld(xsc), dw.data_ptr(), _ld(dw), M, N, K, _stream(stream))
+    args = (dyqT.data_ptr(), _ld(dyqT), dysc.data_ptr(), _ld(dysc), xqT.data_ptr(), _ld(xqT),
+            xsc.data_ptr(), _ld(xsc), dw.data_ptr(), _ld(dw), M, N, K)
+    if split_k:
+        rlq_gemm_wgrad_splitk(*args, *_workspace(GEMM_WGRAD, M, N, K, workspace, dyqT.device), _stream(stream))
+    else:
+        rlq_gemm_wgrad(*args, _stream(stream))
     return dw
 
 

@@ -158,6 +158,53 @@ rlq_status rlq_gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc
                           rlq_stream_t stream);
 
 /*
+ * Split-K forms of the three GEMMs, for outputs too small to occupy every SM
+ * (decode-sized M in FProp and DGrad, a narrow layer's WGrad).  The pages'
+ * GEMMs do not prescribe a tiling; this is a scheduling choice of this
+ * library.  The result follows the same formula as the single-pass call, with
+ * the sum over contraction blocks taken in two levels: each split sums a
+ * contiguous range of 128-blocks in fp32 (as the single-pass kernel does over
+ * all of them), the split sums are added in split order in fp32, and the total
+ * is rounded to bf16 once.  Results are deterministic (no atomics) but may
+ * differ from the single-pass call in the last bits of the fp32 sum.
+ *
+ *   workspace        device scratch owned by the caller, 16-byte aligned, or
+ *                    NULL (then the call is the single-pass GEMM); the kernels
+ *                    write it before they read it, so its contents on entry
+ *                    do not matter.  It must not be used by anything else
+ *                    until the call has completed on `stream`.
+ *   workspace_bytes  its size.  The library picks the number of splits from
+ *                    the shape and the device's SM count, then lowers it until
+ *                    the fp32 partials (splits * rows * cols * 4 bytes) fit;
+ *                    with too little room it runs one pass.
+ * Other arguments, shapes and errors are those of the single-pass call.
+ *
+ * rlq_gemm_splitk_workspace_bytes writes to *bytes the workspace size the
+ * unconstrained plan uses on the current device for that GEMM and shape
+ * (0 when the plan is one pass).
+ */
+typedef enum { RLQ_GEMM_FPROP = 0, RLQ_GEMM_DGRAD = 1, RLQ_GEMM_WGRAD = 2 } rlq_gemm_kind;
+
+rlq_status rlq_gemm_splitk_workspace_bytes(rlq_gemm_kind kind, int64_t M, int64_t N, int64_t K,
+                                           int64_t *bytes);
+
+rlq_status rlq_gemm_fprop_splitk(const uint8_t *xq, int64_t ldxq, const float *xs, int64_t ldxs,
+                                 const uint8_t *wq, int64_t ldwq, const float *ws, int64_t ldws,
+                                 uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                                 void *workspace, int64_t workspace_bytes, rlq_stream_t stream);
+
+rlq_status rlq_gemm_dgrad_splitk(const uint8_t *dyq, int64_t lddyq, const float *dys, int64_t lddys,
+                                 const uint8_t *w, int64_t ldw, int wq_is_transposed,
+                                 const float *ws, int64_t ldws, uint16_t *dx, int64_t lddx,
+                                 int64_t M, int64_t N, int64_t K,
+                                 void *workspace, int64_t workspace_bytes, rlq_stream_t stream);
+
+rlq_status rlq_gemm_wgrad_splitk(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, int64_t lddysc,
+                                 const uint8_t *xqT, int64_t ldxqT, const float *xsc, int64_t ldxsc,
+                                 uint16_t *dw, int64_t lddw, int64_t M, int64_t N, int64_t K,
+                                 void *workspace, int64_t workspace_bytes, rlq_stream_t stream);
+
+/*
  * UAQ invariant-scaling fold, in place.  QuRL notes, 关键设计 §1: WX = (W/s)(sX)
  * with s > 1 applied per column of W and per row of the previous activation
  * (foldable into a LayerNorm / RMSNorm scale); run once before RL.
