@@ -33,6 +33,7 @@ _SIGS = {
     "rlq_gemm_fprop_splitk": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_gemm_dgrad_splitk": [_P, _I, _P, _I, _P, _I, ctypes.c_int, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_gemm_wgrad_splitk": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
+    "rlq_gemm_fprop_splitk_static": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
     "rlq_uaq_fold": [_P, _I, _I, _I, _P, _P, _I, _I, _P],
     "rlq_check": [_P],
     "rlq_diag_bounded_wait": [_I, _P],
@@ -135,6 +136,16 @@ def rlq_gemm_wgrad_splitk(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw
                           workspace_bytes, stream):
     return _call("rlq_gemm_wgrad_splitk", dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K,
                  workspace, workspace_bytes, stream)
+
+
+# Size of the library's static split-K scratch (RLQ_STATIC_SCRATCH_BYTES in rlq.h).
+STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def rlq_gemm_fprop_splitk_static(xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, stream):
+    """Split-K FProp on the library's static scratch, for callers that cannot
+    allocate device memory (see rlq.h); the plan must fit STATIC_SCRATCH_BYTES."""
+    return _call("rlq_gemm_fprop_splitk_static", xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, stream)
 
 
 def rlq_uaq_fold(w, N, K, ldw, s, prev, R, ldp, stream):

@@ -205,6 +205,40 @@ rlq_status rlq_gemm_wgrad_splitk(const uint8_t *dyqT, int64_t lddyqT, const floa
                                  void *workspace, int64_t workspace_bytes, rlq_stream_t stream);
 
 /*
+ * Split-K FProp that allocates nothing: the workspace is a static scratch
+ * array inside the library.  The pages have no counterpart to this call; it
+ * serves callers that cannot allocate device memory: a host program that keeps
+ * all device memory in its own pools and hands this library no allocator (an
+ * inference engine that reserves HBM for weights and the KV cache at start-up,
+ * or a plug-in inside one), or a real-time loop that must not call cudaMalloc
+ * because of its implicit synchronisation.  The caller still owns and passes
+ * every input and output.
+ *
+ *   Arguments, shapes, result and errors are those of rlq_gemm_fprop_splitk
+ *   with a workspace of RLQ_STATIC_SCRATCH_BYTES, with one more error: when
+ *   the split-K plan for (M, N, K) needs more scratch than that (see
+ *   rlq_gemm_splitk_workspace_bytes), the call returns RLQ_ERR_UNSUPPORTED
+ *   and launches nothing.  A plan of one pass uses no scratch.
+ *   The scratch (RLQ_STATIC_SCRATCH_BYTES, 16 MiB, in device memory) is held
+ *   on every device that loads the library until the process exits.  The
+ *   call itself calls no cudaMalloc, cudaFree or other allocating routine.
+ *   The first call on a device looks up the scratch's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   All calls on a device share the one scratch, which keeps whatever the
+ *   last call left there; each call writes every scratch element it reads, so
+ *   nothing needs clearing.  Calls whose executions overlap on the GPU (other
+ *   streams, other host threads) race on the scratch and give wrong results:
+ *   order them, for example on one stream.
+ */
+#define RLQ_STATIC_SCRATCH_BYTES 16777216
+
+rlq_status rlq_gemm_fprop_splitk_static(const uint8_t *xq, int64_t ldxq, const float *xs, int64_t ldxs,
+                                        const uint8_t *wq, int64_t ldwq, const float *ws, int64_t ldws,
+                                        uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                                        rlq_stream_t stream);
+
+/*
  * UAQ invariant-scaling fold, in place.  QuRL notes, 关键设计 §1: WX = (W/s)(sX)
  * with s > 1 applied per column of W and per row of the previous activation
  * (foldable into a LayerNorm / RMSNorm scale); run once before RL.
