@@ -634,6 +634,66 @@ def run_sweep(args):
                         f"{r['bound']} | {frac} |\n")
 
 
+# ------------------------------------------------------------- one kernel ---
+
+CASE_DOC = """Run one kernel of the path on one shape --case-reps times (after 2 warm-up
+calls), for profiler captures of a small case: gemm_fprop, gemm_dgrad,
+gemm_wgrad (optionally --split-k), quant_dual, quant_weight, uaq_fold.  Prints the
+median CUDA-event time; no JSON line."""
+
+
+def run_case(args):
+    from fp8_block_scaled_quantize_gb300 import rlq
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    rlq.lib()
+    M, N, K = args.case_m, args.case_n, args.case_k
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    x = _dev_normal(gen, (M, K), 1.0)
+    w = _dev_normal(gen, (N, K), 0.02)
+    name = args.case
+    if name == "gemm_fprop":
+        qx, sx, _, _ = rlq.quant_act_1x128(x)
+        qw, sw, _ = rlq.quant_weight_128x128(w)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: rlq.gemm_fprop(qx, sx, qw, sw, out=y, split_k=args.split_k)
+    elif name in ("gemm_dgrad", "gemm_wgrad"):
+        dy = _dev_normal(gen, (M, N), 1e-3)
+        qw, sw, qwT = rlq.quant_weight_128x128(w, transposed=True)
+        qx, sx, qxT, sxc = rlq.quant_act_1x128(x, colwise=True)
+        qdy, sdy, qdyT, sdyc = rlq.quant_act_1x128(dy, colwise=True)
+        if name == "gemm_dgrad":
+            dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+            fn = lambda: rlq.gemm_dgrad(qdy, sdy, qwT, sw, out=dx, split_k=args.split_k)
+        else:
+            dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+            fn = lambda: rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc, out=dw, split_k=args.split_k)
+    elif name == "quant_dual":
+        fn = lambda: rlq.quant_act_1x128(x, colwise=True)
+    elif name == "quant_weight":
+        fn = lambda: rlq.quant_weight_128x128(w, transposed=True)
+    elif name == "uaq_fold":
+        s = torch.full((K,), 1.5, dtype=torch.float32, device=dev)
+        fn = lambda: rlq.uaq_fold_(w, s, x)
+    else:
+        raise SystemExit(f"unknown --case {name}")
+    for _ in range(2):
+        fn()
+    ts = []
+    for _ in range(args.case_reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    rlq.check()
+    ts.sort()
+    print(f"{name} M={M} N={N} K={K} split_k={args.split_k}: median {ts[len(ts) // 2] * 1e3:.1f} us")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -647,10 +707,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help=SWEEP_DOC)
     ap.add_argument("--sweep-md", default=None, help="also write the sweep as a markdown table to this path")
+    ap.add_argument("--case", default=None, help=CASE_DOC)
+    ap.add_argument("--case-m", type=int, default=8192)
+    ap.add_argument("--case-n", type=int, default=8192)
+    ap.add_argument("--case-k", type=int, default=4096)
+    ap.add_argument("--case-reps", type=int, default=3)
+    ap.add_argument("--split-k", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.sweep:
+    if args.case:
+        run_case(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)

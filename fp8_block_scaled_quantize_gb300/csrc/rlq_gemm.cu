@@ -201,6 +201,12 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
+// 16-byte global -> shared copy (both addresses 16-byte aligned); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
 // Arrive on `bar` once this thread's earlier cp.async copies have landed.
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar)
 {
@@ -535,10 +541,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (kColScaleB) {
                     const float *sb_row = p.sb + (int64_t)kb * p.sb_bstride;
-#pragma unroll 1  // this warp runs on 40 registers
-                    for (int j = 0; j < BN / 32; ++j) {
-                        const int c = nt * BN + lane + 32 * j;
-                        cp_async4(slot + 4u * (BM + lane + 32 * j), c < p.C ? sb_row + c : sb_row, c < p.C ? 4u : 0u);
+                    // 256 column scales as 64 aligned 16-byte pieces (rows of sb are 16-byte
+                    // aligned, C % 128 == 0: a piece is wholly inside or outside the tensor)
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j) {
+                        const int c = nt * BN + 4 * (lane + 32 * j);
+                        cp_async16(slot + 4u * (BM + 4 * (lane + 32 * j)), c < p.C ? sb_row + c : sb_row,
+                                   c < p.C ? 16u : 0u);
                     }
                 } else if (lane < BN / 128) {
                     const int c = nt * BN + lane * 128;
@@ -561,8 +570,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
             const Unit wu = unit_of(p, u);
             const int mt = wu.mt, nt = wu.nt;
-            const int grow = mt * BM + row;
-            const bool row_ok = grow < p.R;
             const int col0 = nt * BN + h * 128;
             const bool half_ok = col0 < p.C;
             float2 acc[64];
