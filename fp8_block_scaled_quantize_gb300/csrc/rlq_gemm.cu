@@ -57,10 +57,7 @@ constexpr int BM = 128;                    // tile rows (TMEM lanes)
 constexpr int BN = 256;                    // tile columns (MMA N)
 constexpr int BK = 128;                    // contraction block = scale granularity = 128 bytes of E4M3
 constexpr int UMMA_K = 32;                 // K of one kind::f8f6f4 MMA
-constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BK;           // 16 KB
-constexpr int B_BYTES = BN * BK;           // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 // Warpgroup 0: warp 0 TMA, warp 1 MMA (and TMEM owner), warp 2 scales, warp 3 idle.
 // Warpgroups 1-2: eight epilogue warps.  Registers are rebalanced with
 // setmaxnreg: 128 x 40 + 256 x 232 = 384 x 168, the launch allocation.
@@ -75,15 +72,30 @@ constexpr int STG_BYTES = NUM_EPI_WARPS_C * 2 * 32 * 128;  // output staging: pe
 constexpr int SCALE_SLOTS = 8;             // scale ring depth (contraction blocks)
 constexpr int SLOT_FLOATS = BM + BN;       // 128 row scales + up to 256 column scales
 constexpr int RING_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 2 * SCALE_SLOTS;
-constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + STG_BYTES + RING_BYTES + NUM_BARS * 8 + 16;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1),
-// A and B E4M3 (format 0 in bits 7-9 / 10-12), A K-major (bit 15 = 0), B K-major
-// (bit 16 = 0) or MN-major (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t IDESC_BK = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-constexpr uint32_t IDESC_BMN = IDESC_BK | (1u << 16);
+// Per-mode shared-memory plan.  Single CTA: the CTA holds the whole 256-row B tile
+// (48 KB stages, 3 of them).  CTA pair (cta_group::2): an output tile is 256 x 256,
+// each CTA holds its 128 rows of A and half of the B tile (32 KB stages, 4 of them);
+// the pair's MMA reads both halves of B, so each byte of B is staged in one SM only.
+template <bool kPair>
+struct Cfg {
+    static constexpr int STAGES = kPair ? 4 : 3;
+    static constexpr int B_ROWS = kPair ? BN / 2 : BN;  // B rows (output columns) staged per CTA
+    static constexpr int B_BYTES = B_ROWS * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TILE_M = kPair ? 2 * BM : BM;  // output rows per tile
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 2 * SCALE_SLOTS;
+    static constexpr int SMEM_BYTES =
+        1024 /* alignment slack */ + STAGES * STAGE_BYTES + STG_BYTES + RING_BYTES + NUM_BARS * 8 + 16;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    // Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1), A and
+    // B E4M3 (format 0 in bits 7-9 / 10-12), A K-major (bit 15 = 0), B K-major (bit
+    // 16 = 0) or MN-major (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28
+    // (M = 256 for a CTA pair).
+    static constexpr uint32_t IDESC_BK = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(TILE_M >> 4) << 24);
+    static constexpr uint32_t IDESC_BMN = IDESC_BK | (1u << 16);
+};
+
 
 // Error sites (reported by rlq_check / rlq_last_error).
 enum : uint32_t {
@@ -228,6 +240,54 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
                  : "memory");
 }
 
+// Pair forms.  The load lands in this CTA's shared memory and completes its bytes
+// on `bar`, a barrier of either CTA of the pair (a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+// shared::cluster address of the variable at shared::cta address `a` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
+// Arrive on a barrier of either CTA of the cluster (default .release.cta semantics:
+// the signal orders completed work, here TMEM loads finished by tcgen05.wait::ld;
+// a .release.cluster arrive measured 2.3x slower GEMMs).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cta_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// First row, within a tile, of the rows this CTA owns.
+template <bool kPair>
+__device__ __forceinline__ int row_offset()
+{
+    if constexpr (kPair)
+        return (int)cta_rank() * BM;
+    return 0;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
@@ -241,15 +301,44 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// One tcgen05.mma: the CTA's own 128-row tile, or (kPair) the pair's 256-row tile,
+// issued by the even CTA and reading A and B from both CTAs' shared memory.
+template <bool kPair>
 __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (kPair) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
+}
+
+// Commit this thread's earlier MMAs to the barrier at shared::cta offset `bar`:
+// the own CTA's barrier, or (kPair) the barrier at that offset in both CTAs.
+template <bool kPair>
+__device__ __forceinline__ void tc_commit_t(uint32_t bar)
+{
+    if constexpr (kPair) {
+        const uint16_t mask = 0x3;
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+            ::"r"(bar), "h"(mask)
+            : "memory");
+    } else {
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    }
 }
 
 // Issues a load of 32 consecutive fp32 columns of this warp's 32 TMEM lanes
@@ -381,12 +470,21 @@ __device__ __forceinline__ Unit unit_of(const Params &p, int u)
     return w;
 }
 
-template <bool kColScaleB, bool kBMajorMN>
+template <bool kColScaleB, bool kBMajorMN, bool kPair>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_block_scaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmWs,
                         const Params p)
 {
+    using Cf = Cfg<kPair>;
+    constexpr int STAGES = Cf::STAGES;
+    constexpr int STAGE_BYTES = Cf::STAGE_BYTES;
+    constexpr int NUM_BARS = Cf::NUM_BARS;
+    // A CTA pair (cluster of 2) shares one 256-row tile: CTA `rank` owns rows
+    // rank * 128 .. rank * 128 + 127 of it; the even CTA issues the pair's MMAs.
+    // (The rank is re-read where it is used rather than kept in a register.)
+    const int unit0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int unit_step = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *staging = smem + STAGES * STAGE_BYTES;
@@ -414,7 +512,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), NUM_EPI_WARPS);
+            // a pair's buffer is free once the epilogue warps of both CTAs released it
+            mbar_init(tempty_bar(b), kPair ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
         }
         mbar_init(teardown_bar, 1);
         for (int k = 0; k < SCALE_SLOTS; ++k) {
@@ -426,10 +525,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (kPair) {
+            // collective: one warp of each CTA of the pair; both receive the same address
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
@@ -440,6 +549,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair)
+        cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -450,7 +561,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            for (int u = unit0; ok && u < p.num_units; u += unit_step) {
                 const Unit w = unit_of(p, u);
                 const int mt = w.mt, nt = w.nt;
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
@@ -460,32 +571,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
-                    tma_load_2d(a_stage(s), &tmA, full_bar(s), kb * BK, mt * BM);
-                    if (kBMajorMN) {
-                        // B stored [contraction][output]: two 128-column boxes of 128 rows
-                        tma_load_2d(b_stage(s), &tmB, full_bar(s), nt * BN, kb * BK);
-                        tma_load_2d(b_stage(s) + B_BYTES / 2, &tmB, full_bar(s), nt * BN + 128, kb * BK);
+                    if constexpr (kPair) {
+                        // both CTAs' copies complete on the even CTA's barrier, which
+                        // expects the bytes of the two stages
+                        const uint32_t fb = cluster_addr(full_bar(s), 0);
+                        if (cta_rank() == 0)
+                            mbar_arrive_expect_tx(full_bar(s), 2 * STAGE_BYTES);
+                        tma_load_2d_pair(a_stage(s), &tmA, fb, kb * BK, mt * Cf::TILE_M + row_offset<kPair>());
+                        if (kBMajorMN)  // this CTA's 128 output columns: one 128 x 128 box
+                            tma_load_2d_pair(b_stage(s), &tmB, fb, nt * BN + row_offset<kPair>(), kb * BK);
+                        else
+                            tma_load_2d_pair(b_stage(s), &tmB, fb, kb * BK, nt * BN + row_offset<kPair>());
                     } else {
-                        tma_load_2d(b_stage(s), &tmB, full_bar(s), kb * BK, nt * BN);
+                        mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+                        tma_load_2d(a_stage(s), &tmA, full_bar(s), kb * BK, mt * BM);
+                        if (kBMajorMN) {
+                            // B stored [contraction][output]: two 128-column boxes of 128 rows
+                            tma_load_2d(b_stage(s), &tmB, full_bar(s), nt * BN, kb * BK);
+                            tma_load_2d(b_stage(s) + Cf::B_BYTES / 2, &tmB, full_bar(s), nt * BN + 128, kb * BK);
+                        } else {
+                            tma_load_2d(b_stage(s), &tmB, full_bar(s), kb * BK, nt * BN);
+                        }
                     }
                 }
             }
             if (!ok) {
-                // drain: the copies issued into the last stages complete on their own
-                const int first = it > STAGES ? it - STAGES : 0;
-                for (int j = first; j < it; ++j) {
-                    volatile uint32_t never = 0;
-                    mbar_wait(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, &never, 20000000ull, SITE_DRAIN);
+                if constexpr (kPair) {
+                    // the copies complete on the even CTA's barriers: give them time to land
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 200000ull)
+                        __nanosleep(1000);
+                } else {
+                    // drain: the copies issued into the last stages complete on their own
+                    const int first = it > STAGES ? it - STAGES : 0;
+                    for (int j = first; j < it; ++j) {
+                        volatile uint32_t never = 0;
+                        mbar_wait(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, &never, 20000000ull,
+                                  SITE_DRAIN);
+                    }
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer ---
-        if (lane == 0) {
+        // (a pair's MMAs are issued by the even CTA only)
+        if (lane == 0 && (!kPair || cta_rank() == 0)) {
             int it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            for (int u = unit0; ok && u < p.num_units; u += unit_step) {
                 const Unit w = unit_of(p, u);
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = it % STAGES;
@@ -506,14 +639,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // K-major: +32 bytes along K (+2 in the address field); MN-major:
                         // +32 contraction rows of 128 bytes (+256)
                         const uint64_t bj = kBMajorMN ? bd + (uint64_t)(256 * j) : bd + 2 * j;
-                        tc_mma_f8(d, ad + 2 * j, bj, kBMajorMN ? IDESC_BMN : IDESC_BK, j > 0 ? 1u : 0u);
+                        tc_mma_f8<kPair>(d, ad + 2 * j, bj, kBMajorMN ? Cf::IDESC_BMN : Cf::IDESC_BK, j > 0 ? 1u : 0u);
                     }
-                    tc_commit(empty_bar(s));
-                    tc_commit(tfull_bar(buf));
+                    // (pair: arrives on the barrier at this offset in both CTAs)
+                    tc_commit_t<kPair>(empty_bar(s));
+                    tc_commit_t<kPair>(tfull_bar(buf));
                 }
             }
             // every MMA issued above has completed once this commit arrives
-            tc_commit(teardown_bar);
+            tc_commit_t<kPair>(teardown_bar);
             volatile uint32_t never = 0;
             mbar_wait(teardown_bar, 0, &never, 20000000ull, SITE_TEARDOWN);
         }
@@ -521,7 +655,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------ scale loader ---
         int it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        for (int u = unit0; ok && u < p.num_units; u += unit_step) {
             const Unit w = unit_of(p, u);
             const int mt = w.mt, nt = w.nt;
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
@@ -536,7 +670,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float *sa_row = p.sa + (int64_t)kb * p.ld_sa;
 #pragma unroll
                 for (int j = 0; j < BM / 32; ++j) {
-                    const int r = mt * BM + lane + 32 * j;
+                    const int r = mt * Cf::TILE_M + row_offset<kPair>() + lane + 32 * j;
                     cp_async4(slot + 4u * (lane + 32 * j), r < p.R ? sa_row + r : sa_row, r < p.R ? 4u : 0u);
                 }
                 if (kColScaleB) {
@@ -567,7 +701,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         int it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        for (int u = unit0; ok && u < p.num_units; u += unit_step) {
             const Unit wu = unit_of(p, u);
             const int mt = wu.mt, nt = wu.nt;
             const int col0 = nt * BN + h * 128;
@@ -628,7 +762,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(tempty_bar(buf));
+                    if constexpr (kPair)
+                        mbar_arrive_cluster(cluster_addr(tempty_bar(buf), 0));  // the issuing CTA's barrier
+                    else
+                        mbar_arrive(tempty_bar(buf));
                     mbar_arrive(sempty_bar(k));
                 }
             }
@@ -656,8 +793,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
                     if (lane == 0 && half_ok) {
-                        tma_store_3d(&tmWs, stg, col0 + rd * 64, mt * BM + q * 32, wu.split);
-                        tma_store_3d(&tmWs, stg + 32 * 128, col0 + rd * 64 + 32, mt * BM + q * 32, wu.split);
+                        const int y = mt * Cf::TILE_M + row_offset<kPair>() + q * 32;
+                        tma_store_3d(&tmWs, stg, col0 + rd * 64, y, wu.split);
+                        tma_store_3d(&tmWs, stg + 32 * 128, col0 + rd * 64 + 32, y, wu.split);
                         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                     }
                 }
@@ -681,8 +819,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0 && half_ok) {
                     // rows beyond R are clipped by the tensor map
-                    tma_store_2d(&tmOut, stg, col0, mt * BM + q * 32);
-                    tma_store_2d(&tmOut, stg + 32 * 128, col0 + 64, mt * BM + q * 32);
+                    const int y = mt * Cf::TILE_M + row_offset<kPair>() + q * 32;
+                    tma_store_2d(&tmOut, stg, col0, y);
+                    tma_store_2d(&tmOut, stg + 32 * 128, col0 + 64, y);
                     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                 }
             }
@@ -694,10 +833,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) {
+        if (warp == 1) {
+            if (cta_rank() == 1 && lane == 0) {
+                // the even CTA's last commit: every MMA writing this CTA's TMEM or
+                // reading its shared memory has completed
+                volatile uint32_t never = 0;
+                mbar_wait(teardown_bar, 0, &never, p.timeout_ns, SITE_TEARDOWN);
+            }
+            __syncwarp();
+        }
+        // neither CTA leaves while the other may still signal its barriers
+        cluster_sync();
+    }
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                     : "memory");
+        if constexpr (kPair)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                         : "memory");
     }
 }
 
@@ -828,7 +984,8 @@ rlq_status encode_map(CUtensorMap *map, const uint8_t *base, int64_t inner, int6
 
 struct DevInfo {
     int sms = 0;
-    bool attr_set[4] = {false, false, false, false};
+    bool attr_set[8] = {};
+    int max_clusters[8] = {};  // co-resident CTA pairs of each paired variant (0: not yet known, -1: none)
 };
 
 DevInfo &dev_info(int dev)
@@ -889,15 +1046,27 @@ int plan_splits(int64_t R, int64_t C, int64_t L, int sms, int64_t ws_cap)
     return best;
 }
 
-template <bool kCol, bool kBMN>
+// Pairs of CTAs (cta_group::2 MMAs) unless RLQ_GEMM_PAIR=0 is set in the environment.
+bool pair_mode_enabled()
+{
+    static const bool on = [] {
+        const char *e = std::getenv("RLQ_GEMM_PAIR");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+template <bool kCol, bool kBMN, bool kPair>
 rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
 {
+    using Cf = Cfg<kPair>;
     CUtensorMap tmA, tmB, tmO;
     rlq_status rs = encode_map(&tmA, a.A, a.L, a.R, a.lda, BM);
     if (rs != RLQ_OK)
         return rs;
-    // B is [C][L] (K-major) or [L][C] (MN-major, boxes of 128 columns x 128 rows)
-    rs = kBMN ? encode_map(&tmB, a.B, a.C, a.L, a.ldb, BK) : encode_map(&tmB, a.B, a.L, a.C, a.ldb, BN);
+    // B is [C][L] (K-major; boxes of the B rows one CTA stages) or [L][C] (MN-major,
+    // boxes of 128 columns x 128 rows)
+    rs = kBMN ? encode_map(&tmB, a.B, a.C, a.L, a.ldb, BK) : encode_map(&tmB, a.B, a.L, a.C, a.ldb, Cf::B_ROWS);
     if (rs != RLQ_OK)
         return rs;
     rs = encode_out_map(&tmO, a.out, a.C, a.R, a.ldo);
@@ -908,13 +1077,36 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
     if (e != cudaSuccess)
         return cuda_status(e, "cudaGetDevice");
     DevInfo &di = dev_info(dev);
-    const int variant = (kCol ? 1 : 0) + (kBMN ? 2 : 0);
+    const int variant = (kCol ? 1 : 0) + (kBMN ? 2 : 0) + (kPair ? 4 : 0);
+    auto kernel = k_gemm_block_scaled<kCol, kBMN, kPair>;
     if (!di.attr_set[variant]) {
-        e = cudaFuncSetAttribute(k_gemm_block_scaled<kCol, kBMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
         if (e != cudaSuccess)
             return cuda_status(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         di.attr_set[variant] = true;
+    }
+    cudaLaunchAttribute cluster_attr[1];
+    cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
+    cluster_attr[0].val.clusterDim.x = 2;
+    cluster_attr[0].val.clusterDim.y = 1;
+    cluster_attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
+    cfg.stream = st;
+    if constexpr (kPair) {
+        cfg.attrs = cluster_attr;
+        cfg.numAttrs = 1;
+        if (di.max_clusters[variant] == 0) {
+            cfg.gridDim = dim3(2 * (di.sms / 2), 1, 1);
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+            if (e != cudaSuccess)
+                return cuda_status(e, "cudaOccupancyMaxActiveClusters");
+            di.max_clusters[variant] = n < 1 ? -1 : n;  // -1: no pair fits, use single CTAs
+        }
+        if (di.max_clusters[variant] < 0)
+            return launch_impl<kCol, kBMN, false>(a, splits, st);
     }
     Params p;
     p.sa = a.sa;
@@ -927,7 +1119,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
     p.R = (int)a.R;
     p.C = (int)a.C;
     p.kblocks = (int)((a.L + BK - 1) / BK);
-    p.m_tiles = (int)((a.R + BM - 1) / BM);
+    p.m_tiles = (int)((a.R + Cf::TILE_M - 1) / Cf::TILE_M);
     p.n_tiles = (int)((a.C + BN - 1) / BN);
     p.num_tiles = p.m_tiles * p.n_tiles;
     // keep the smaller operand resident in L2: sweep the tiles along it
@@ -942,9 +1134,15 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
         if (rs != RLQ_OK)
             return rs;
     }
-    const int grid = p.num_units < di.sms ? p.num_units : di.sms;
-    k_gemm_block_scaled<kCol, kBMN><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, tmO, tmW, p);
-    e = cudaGetLastError();
+    if (kPair) {
+        const int pairs = p.num_units < di.max_clusters[variant] ? p.num_units : di.max_clusters[variant];
+        cfg.gridDim = dim3(2 * pairs, 1, 1);
+    } else {
+        cfg.gridDim = dim3(p.num_units < di.sms ? p.num_units : di.sms, 1, 1);
+    }
+    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmO, tmW, p);
+    if (e == cudaSuccess)
+        e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1)
         return cuda_status(e, "block-scaled GEMM launch");
     const int64_t total = a.R * (a.C / 8);
@@ -983,9 +1181,14 @@ rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st)
         if (rs != RLQ_OK)
             return rs;
     }
+    // CTA pairs for tiles of 256 output rows; one CTA per 128 rows when the output
+    // has fewer rows or the contraction is split
+    const bool pair = splits == 1 && a.R >= 2 * BM && pair_mode_enabled();
     if (a.per_col_sb)
-        return launch_impl<true, false>(a, splits, st);
-    return a.b_mn_major ? launch_impl<false, true>(a, splits, st) : launch_impl<false, false>(a, splits, st);
+        return pair ? launch_impl<true, false, true>(a, splits, st) : launch_impl<true, false, false>(a, splits, st);
+    if (a.b_mn_major)
+        return pair ? launch_impl<false, true, true>(a, splits, st) : launch_impl<false, true, false>(a, splits, st);
+    return pair ? launch_impl<false, false, true>(a, splits, st) : launch_impl<false, false, false>(a, splits, st);
 }
 
 rlq_status plan_splitk(int64_t R, int64_t C, int64_t L, int64_t ws_cap, int *splits, int64_t *ws_bytes)

@@ -229,3 +229,39 @@ def test_sweep_32b_small_and_mid_M(M):
     rows_n = _sample(27648, 64, rng)
     assert_gemm_close(dw[torch.from_numpy(rows_n).cuda()],
                       oracle.gemm_wgrad(np_(qdyT), np_(sdyc), np_(qxT), np_(sxc), rows=rows_n), f"WGrad 32B M={M}")
+
+
+_MODE_SCRIPT = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1]); sys.path.insert(0, sys.argv[1] + "/tests")
+from fp8_block_scaled_quantize_gb300 import rlq
+from gpu_util import normal_bits, to_dev
+M, N, K = 512, 768, 1024
+qx, sx, qxT, sxc = rlq.quant_act_1x128(to_dev(normal_bits(60, (M, K), 1.0, "x")), colwise=True)
+qdy, sdy, qdyT, sdyc = rlq.quant_act_1x128(to_dev(normal_bits(60, (M, N), 1e-3, "dy")), colwise=True)
+qw, sw, qwT = rlq.quant_weight_128x128(to_dev(normal_bits(60, (N, K), 0.02, "w")), transposed=True)
+outs = [rlq.gemm_fprop(qx, sx, qw, sw), rlq.gemm_dgrad(qdy, sdy, qwT, sw), rlq.gemm_dgrad(qdy, sdy, qw, sw, transposed=False),
+        rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc)]
+rlq.check()
+np.savez(sys.argv[2], *[o.view(torch.int16).cpu().numpy() for o in outs])
+"""
+
+
+def test_pair_and_single_cta_modes_agree_bitwise(tmp_path):
+    """Tiles of 256 output rows run on CTA pairs (cta_group::2); RLQ_GEMM_PAIR=0
+    forces one CTA per 128 rows.  The per-element arithmetic is the same, so the
+    two modes must give identical bits for FProp, both DGrad forms and WGrad."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = {}
+    for mode in ("0", "1"):
+        out = str(tmp_path / f"mode{mode}.npz")
+        env = dict(os.environ, RLQ_GEMM_PAIR=mode)
+        r = subprocess.run([sys.executable, "-c", _MODE_SCRIPT, root, out], env=env, capture_output=True, text=True,
+                           timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        res[mode] = np.load(out)
+    for key in res["0"].files:
+        assert np.array_equal(res["0"][key], res["1"][key]), key
