@@ -58,7 +58,8 @@ constexpr int BN = 256;                    // tile columns (MMA N)
 constexpr int BK = 128;                    // contraction block = scale granularity = 128 bytes of E4M3
 constexpr int UMMA_K = 32;                 // K of one kind::f8f6f4 MMA
 constexpr int A_BYTES = BM * BK;           // 16 KB
-// Warpgroup 0: warp 0 TMA, warp 1 MMA (and TMEM owner), warp 2 scales, warp 3 idle.
+// Warpgroup 0: warp 0 TMA, warps 1 and 3 MMA (even / odd contraction blocks; warp 1
+// owns TMEM), warp 2 scales.
 // Warpgroups 1-2: eight epilogue warps.  Registers are rebalanced with
 // setmaxnreg: 128 x 40 + 256 x 232 = 384 x 168, the launch allocation.
 constexpr int NUM_THREADS = 384;
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // a pair's buffer is free once the epilogue warps of both CTAs released it
             mbar_init(tempty_bar(b), kPair ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
         }
-        mbar_init(teardown_bar, 1);
+        mbar_init(teardown_bar, 2);  // one commit per MMA-issuing warp
         for (int k = 0; k < SCALE_SLOTS; ++k) {
             mbar_init(sfull_bar(k), 32);              // one cp.async arrival per scale-warp lane
             mbar_init(sempty_bar(k), NUM_EPI_WARPS);  // one arrival per epilogue warp
@@ -612,15 +613,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------- MMA issuer ---
-        // (a pair's MMAs are issued by the even CTA only)
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------- MMA issuers ---
+        // Warp 1 issues the even contraction blocks (TMEM buffer 0), warp 3 the odd
+        // ones (buffer 1): one thread's issue latency overlaps the other's MMAs.
+        // (A pair's MMAs are issued by the even CTA only.)
+        const int parity = warp == 1 ? 0 : 1;
         if (lane == 0 && (!kPair || cta_rank() == 0)) {
             int it = 0;
             bool ok = true;
             for (int u = unit0; ok && u < p.num_units; u += unit_step) {
                 const Unit w = unit_of(p, u);
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                    if ((it & 1) != parity)
+                        continue;
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     const int buf = it & 1;
