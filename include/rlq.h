@@ -7,7 +7,7 @@
  *     the second WGrad operand fused with the first (Jet-RL notes, section
  *     "细粒度 GEMM 量化方案", Fig. 6);
  *   - FP8 GEMMs for the three training passes FProp, DGrad and WGrad on those
- *     operands (same section; DGrad "equivalent to FProp, same configuration");
+ *     operands (same section; DGrad takes FProp's configuration);
  *   - the one-time UAQ invariant-scaling fold WX = (W/s)(sX), s applied per
  *     column of W and per row of the previous activation (QuRL notes,
  *     关键设计 §1).
