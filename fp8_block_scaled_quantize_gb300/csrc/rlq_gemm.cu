@@ -78,16 +78,20 @@ constexpr int RING_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
 // (48 KB stages, 3 of them).  CTA pair (cta_group::2): an output tile is 256 x 256,
 // each CTA holds its 128 rows of A and half of the B tile (32 KB stages, 4 of them);
 // the pair's MMA reads both halves of B, so each byte of B is staged in one SM only.
+// A single CTA (outputs of fewer than 256 rows, split-K) stores its rows straight to
+// global memory instead of through a staging tile: the 64 KB buys a fourth stage,
+// which decode-sized GEMMs, bound by the latency of streaming B from HBM, need.
 template <bool kPair>
 struct Cfg {
-    static constexpr int STAGES = kPair ? 4 : 3;
+    static constexpr int STAGES = 4;
+    static constexpr int STAGING = kPair ? STG_BYTES : 0;  // output staging (TMA stores)
     static constexpr int B_ROWS = kPair ? BN / 2 : BN;  // B rows (output columns) staged per CTA
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TILE_M = kPair ? 2 * BM : BM;  // output rows per tile
     static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 2 * SCALE_SLOTS;
     static constexpr int SMEM_BYTES =
-        1024 /* alignment slack */ + STAGES * STAGE_BYTES + STG_BYTES + RING_BYTES + NUM_BARS * 8 + 16;
+        1024 /* alignment slack */ + STAGES * STAGE_BYTES + STAGING + RING_BYTES + NUM_BARS * 8 + 16;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     // Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1), A and
     // B E4M3 (format 0 in bits 7-9 / 10-12), A K-major (bit 15 = 0), B K-major (bit
@@ -439,8 +443,9 @@ struct Params {
     int m_fastest;
     // split-K: unit u covers tile u / splits and contraction blocks
     // [(u % splits) * kbps, min(kblocks, ... + kbps)); with splits > 1 the
-    // epilogue writes fp32 partials to the workspace [splits][R][C]
+    // epilogue writes fp32 partials to the workspace ws [splits][R][C]
     int splits, kbps, num_units;
+    float *ws;
     uint64_t timeout_ns;
 };
 
@@ -489,8 +494,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *staging = smem + STAGES * STAGE_BYTES;
-    float *ring = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES + STG_BYTES);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + STG_BYTES + RING_BYTES);
+    float *ring = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES + Cf::STAGING);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + Cf::STAGING + RING_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -775,7 +780,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_arrive(sempty_bar(k));
                 }
             }
-            if (ok && p.splits > 1) {
+            if (!kPair) {
+                // single CTA: this thread's row, 128 columns, stored directly (512 or
+                // 256 contiguous bytes per thread); rows beyond R are skipped
+                const int grow = mt * BM + row;
+                if (ok && half_ok && grow < p.R) {
+                    if (p.splits > 1) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)wu.split * p.R + grow) * p.C + col0);
+#pragma unroll
+                        for (int v = 0; v < 32; ++v)
+                            dst[v] = make_float4(acc[2 * v].x, acc[2 * v].y, acc[2 * v + 1].x, acc[2 * v + 1].y);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (int64_t)grow * p.ldo + col0);
+#pragma unroll
+                        for (int v = 0; v < 16; ++v)
+                            dst[v] = make_uint4(bf16x2_rn(acc[4 * v]), bf16x2_rn(acc[4 * v + 1]),
+                                                bf16x2_rn(acc[4 * v + 2]), bf16x2_rn(acc[4 * v + 3]));
+                    }
+                }
+            } else if (ok && p.splits > 1) {
                 // fp32 partial of this contraction range into plane `split` of the
                 // workspace [splits][R][C] (reduced by k_splitk_reduce): two rounds
                 // of two 32x32 boxes (rows of 128 bytes, swizzled as below)
@@ -1134,6 +1157,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
     p.kbps = (p.kblocks + splits - 1) / splits;
     p.splits = (p.kblocks + p.kbps - 1) / p.kbps;
     p.num_units = p.num_tiles * p.splits;
+    p.ws = p.splits > 1 ? a.ws : nullptr;
     CUtensorMap tmW = tmO;  // not read with one split
     if (p.splits > 1) {
         rs = encode_ws_map(&tmW, a.ws, a.C, a.R, p.splits);
