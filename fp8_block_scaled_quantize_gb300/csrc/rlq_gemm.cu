@@ -394,6 +394,23 @@ __device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr)
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Explicit shared-memory loads: the aligned dynamic-smem base is computed through
+// an integer, so plain C++ loads through it compile to generic loads; those cost
+// WGrad's promotion 14% (its 256 column scales per block).
+__device__ __forceinline__ float lds_f32(uint32_t a)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 lds_v4(uint32_t a)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float2 f2_of(uint32_t lo, uint32_t hi)
 {
     return make_float2(__uint_as_float(lo), __uint_as_float(hi));
@@ -408,13 +425,13 @@ __device__ __forceinline__ void promote_chunk(float2 *acc, const uint32_t (&r)[3
 }
 
 // acc[0..15] += chunk * sa * sb[column]; sb is 32 consecutive column scales in
-// shared memory, read by every lane (broadcast).
+// shared memory (shared-window address), read by every lane (broadcast).
 __device__ __forceinline__ void promote_chunk_cols(float2 *acc, const uint32_t (&r)[32], float2 sa2,
-                                                   const float4 *sbs)
+                                                   uint32_t sbs)
 {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float4 sb4 = sbs[j];
+        const float4 sb4 = lds_v4(sbs + 16u * j);
         const float2 s01 = __fmul2_rn(sa2, make_float2(sb4.x, sb4.y));
         const float2 s23 = __fmul2_rn(sa2, make_float2(sb4.z, sb4.w));
         acc[2 * j] = __ffma2_rn(f2_of(r[4 * j], r[4 * j + 1]), s01, acc[2 * j]);
@@ -735,12 +752,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const float *slot = ring + k * SLOT_FLOATS;
-                const float sa = slot[row];
+                const uint32_t slot = smem_u32(ring) + (uint32_t)(k * SLOT_FLOATS * 4);
+                const float sa = lds_f32(slot + 4u * row);
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
                 uint32_t ra[32], rb[32];
                 if (!kColScaleB) {
-                    const float scl = sa * slot[BM + h];
+                    const float scl = sa * lds_f32(slot + 4u * (BM + h));
                     const float2 scl2 = make_float2(scl, scl);
                     tmem_ld32_async(taddr, ra);
                     tmem_wait32(ra);
@@ -755,7 +772,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_wait32(rb);
                     promote_chunk(&acc[48], rb, scl2);
                 } else {
-                    const float4 *sbs = reinterpret_cast<const float4 *>(slot + BM + h * 128);
+                    const uint32_t sbs = slot + 4u * (BM + h * 128);
                     const float2 sa2v = make_float2(sa, sa);
                     tmem_ld32_async(taddr, ra);
                     tmem_wait32(ra);
@@ -763,12 +780,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     promote_chunk_cols(&acc[0], ra, sa2v, sbs);
                     tmem_wait32(rb);
                     tmem_ld32_async(taddr + 64, ra);
-                    promote_chunk_cols(&acc[16], rb, sa2v, sbs + 8);
+                    promote_chunk_cols(&acc[16], rb, sa2v, sbs + 128);
                     tmem_wait32(ra);
                     tmem_ld32_async(taddr + 96, rb);
-                    promote_chunk_cols(&acc[32], ra, sa2v, sbs + 16);
+                    promote_chunk_cols(&acc[32], ra, sa2v, sbs + 256);
                     tmem_wait32(rb);
-                    promote_chunk_cols(&acc[48], rb, sa2v, sbs + 24);
+                    promote_chunk_cols(&acc[48], rb, sa2v, sbs + 384);
                 }
                 tc_fence_before();
                 __syncwarp();
