@@ -357,40 +357,65 @@ def _load_traffic(kernel: str):
 
 
 def run_e2e(st: Step, host, args, dist, world, flop_step):
-    """The same step through host buffers: H2D of X, W, dY from pinned memory,
-    the step, D2H of Y, dX, dW into pinned memory, all inside the timed region."""
+    """The same step through host buffers, every step's H2D of X, W, dY from pinned
+    memory and D2H of Y, dX, dW into pinned memory inside the timed region.
+
+    Steps are pipelined the way a training loop would run them: three streams
+    (copy in, compute, copy out) and two device buffer sets, so step i+1's inputs
+    arrive and step i-1's results leave while step i computes.  Events order each
+    set's reuse: a set's inputs are rewritten only after its previous compute, its
+    outputs only after their previous copy out."""
+    dev = st.dev
+    sets = [st, Step(dev, host)]
     pin = {k: v.pin_memory() for k, v in host.items()}
-    outs = {"y": torch.empty(st.y.shape, dtype=torch.bfloat16).pin_memory(),
-            "dx": torch.empty(st.dx.shape, dtype=torch.bfloat16).pin_memory(),
-            "dw": torch.empty(st.dw.shape, dtype=torch.bfloat16).pin_memory()}
-    stream = torch.cuda.current_stream()
-    sh = stream.cuda_stream
+    outs = [{"y": torch.empty(st.y.shape, dtype=torch.bfloat16).pin_memory(),
+             "dx": torch.empty(st.dx.shape, dtype=torch.bfloat16).pin_memory(),
+             "dw": torch.empty(st.dw.shape, dtype=torch.bfloat16).pin_memory()} for _ in range(2)]
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
+    started = [False, False]
 
-    def one():
-        st.x.copy_(pin["x"], non_blocking=True)
-        st.w.copy_(pin["w"], non_blocking=True)
-        st.dy.copy_(pin["dy"], non_blocking=True)
-        st.run(sh)
-        outs["y"].copy_(st.y, non_blocking=True)
-        outs["dx"].copy_(st.dx, non_blocking=True)
-        outs["dw"].copy_(st.dw, non_blocking=True)
+    def one(i):
+        b = i % 2
+        S, o = sets[b], outs[b]
+        if started[b]:
+            s_in.wait_event(ev["comp"][b])    # the set's previous compute has read its inputs
+            s_comp.wait_event(ev["out"][b])   # ... and its previous results have left
+        with torch.cuda.stream(s_in):
+            S.x.copy_(pin["x"], non_blocking=True)
+            S.w.copy_(pin["w"], non_blocking=True)
+            S.dy.copy_(pin["dy"], non_blocking=True)
+            ev["in"][b].record(s_in)
+        s_comp.wait_event(ev["in"][b])
+        S.run(s_comp.cuda_stream)
+        ev["comp"][b].record(s_comp)
+        s_out.wait_event(ev["comp"][b])
+        with torch.cuda.stream(s_out):
+            o["y"].copy_(S.y, non_blocking=True)
+            o["dx"].copy_(S.dx, non_blocking=True)
+            o["dw"].copy_(S.dw, non_blocking=True)
+            ev["out"][b].record(s_out)
+        started[b] = True
 
-    for _ in range(max(1, args.warmup // 2)):
-        one()
+    for i in range(max(2, args.warmup // 2)):
+        one(i)
     torch.cuda.synchronize()
     n = max(2, args.steps // 2)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(dist)
-    e0.record()
-    for _ in range(n):
-        one()
-    e1.record()
+    e0.record(s_in)
+    for i in range(n):
+        one(i)
+    s_in.wait_stream(s_out)
+    e1.record(s_in)
     torch.cuda.synchronize()
     ms = _max_over_ranks(dist, e0.elapsed_time(e1) / n)
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
-    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs[0].values())
+    del sets[1]
     return {"value": round(world * flop_step / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "pipelining": "copy in / compute / copy out on three streams, two device buffer sets"}
 
 
 # ------------------------------------------------------------------ CPU ---
