@@ -17,13 +17,13 @@ Contents
 Sources (the web pages on quantized RL rollout):
 * Jet-RL notes, section "细粒度 GEMM 量化方案" (Fig. 6): 128x128 per-block
   weight quantization; 1x128 per-group activation / gradient quantization;
-  FProp takes 1x128 activations and 128x128 weights; DGrad "is equivalent to
-  FProp"; WGrad takes a 1x128 first operand and a 128x1 second operand.
+  FProp takes 1x128 activations and 128x128 weights; DGrad takes FProp's
+  configuration; WGrad takes a 1x128 first operand and a 128x1 second operand.
 * QuRL notes, section 关键设计 §1 (UAQ): WX = (W/s)(sX), s applied per column
   of W and per row of the previous activation.
 * The FP8 sub-format (E4M3, max 448), the scale rule (amax/448, 1.0 for an
-  all-zero group), RN-satfinite rounding and fp32 IEEE division are readings
-  the pages leave open; they are listed in the design doc.
+  all-zero group), RN-satfinite rounding and fp32 IEEE division are the
+  plainest readings of what the pages leave open.
 
 Pins: ``tests/test_oracle_*.py`` check every function here against the OCP
 E4M3 definition, an independent library (torch / ml_dtypes float8), exact

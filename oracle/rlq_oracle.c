@@ -12,7 +12,8 @@
  *    and round-to-nearest-even, saturating encode.  The pages name FP8 for the
  *    GEMMs (Jet-RL notes, "细粒度 GEMM 量化方案") and E4M3 only as the NVFP4
  *    block-scale format (QeRL news article, key takeaways); the sub-format,
- *    the rounding and the saturation are the readings recorded in the design doc.
+ *    the rounding and the saturation are the plainest readings of what the
+ *    pages leave open.
  *  - Fine-grained quantization (Jet-RL notes, "细粒度 GEMM 量化方案", Fig. 6):
  *      * 1x128 groups along K for activations / gradients,
  *      * 128x1 groups along the token dimension for the second WGrad operand,

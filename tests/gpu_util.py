@@ -6,7 +6,7 @@ from fp8_block_scaled_quantize_gb300 import inputs as I
 
 DEV = "cuda"
 
-# GEMM tolerance (the benchmark spec): relative Frobenius error and per-element bound,
+# GEMM tolerance: relative Frobenius error and per-element bound,
 # measured on the bf16 output against the fp64 oracle.
 REL_FRO = 2e-3
 ELEM_ABS = 1e-2

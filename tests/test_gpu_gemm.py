@@ -1,7 +1,7 @@
 """GPU parity of the block-scaled FP8 GEMMs (FProp, DGrad, WGrad through the
 C ABI) against the oracle's fp64 GEMMs over the same codes and scales.
 
-* Tolerance (the benchmark spec): relative Frobenius error <= 2e-3 and per element
+* Tolerance: relative Frobenius error <= 2e-3 and per element
   |err| <= 1e-2 * (|ref| + 1), on the bf16 output.
 * Integer pins: integer-valued codes with scales 1 (or one power of two) give
   exact fp32 accumulations; the bf16 outputs must then match the oracle's
