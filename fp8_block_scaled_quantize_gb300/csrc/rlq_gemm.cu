@@ -238,6 +238,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"((uint64_t)map), "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // Pair forms.  The load lands in this CTA's shared memory and completes its bytes
 // on `bar`, a barrier of either CTA of the pair (a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y)
@@ -294,6 +301,10 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+__device__ __forceinline__ void tc_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
 
 // One tcgen05.mma: the CTA's own 128-row tile, or (kPair) the pair's 256-row tile,
 // issued by the even CTA and reading A and B from both CTAs' shared memory.
@@ -485,7 +496,8 @@ __device__ __forceinline__ Unit unit_of(const Params &p, int u)
 template <bool kColScaleB, bool kBMajorMN, bool kPair>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_block_scaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmOut, const Params p)
+                        const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmWs,
+                        const Params p)
 {
     using Cf = Cfg<kPair>;
     constexpr int STAGES = Cf::STAGES;
@@ -554,8 +566,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
-        if (kPair)
-            prefetch_tmap(&tmOut);
+        prefetch_tmap(&tmOut);
+        if (p.splits > 1)
+            prefetch_tmap(&tmWs);
     }
     tc_fence_before();
     __syncthreads();
@@ -802,6 +815,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                 bf16x2_rn(acc[4 * v + 2]), bf16x2_rn(acc[4 * v + 3]));
                     }
                 }
+            } else if (ok && p.splits > 1) {
+                // fp32 partial of this contraction range into plane `split` of the
+                // workspace [splits][R][C] (reduced by k_splitk_reduce): two rounds
+                // of two 32x32 boxes (rows of 128 bytes, swizzled as below)
+                const uint32_t stg = smem_u32(staging) + (uint32_t)((warp - FIRST_EPI_WARP) * 2 * 32 * 128);
+#pragma unroll
+                for (int rd = 0; rd < 2; ++rd) {
+                    if (lane == 0)
+                        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    __syncwarp();
+#pragma unroll
+                    for (int v = 0; v < 16; ++v) {
+                        const uint32_t addr = stg + (uint32_t)((v >> 3) * 32 * 128 + lane * 128 +
+                                                               ((((v & 7) ^ (lane & 7))) << 4));
+                        const int j = rd * 32 + 2 * v;  // columns 2j .. 2j+3 of this half
+                        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(acc[j].x), "f"(acc[j].y)
+                                     : "memory");
+                        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr + 8), "f"(acc[j + 1].x),
+                                     "f"(acc[j + 1].y)
+                                     : "memory");
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0 && half_ok) {
+                        const int y = mt * Cf::TILE_M + row_offset<kPair>() + q * 32;
+                        tma_store_3d(&tmWs, stg, col0 + rd * 64, y, wu.split);
+                        tma_store_3d(&tmWs, stg + 32 * 128, col0 + rd * 64 + 32, y, wu.split);
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    }
+                }
             } else if (ok) {
                 // this warp's 32 rows x 128 columns: two 32x64 boxes, rows of
                 // 128 bytes with the 16-byte chunks XOR-swizzled by (row % 8)
@@ -945,6 +988,24 @@ rlq_status encode_out_map(CUtensorMap *map, uint16_t *base, int64_t cols, int64_
     if (r != CUDA_SUCCESS)
         return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for the [%lld x %lld] output",
                     (int)r, (long long)rows, (long long)cols);
+    return RLQ_OK;
+}
+
+// fp32 split-K workspace [splits][rows][cols], dense; box 32 columns x 32 rows x 1, 128-byte swizzle.
+rlq_status encode_ws_map(CUtensorMap *map, float *base, int64_t cols, int64_t rows, int splits)
+{
+    auto enc = get_encode_fn();
+    if (!enc)
+        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)splits};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)(cols * rows * 4)};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for the split-K workspace", (int)r);
     return RLQ_OK;
 }
 
@@ -1114,13 +1175,19 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
     p.splits = (p.kblocks + p.kbps - 1) / p.kbps;
     p.num_units = p.num_tiles * p.splits;
     p.ws = p.splits > 1 ? a.ws : nullptr;
+    CUtensorMap tmW = tmO;  // not read with one split
+    if (p.splits > 1) {
+        rs = encode_ws_map(&tmW, a.ws, a.C, a.R, p.splits);
+        if (rs != RLQ_OK)
+            return rs;
+    }
     if (kPair) {
         const int pairs = p.num_units < di.max_clusters[variant] ? p.num_units : di.max_clusters[variant];
         cfg.gridDim = dim3(2 * pairs, 1, 1);
     } else {
         cfg.gridDim = dim3(p.num_units < di.sms ? p.num_units : di.sms, 1, 1);
     }
-    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmO, p);
+    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmO, tmW, p);
     if (e == cudaSuccess)
         e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1)
