@@ -101,3 +101,27 @@ def test_gemm_validation():
 def test_diag_validation():
     assert _status(rlq.rlq_diag_bounded_wait, 0, None) == 1
     assert _status(rlq.rlq_diag_bounded_wait, 10 ** 8, None) == 1
+
+
+def test_splitk_and_static_validation():
+    """Host-side checks of the split-K, workspace-query and static-scratch entry
+    points, all made before any CUDA call."""
+    fp = rlq.rlq_gemm_fprop_splitk
+    args = (FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 1, FAKE, 128, 4, 128, 128)
+    assert _status(fp, *args, FAKE + 4, 1 << 20, None) == 3    # workspace not 16-byte aligned
+    assert _status(fp, *args, FAKE, -1, None) == 1             # negative workspace size
+    assert _status(fp, FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 1, FAKE, 136, 4, 130, 128, FAKE, 0, None) == 2
+    dg = rlq.rlq_gemm_dgrad_splitk
+    assert _status(dg, FAKE, 128, FAKE, 4, FAKE, 128, 1, FAKE, 1, FAKE, 128, 4, 128, 128, FAKE + 8, 64, None) == 3
+    wg = rlq.rlq_gemm_wgrad_splitk
+    assert _status(wg, FAKE, 16, FAKE, 128, FAKE, 16, FAKE, 128, FAKE, 128, 4, 128, 128, FAKE, -8, None) == 1
+    q = rlq.rlq_gemm_splitk_workspace_bytes
+    assert _status(q, 7, 64, 256, 4096) == 1                   # unknown GEMM kind
+    assert _status(q, rlq.GEMM_FPROP, -1, 256, 4096) == 1     # negative size
+    assert _status(q, rlq.GEMM_FPROP, 64, 1 << 31, 4096) == 2  # dimension beyond 2^31
+    st = rlq.rlq_gemm_fprop_splitk_static
+    assert _status(st, FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 1, FAKE, 128, -4, 128, 128, None) == 1
+    assert _status(st, FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 1, FAKE, 128, 4, 1 << 31, 128, None) == 2
+    assert rlq.STATIC_SCRATCH_BYTES == 16 << 20
+    header = open(HEADER).read()
+    assert "#define RLQ_STATIC_SCRATCH_BYTES 16777216" in header
