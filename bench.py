@@ -663,7 +663,7 @@ def run_sweep(args):
 
 CASE_DOC = """Run one kernel of the path on one shape --case-reps times (after 2 warm-up
 calls), for profiler captures of a small case: gemm_fprop, gemm_dgrad,
-gemm_wgrad (optionally --split-k), quant_dual, quant_weight, uaq_fold.  Prints the
+gemm_wgrad (optionally --split-k), quant_rows, quant_dual, quant_weight, uaq_fold.  Prints the
 median CUDA-event time; no JSON line."""
 
 
@@ -695,6 +695,8 @@ def run_case(args):
         else:
             dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
             fn = lambda: rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc, out=dw, split_k=args.split_k)
+    elif name == "quant_rows":
+        fn = lambda: rlq.quant_act_1x128(x)
     elif name == "quant_dual":
         fn = lambda: rlq.quant_act_1x128(x, colwise=True)
     elif name == "quant_weight":

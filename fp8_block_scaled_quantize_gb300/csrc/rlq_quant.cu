@@ -188,25 +188,41 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t *__restrict__
     const int64_t g0 = 2 * warp + half;
     int64_t m = g0 / KB;
     int kb = (int)(g0 % KB);
-    for (int64_t base = 2 * warp; base < G; base += 2 * step) {
-        int64_t m1 = m + dm;
-        int kb1 = kb + dkb;
+    // the next iteration's two groups are loaded before this iteration's are quantized
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    auto second = [&](int64_t mm, int kk, int64_t &m1, int &kb1) {
+        m1 = mm + dm;
+        kb1 = kk + dkb;
         if (kb1 >= KB) {
             kb1 -= KB;
             ++m1;
         }
-        const bool v0 = m < M, v1 = m1 < M;
-        const uint4 zero = make_uint4(0, 0, 0, 0);
-        const uint4 a = v0 ? ld_stream(x + m * ldx + (int64_t)kb * GRP + l16 * 8) : zero;
-        const uint4 b = v1 ? ld_stream(x + m1 * ldx + (int64_t)kb1 * GRP + l16 * 8) : zero;
-        row_group(a, v0, m, kb, l16, q, ldq, s, lds);
-        row_group(b, v1, m1, kb1, l16, q, ldq, s, lds);
-        m = m1 + dm;
-        kb = kb1 + dkb;
-        if (kb >= KB) {
-            kb -= KB;
-            ++m;
+    };
+    int64_t m1;
+    int kb1;
+    second(m, kb, m1, kb1);
+    uint4 a = m < M ? ld_stream(x + m * ldx + (int64_t)kb * GRP + l16 * 8) : zero;
+    uint4 b = m1 < M ? ld_stream(x + m1 * ldx + (int64_t)kb1 * GRP + l16 * 8) : zero;
+    for (int64_t base = 2 * warp; base < G; base += 2 * step) {
+        int64_t mn = m1 + dm;
+        int kbn = kb1 + dkb;
+        if (kbn >= KB) {
+            kbn -= KB;
+            ++mn;
         }
+        int64_t mn1;
+        int kbn1;
+        second(mn, kbn, mn1, kbn1);
+        const uint4 an = mn < M ? ld_stream(x + mn * ldx + (int64_t)kbn * GRP + l16 * 8) : zero;
+        const uint4 bn = mn1 < M ? ld_stream(x + mn1 * ldx + (int64_t)kbn1 * GRP + l16 * 8) : zero;
+        row_group(a, m < M, m, kb, l16, q, ldq, s, lds);
+        row_group(b, m1 < M, m1, kb1, l16, q, ldq, s, lds);
+        a = an;
+        b = bn;
+        m = mn;
+        kb = kbn;
+        m1 = mn1;
+        kb1 = kbn1;
     }
 }
 
