@@ -76,6 +76,8 @@ def _dist_setup(n_gpus: int):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)  # before the group: NCCL binds each rank to its current device
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
         return dist, rank, world, local
     return None, 0, 1, local
