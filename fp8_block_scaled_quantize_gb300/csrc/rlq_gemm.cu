@@ -12,16 +12,14 @@
 // per-128 scales, so the scaling ("promotion") is done in software:
 //
 //   * a TMA warp streams 128x128 A tiles and 256x128 B tiles (128-byte swizzle)
-//     into a 3-stage shared-memory ring guarded by mbarriers;
-//   * an MMA warp issues, per contraction block, four tcgen05.mma
-//     (kind::f8f6f4, M=128, N=256, K=32) into one of two TMEM partial buffers
-//     (2 x 256 fp32 columns = the whole 512-column TMEM), then commits;
+//     into a 4-stage shared-memory ring guarded by mbarriers;
+//   * two MMA warps issue, per contraction block (even blocks one warp, odd
+//     blocks the other), four tcgen05.mma (kind::f8f6f4, M=128, N=256, K=32)
+//     into one of two TMEM partial buffers (2 x 256 fp32 columns = the whole
+//     512-column TMEM), then commit;
 //   * eight epilogue warps read the finished partial with tcgen05.ld, multiply
 //     by sa * sb and accumulate into fp32 registers (packed f32x2 FMA), release
-//     the TMEM buffer, and after the last block round to bf16, stage the tile
-//     in shared memory (128-byte swizzle) and hand it to asynchronous TMA
-//     stores, so the next tile's promotion starts at once.
-//
+//     the TMEM buffer, and after the tile's last block round to bf16 and store;
 //   * a scale warp streams each block's scales (128 row scales, and the block
 //     or per-column scales of the tile's columns) into an 8-slot shared-memory
 //     ring with cp.async, up to 8 blocks ahead of the epilogue, so that their
@@ -31,11 +29,16 @@
 //     buffer that the async proxy rewrites are not ordered by mbarriers alone
 //     (a TMA-staged variant measured non-deterministic).
 //
-// Tiles are 128 x 256; the kernel is persistent (one CTA per SM) and walks
-// the tile list with the smaller operand resident in L2.  Every mbarrier wait
-// is bounded: on timeout the waiting thread records an error word that
-// rlq_check() reports, raises a CTA-wide abort flag, and the CTA drains its
-// in-flight copies and MMAs, frees TMEM and exits.  Nothing traps.
+// Tiles are 128 x 256 per CTA.  Outputs of at least 256 rows run on CTA pairs
+// (clusters of two, tcgen05.mma.cta_group::2, M = 256): each CTA stages its 128
+// rows of A and half of B, the even CTA issues the pair's MMAs and commits to
+// both CTAs' barriers, and the epilogue stages the bf16 tile in shared memory
+// for TMA stores.  A single CTA (fewer rows, or a split contraction) stores its
+// rows directly.  The kernel is persistent (one CTA per SM, one pair per two)
+// and walks (tile, contraction split) units with the smaller operand resident in
+// L2.  Every mbarrier wait is bounded: on timeout the waiting thread records an
+// error word that rlq_check() reports, raises a CTA-wide abort flag, and the CTA
+// drains its in-flight copies and MMAs, frees TMEM and exits.  Nothing traps.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
