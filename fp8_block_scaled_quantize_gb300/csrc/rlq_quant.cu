@@ -8,9 +8,10 @@
 // Per group: amax = max |x|; s = fl32(amax / 448), or 1 when amax == 0;
 // code = RN-even satfinite E4M3 of fl32(x / s).
 //
-// All kernels are HBM-bound streaming kernels: 16-byte loads of 8 bf16 per
-// lane, a group of 128 spread over 16 lanes (warp-shuffle amax), packed code
-// stores.  The per-element quotient x / s uses the group's reciprocal
+// All kernels are HBM-bound streaming kernels with vector loads and packed
+// code stores; a group's scale is computed once (not by every lane that holds
+// part of the group) and handed to the encoding lanes by shuffle or through
+// shared memory.  The per-element quotient x / s uses the group's reciprocal
 // r = RN(1/s) plus one FMA residual correction (1.5 packed fp32x2 ops per
 // element) instead of an IEEE division sequence.  For bf16 x with |x| <= amax and
 // s = fl32(amax/448) this equals IEEE fp32 division wherever the E4M3 code can
@@ -227,76 +228,165 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t *__restrict__
 }
 
 // ---------------------------------------------------------------------------
-// Fused 1x128 + 128x1 on a 128x128 tile: one read of x.  Row groups are
-// quantized straight from registers; the tile is staged in shared memory
-// (row pitch 272 B) for the column groups, whose codes are written transposed.
+// Fused 1x128 + 128x1 on a 128x128 tile: one read of x.
+//
+// Row pass (registers): half-warp hw16 holds rows hw16 + 16 i (i = 0..7), lane
+// l16 columns 8 l16 .. 8 l16 + 7.  Both maxima come from the packed bf16 words
+// (|x| by clearing the sign bits, then max.bf16x2; the maximum of bf16 values is
+// one of them, so it is exact): one word per row (two candidates) and one per
+// column pair over the lane's eight rows.  The eight row maxima of a half-warp
+// are reduced in one transposed exchange (each step hands half of the remaining
+// groups to the partner lane), after which lane pair (2g, 2g+1) holds group g's
+// amax and computes its scale once; the encoding lanes fetch (r, s) by shuffle.
+// The raw tile is staged in shared memory (row pitch 272 B): the row encode reads
+// its rows back from there (the registers are not held across the reductions),
+// and so does the column pass.
+//
+// Column pass: 128 threads reduce the eight per-warp column maxima and compute
+// the 128 column scales once; then every thread encodes two adjacent columns
+// over 32 rows from the staged tile and writes their codes transposed.
+//
+// Tiles are ordered with the row block fastest: CTAs that run together write
+// whole rows of the transposed codes (contiguous 128-byte pieces of one row)
+// rather than one piece of many rows.
 constexpr int TP = GRP + 8;  // staging row pitch in bf16 elements
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t babs2(uint32_t a) { return a & 0x7FFF7FFFu; }
+
+// amax of a packed pair of candidates; an all-NaN group reads as 0, as a
+// running fmaxf from 0 would give.
+__device__ __forceinline__ float bmax_final(uint32_t p) { return fmaxf(fmaxf(bf_lo(p), bf_hi(p)), 0.0f); }
+
+// Row codes of the eight rows a lane holds, read back from the staged tile (each
+// lane reads the words it wrote itself); (r, s[, f]) of row group i come from
+// lane (half * 16 + 2 i), which computed it.
+template <bool kPrescale>
+__device__ __forceinline__ void dual_row_codes(const uint16_t *tile, const Quot &own, int lane, int hw16, int l16,
+                                               int rows, uint8_t *__restrict__ qrow, int64_t ldq)
+{
+    const int src0 = lane & 16;
+#pragma unroll 4  // full unrolling hoists every load and shuffle and spills at 64 registers
+    for (int i = 0; i < 8; ++i) {
+        Quot c;
+        c.r = __shfl_sync(0xFFFFFFFFu, own.r, src0 + 2 * i);
+        c.sd = __shfl_sync(0xFFFFFFFFu, own.sd, src0 + 2 * i);
+        c.f = kPrescale ? __shfl_sync(0xFFFFFFFFu, own.f, src0 + 2 * i) : 1.0f;
+        const int r = hw16 + 16 * i;
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(&tile[r * TP + l16 * 8]), f);
+        const uint2 codes = encode8_t<kPrescale>(f, c);
+        if (r < rows)
+            *reinterpret_cast<uint2 *>(qrow + (int64_t)r * ldq + l16 * 8) = codes;
+    }
+}
 
 __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restrict__ x, int64_t M, int64_t ldx,
                                                     uint8_t *__restrict__ q, int64_t ldq,
                                                     float *__restrict__ s, int64_t lds,
                                                     uint8_t *__restrict__ qT, int64_t ldqT,
-                                                    float *__restrict__ sc, int64_t ldsc, int64_t MB)
+                                                    float *__restrict__ sc, int64_t ldsc, int64_t MB, int64_t KB)
 {
     __shared__ __align__(16) uint16_t tile[GRP * TP];
-    __shared__ float cam[4][GRP];  // column maxima of the four row quarters
+    __shared__ __align__(16) uint32_t ccm[8][GRP / 2];  // per-warp column-pair maxima
+    __shared__ __align__(8) float col_r[GRP], col_nsd[GRP], col_f[GRP];
     const int t = threadIdx.x, lane = t & 31, half = lane >> 4, l16 = lane & 15, warp = t >> 5;
     const int hw16 = warp * 2 + half;  // 0..15
-    const int64_t kb = blockIdx.x;
     const int c2 = t & 63, rq = t >> 6;
 
-    for (int64_t mb = blockIdx.y; mb < MB; mb += gridDim.y) {
+    for (int64_t kb = blockIdx.y; kb < KB; kb += gridDim.y)
+    for (int64_t mb = blockIdx.x; mb < MB; mb += gridDim.x) {
         const int64_t m0 = mb * GRP;
         const int rows = (int)((M - m0) < GRP ? (M - m0) : GRP);
 
-        // ---- row pass: half-warp hw16 owns rows hw16 + 16 i; lane l16 owns
-        // columns 8 l16 .. 8 l16 + 7.  Rows beyond M read as zero.
+        // ---- row pass.  Rows beyond M read as zero (they raise no maximum).
         uint4 v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = hw16 + 16 * i;
             v[i] = (r < rows) ? ld_stream(x + (m0 + r) * ldx + kb * GRP + l16 * 8) : make_uint4(0, 0, 0, 0);
         }
+        uint32_t pm[8], cm[4];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int r = hw16 + 16 * i;
-            float f[8];
-            unpack8(v[i], f);
-            const float amax = halfwarp_max(amax8(f));
-            const float scl = group_scale(amax);
-            const Quot c = make_quot(scl);
-            const uint2 codes = encode8(f, c);
-            if (r < rows) {
-                *reinterpret_cast<uint2 *>(q + (m0 + r) * ldq + kb * GRP + l16 * 8) = codes;
-                if (l16 == 0)
-                    s[kb * lds + m0 + r] = scl;
+            const uint32_t a0 = babs2(v[i].x), a1 = babs2(v[i].y), a2 = babs2(v[i].z), a3 = babs2(v[i].w);
+            pm[i] = bmax2(bmax2(a0, a1), bmax2(a2, a3));
+            if (i == 0) {
+                cm[0] = a0, cm[1] = a1, cm[2] = a2, cm[3] = a3;
+            } else {
+                cm[0] = bmax2(cm[0], a0), cm[1] = bmax2(cm[1], a1);
+                cm[2] = bmax2(cm[2], a2), cm[3] = bmax2(cm[3], a3);
             }
-            *reinterpret_cast<uint4 *>(&tile[r * TP + l16 * 8]) = v[i];
+            *reinterpret_cast<uint4 *>(&tile[(hw16 + 16 * i) * TP + l16 * 8]) = v[i];
+        }
+        // column maxima: the two half-warps hold the same columns
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            cm[j] = bmax2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 16));
+        if (half == 0)
+            *reinterpret_cast<uint4 *>(&ccm[warp][4 * l16]) = make_uint4(cm[0], cm[1], cm[2], cm[3]);
+        // row maxima: transposed exchange over the half-warp (lane bits 3, 2, 1
+        // pick the group kept at each step; bit 0 pairs lanes with equal results)
+        const bool b3 = l16 & 8, b2 = l16 & 4, b1 = l16 & 2;
+        uint32_t p1[4], p2[2];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t keep = b3 ? pm[k + 4] : pm[k], send = b3 ? pm[k] : pm[k + 4];
+            p1[k] = bmax2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 8));
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t keep = b2 ? p1[k + 2] : p1[k], send = b2 ? p1[k] : p1[k + 2];
+            p2[k] = bmax2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 4));
+        }
+        uint32_t p3;
+        {
+            const uint32_t keep = b1 ? p2[1] : p2[0], send = b1 ? p2[0] : p2[1];
+            p3 = bmax2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2));
+        }
+        p3 = bmax2(p3, __shfl_xor_sync(0xFFFFFFFFu, p3, 1));
+        const int gr = hw16 + 16 * (l16 >> 1);  // the row whose scale this lane computes
+        const float own_s = group_scale(bmax_final(p3));
+        const Quot own = make_quot(own_s);
+        if ((l16 & 1) == 0 && gr < rows)
+            s[kb * lds + m0 + gr] = own_s;
+        uint8_t *qrow = q + m0 * ldq + kb * GRP;
+        if (__any_sync(0xFFFFFFFFu, own.f != 1.0f))
+            dual_row_codes<true>(tile, own, lane, hw16, l16, rows, qrow, ldq);
+        else
+            dual_row_codes<false>(tile, own, lane, hw16, l16, rows, qrow, ldq);
+        __syncthreads();
+
+        // ---- column scales, once per column
+        if (t < GRP) {
+            uint32_t m = ccm[0][t >> 1];
+#pragma unroll
+            for (int w = 1; w < 8; ++w)
+                m = bmax2(m, ccm[w][t >> 1]);
+            const float am = fmaxf((t & 1) ? bf_hi(m) : bf_lo(m), 0.0f);
+            const float cs = group_scale(am);
+            const Quot c = make_quot(cs);
+            col_r[t] = c.r;
+            col_nsd[t] = -c.sd;
+            col_f[t] = c.f;
+            sc[mb * ldsc + kb * GRP + t] = cs;
         }
         __syncthreads();
 
-        // ---- column pass: thread owns columns 2*c2, 2*c2+1 over rows rq*32 .. +31;
-        // first the column maxima (four row quarters combined through smem)
+        // ---- column pass: thread owns columns 2*c2, 2*c2+1 over rows rq*32 .. +31
         const uint32_t *col = reinterpret_cast<const uint32_t *>(tile) + c2;
-        float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll 8
-        for (int rr = 0; rr < 32; ++rr) {
-            const uint32_t wv = col[(rq * 32 + rr) * (TP / 2)];
-            a0 = fmaxf(a0, fabsf(bf_lo(wv)));
-            a1 = fmaxf(a1, fabsf(bf_hi(wv)));
-        }
-        cam[rq][2 * c2] = a0;
-        cam[rq][2 * c2 + 1] = a1;
-        __syncthreads();
-        a0 = fmaxf(fmaxf(cam[0][2 * c2], cam[1][2 * c2]), fmaxf(cam[2][2 * c2], cam[3][2 * c2]));
-        a1 = fmaxf(fmaxf(cam[0][2 * c2 + 1], cam[1][2 * c2 + 1]), fmaxf(cam[2][2 * c2 + 1], cam[3][2 * c2 + 1]));
-        const float s0 = group_scale(a0), s1 = group_scale(a1);
-        const Quot c0 = make_quot(s0), c1 = make_quot(s1);
         // one packed lane per column: (even column, odd column) of the same row
-        const float2 pf = make_float2(c0.f, c1.f), pr = make_float2(c0.r, c1.r), pn = make_float2(-c0.sd, -c1.sd);
-        const bool fast = (c0.f == 1.0f) && (c1.f == 1.0f);
+        const float2 pf = *reinterpret_cast<const float2 *>(&col_f[2 * c2]);
+        const float2 pr = *reinterpret_cast<const float2 *>(&col_r[2 * c2]);
+        const float2 pn = *reinterpret_cast<const float2 *>(&col_nsd[2 * c2]);
         uint32_t e[8], o[8];  // 32 codes of each column, 4 per word
-        if (fast)
+        if (pf.x == 1.0f && pf.y == 1.0f)
             encode_cols<false>(col, rq, TP / 2, pf, pr, pn, e, o);
         else
             encode_cols<true>(col, rq, TP / 2, pf, pr, pn, e, o);
@@ -318,94 +408,118 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
                 }
             }
         }
-        if (rq == 0) {
-            sc[mb * ldsc + k] = s0;
-            sc[mb * ldsc + k + 1] = s1;
-        }
-        __syncthreads();  // tile and cam are reused by the next mb
+        __syncthreads();  // tile, ccm and the column scales are reused by the next mb
     }
 }
 
 // ---------------------------------------------------------------------------
-// 128x128 weight blocks: one CTA per block.  The block is read once (16-byte
-// loads), its amax reduced while the raw values are stashed in shared memory,
-// then quantized from shared memory; the same buffer is reused to transpose the
-// codes for the optional [K,N] copy.  32 KB of shared memory and few registers
-// per thread keep several blocks in flight per SM.
-constexpr int CTP = GRP + 16;  // code staging row pitch (bytes) for the transposed copy
+// 128x128 weight blocks: one CTA per block, everything in registers.  Thread
+// (warp a, lane j) loads rows 16 a .. 16 a + 15, columns 4 j .. 4 j + 3 (one
+// 8-byte load per row; a warp covers whole 256-byte rows), so the block's amax
+// is a packed bf16 maximum, a warp shuffle reduction and one exchange through
+// shared memory.  Each thread then encodes its 64 elements: one 32-bit word of
+// codes per row, and for the [K,N] copy four 4x4 byte transposes (byte
+// permutes) turn the sixteen row words into four 16-byte runs, one per column.
+// Blocks are ordered with the row block fastest, as in the fused quantizer.
+__device__ __forceinline__ uint2 ld_stream8(const uint16_t *p)
+{
+    uint2 v;
+    asm volatile("ld.global.cs.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Four rows of four bytes (r[i] = row i, column c in byte c) to four columns
+// (c[k] = column k, row i in byte i).
+__device__ __forceinline__ void transpose4x4(const uint32_t (&r)[4], uint32_t (&c)[4])
+{
+    const uint32_t t0 = prmt(r[0], r[1], 0x5140), t1 = prmt(r[0], r[1], 0x7362);
+    const uint32_t t2 = prmt(r[2], r[3], 0x5140), t3 = prmt(r[2], r[3], 0x7362);
+    c[0] = prmt(t0, t2, 0x5410);
+    c[1] = prmt(t0, t2, 0x7632);
+    c[2] = prmt(t1, t3, 0x5410);
+    c[3] = prmt(t1, t3, 0x7632);
+}
+
+template <bool kPrescale>
+__device__ __forceinline__ void encode_strip(const uint2 (&v)[16], const Quot &c, uint32_t (&cw)[16])
+{
+    const float2 f = make_float2(c.f, c.f), r = make_float2(c.r, c.r), nsd = make_float2(-c.sd, -c.sd);
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+        const float2 a = quot2<kPrescale>(make_float2(bf_lo(v[rr].x), bf_hi(v[rr].x)), f, r, nsd);
+        const float2 b = quot2<kPrescale>(make_float2(bf_lo(v[rr].y), bf_hi(v[rr].y)), f, r, nsd);
+        cw[rr] = e4m3x2(a.x, a.y) | (e4m3x2(b.x, b.y) << 16);
+    }
+}
 
 __global__ void __launch_bounds__(256, 4) k_quant_weight(const uint16_t *__restrict__ w, int64_t ldw,
                                                          uint8_t *__restrict__ q, int64_t ldq,
                                                          float *__restrict__ s, int64_t lds,
-                                                         uint8_t *__restrict__ qT, int64_t ldqT, int64_t NB)
+                                                         uint8_t *__restrict__ qT, int64_t ldqT, int64_t NB, int64_t KB)
 {
-    __shared__ __align__(16) uint16_t wt[GRP * GRP];  // raw block, row pitch 256 bytes
     __shared__ float red[8];
-    uint8_t *ct = reinterpret_cast<uint8_t *>(wt);     // code staging, reuses the raw buffer
-    const int t = threadIdx.x, lane = t & 31, half = lane >> 4, l16 = lane & 15, warp = t >> 5;
-    const int hw16 = warp * 2 + half;
-    const int64_t kb = blockIdx.x;
+    const int t = threadIdx.x, j = t & 31, a = t >> 5;
 
-    for (int64_t nb = blockIdx.y; nb < NB; nb += gridDim.y) {
+    for (int64_t kb = blockIdx.y; kb < KB; kb += gridDim.y)
+    for (int64_t nb = blockIdx.x; nb < NB; nb += gridDim.x) {
         const int64_t n0 = nb * GRP;
-        // ---- read, amax, stash
-        uint4 v[8];
+        const uint16_t *src = w + (n0 + 16 * a) * ldw + kb * GRP + 4 * j;
+        uint2 v[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            v[i] = ld_stream(w + (n0 + hw16 + 16 * i) * ldw + kb * GRP + l16 * 8);
-        float a = 0.0f;
+        for (int rr = 0; rr < 16; ++rr)
+            v[rr] = ld_stream8(src + rr * ldw);
+        uint32_t m = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float f[8];
-            unpack8(v[i], f);
-            a = fmaxf(a, amax8(f));
-            *reinterpret_cast<uint4 *>(&wt[(hw16 + 16 * i) * GRP + l16 * 8]) = v[i];
-        }
+        for (int rr = 0; rr < 16; ++rr)
+            m = bmax2(m, bmax2(babs2(v[rr].x), babs2(v[rr].y)));
+        float am = bmax_final(m);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1)
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-        if (lane == 0)
-            red[warp] = a;
+            am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+        if (j == 0)
+            red[a] = am;
         __syncthreads();
-        a = red[0];
+        am = red[0];
 #pragma unroll
         for (int i = 1; i < 8; ++i)
-            a = fmaxf(a, red[i]);
-        const float sc = group_scale(a);
+            am = fmaxf(am, red[i]);
+        const float sc = group_scale(am);
         const Quot c = make_quot(sc);
         if (t == 0)
             s[nb * lds + kb] = sc;
-        // ---- quantize from shared memory
-        uint2 cd[8];
+        uint32_t cw[16];  // codes of row 16 a + rr, columns 4 j .. 4 j + 3
+        if (c.f == 1.0f)
+            encode_strip<false>(v, c, cw);
+        else
+            encode_strip<true>(v, c, cw);
+        uint8_t *dst = q + (n0 + 16 * a) * ldq + kb * GRP + 4 * j;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = hw16 + 16 * i;
-            float f[8];
-            unpack8(*reinterpret_cast<const uint4 *>(&wt[r * GRP + l16 * 8]), f);
-            cd[i] = encode8(f, c);
-            *reinterpret_cast<uint2 *>(q + (n0 + r) * ldq + kb * GRP + l16 * 8) = cd[i];
-        }
+        for (int rr = 0; rr < 16; ++rr)
+            *reinterpret_cast<uint32_t *>(dst + rr * ldq) = cw[rr];
         if (qT) {
-            __syncthreads();  // the raw block is no longer read: reuse it for the codes
+            uint32_t col[4][4];  // col[k][b]: column 4 j + k, rows 16 a + 4 b .. + 3
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                *reinterpret_cast<uint2 *>(&ct[(hw16 + 16 * i) * CTP + l16 * 8]) = cd[i];
-            __syncthreads();
-            // thread -> output row k0 + cc of qT, 64 consecutive n (rows nh*64 .. +63 of the block)
-            const int cc = t >> 1, nh = t & 1;
-            uint32_t wv[16];
+            for (int b = 0; b < 4; ++b) {
+                const uint32_t rw[4] = {cw[4 * b], cw[4 * b + 1], cw[4 * b + 2], cw[4 * b + 3]};
+                uint32_t cc[4];
+                transpose4x4(rw, cc);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int r = nh * 64 + 4 * j;
-                wv[j] = (uint32_t)ct[(r + 0) * CTP + cc] | ((uint32_t)ct[(r + 1) * CTP + cc] << 8) |
-                        ((uint32_t)ct[(r + 2) * CTP + cc] << 16) | ((uint32_t)ct[(r + 3) * CTP + cc] << 24);
+                for (int k = 0; k < 4; ++k)
+                    col[k][b] = cc[k];
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(qT + (kb * GRP + cc) * ldqT + n0 + nh * 64);
+            uint8_t *dT = qT + (kb * GRP + 4 * j) * ldqT + n0 + 16 * a;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                dst[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4 *>(dT + k * ldqT) = make_uint4(col[k][0], col[k][1], col[k][2], col[k][3]);
         }
-        __syncthreads();  // wt / red are reused by the next block
+        __syncthreads();  // red is reused by the next block
     }
 }
 
@@ -482,18 +596,18 @@ cudaError_t launch_quant_dual(const uint16_t *x, int64_t M, int64_t K, int64_t l
                               float *s, int64_t lds, uint8_t *qT, int64_t ldqT, float *sc, int64_t ldsc,
                               cudaStream_t st)
 {
-    const int64_t MB = (M + GRP - 1) / GRP;
-    const dim3 grid((unsigned)(K / GRP), (unsigned)(MB < 65535 ? MB : 65535));
-    k_quant_dual<<<grid, 256, 0, st>>>(x, M, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, MB);
+    const int64_t MB = (M + GRP - 1) / GRP, KB = K / GRP;
+    const dim3 grid((unsigned)(MB < 0x7FFFFFFF ? MB : 0x7FFFFFFF), (unsigned)(KB < 65535 ? KB : 65535));
+    k_quant_dual<<<grid, 256, 0, st>>>(x, M, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, MB, KB);
     return cudaGetLastError();
 }
 
 cudaError_t launch_quant_weight(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
                                 float *s, int64_t lds, uint8_t *qT, int64_t ldqT, cudaStream_t st)
 {
-    const int64_t NB = N / GRP;
-    const dim3 grid((unsigned)(K / GRP), (unsigned)(NB < 65535 ? NB : 65535));
-    k_quant_weight<<<grid, 256, 0, st>>>(w, ldw, q, ldq, s, lds, qT, ldqT, NB);
+    const int64_t NB = N / GRP, KB = K / GRP;
+    const dim3 grid((unsigned)(NB < 0x7FFFFFFF ? NB : 0x7FFFFFFF), (unsigned)(KB < 65535 ? KB : 65535));
+    k_quant_weight<<<grid, 256, 0, st>>>(w, ldw, q, ldq, s, lds, qT, ldqT, NB, KB);
     return cudaGetLastError();
 }
 
