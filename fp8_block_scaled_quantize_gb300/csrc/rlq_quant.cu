@@ -135,40 +135,66 @@ __device__ __forceinline__ void encode_cols(const uint32_t *col, int rq, int tp2
     }
 }
 
-__device__ __forceinline__ float amax8(const float (&f)[8])
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
 {
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        a = fmaxf(a, fabsf(f[i]));
-    return a;
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
-// amax over the 16 lanes of a half-warp (all 32 lanes must call).
-__device__ __forceinline__ float halfwarp_max(float a)
+__device__ __forceinline__ uint32_t babs2(uint32_t a) { return a & 0x7FFF7FFFu; }
+
+// amax of a packed pair of candidates; an all-NaN group reads as 0, as a
+// running fmaxf from 0 would give.
+__device__ __forceinline__ float bmax_final(uint32_t p) { return fmaxf(fmaxf(bf_lo(p), bf_hi(p)), 0.0f); }
+
+// max(|a|, |b|) per half, with the sign of the product (only the magnitude is used)
+__device__ __forceinline__ uint32_t bmaxabs2(uint32_t a, uint32_t b)
 {
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1)
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-    return a;
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
-// One 1x128 group held by a half-warp (8 values per lane): quantize and store.
-__device__ __forceinline__ void row_group(const uint4 &v, bool valid, int64_t m, int64_t kb, int l16,
-                                          uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ s,
-                                          int64_t lds)
+// Two 1x128 groups held by a half-warp (8 values per lane of each): the groups'
+// maxima are reduced in one exchange (the first step hands group a to lanes 0..7
+// and group b to lanes 8..15), each lane computes one scale, and lanes 0 and 8
+// of the half hand (r, s, f) of their group to the encoding lanes.
+__device__ __forceinline__ void row_groups2(const uint4 &va, const uint4 &vb, bool valid_a, bool valid_b,
+                                            int64_t ma, int64_t kba, int64_t mb, int64_t kbb, int lane,
+                                            uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ s, int64_t lds)
 {
+    const int l16 = lane & 15;
+    const uint32_t pa = bmaxabs2(bmaxabs2(va.x, va.y), bmaxabs2(va.z, va.w));
+    const uint32_t pb = bmaxabs2(bmaxabs2(vb.x, vb.y), bmaxabs2(vb.z, vb.w));
+    const bool upper = l16 & 8;
+    uint32_t p = bmaxabs2(upper ? pb : pa, __shfl_xor_sync(0xFFFFFFFFu, upper ? pa : pb, 8));
+    p = bmaxabs2(p, __shfl_xor_sync(0xFFFFFFFFu, p, 4));
+    p = bmaxabs2(p, __shfl_xor_sync(0xFFFFFFFFu, p, 2));
+    p = babs2(bmaxabs2(p, __shfl_xor_sync(0xFFFFFFFFu, p, 1)));
+    const float own_s = group_scale(bmax_final(p));
+    const Quot own = make_quot(own_s);
+    if (l16 == 0 && valid_a)
+        s[kba * lds + ma] = own_s;
+    if (l16 == 8 && valid_b)
+        s[kbb * lds + mb] = own_s;
+    const int src_a = lane & 16, src_b = src_a | 8;
+    Quot ca, cb;
+    ca.r = __shfl_sync(0xFFFFFFFFu, own.r, src_a);
+    ca.sd = __shfl_sync(0xFFFFFFFFu, own.sd, src_a);
+    ca.f = __shfl_sync(0xFFFFFFFFu, own.f, src_a);
+    cb.r = __shfl_sync(0xFFFFFFFFu, own.r, src_b);
+    cb.sd = __shfl_sync(0xFFFFFFFFu, own.sd, src_b);
+    cb.f = __shfl_sync(0xFFFFFFFFu, own.f, src_b);
     float f[8];
-    unpack8(v, f);
-    const float amax = halfwarp_max(amax8(f));
-    const float sc = group_scale(amax);
-    const Quot c = make_quot(sc);
-    const uint2 codes = encode8(f, c);
-    if (valid) {
-        *reinterpret_cast<uint2 *>(q + m * ldq + kb * GRP + l16 * 8) = codes;
-        if (l16 == 0)
-            s[kb * lds + m] = sc;
-    }
+    unpack8(va, f);
+    const uint2 codes_a = encode8(f, ca);
+    unpack8(vb, f);
+    const uint2 codes_b = encode8(f, cb);
+    if (valid_a)
+        *reinterpret_cast<uint2 *>(q + ma * ldq + kba * GRP + l16 * 8) = codes_a;
+    if (valid_b)
+        *reinterpret_cast<uint2 *>(q + mb * ldq + kbb * GRP + l16 * 8) = codes_b;
 }
 
 // ---------------------------------------------------------------------------
@@ -216,8 +242,7 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t *__restrict__
         second(mn, kbn, mn1, kbn1);
         const uint4 an = mn < M ? ld_stream(x + mn * ldx + (int64_t)kbn * GRP + l16 * 8) : zero;
         const uint4 bn = mn1 < M ? ld_stream(x + mn1 * ldx + (int64_t)kbn1 * GRP + l16 * 8) : zero;
-        row_group(a, m < M, m, kb, l16, q, ldq, s, lds);
-        row_group(b, m1 < M, m1, kb1, l16, q, ldq, s, lds);
+        row_groups2(a, b, m < M, m1 < M, m, kb, m1, kb1, lane, q, ldq, s, lds);
         a = an;
         b = bn;
         m = mn;
@@ -250,19 +275,6 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t *__restrict__
 // whole rows of the transposed codes (contiguous 128-byte pieces of one row)
 // rather than one piece of many rows.
 constexpr int TP = GRP + 8;  // staging row pitch in bf16 elements
-
-__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t babs2(uint32_t a) { return a & 0x7FFF7FFFu; }
-
-// amax of a packed pair of candidates; an all-NaN group reads as 0, as a
-// running fmaxf from 0 would give.
-__device__ __forceinline__ float bmax_final(uint32_t p) { return fmaxf(fmaxf(bf_lo(p), bf_hi(p)), 0.0f); }
 
 // Row codes of the eight rows a lane holds, read back from the staged tile (each
 // lane reads the words it wrote itself); (r, s[, f]) of row group i come from
