@@ -55,6 +55,40 @@ def test_weight_parity(N, K, transposed):
         assert np.array_equal(np_(qT), oqT)
 
 
+
+def _group_scaled(seed, M, K, span=30):
+    """N(0,1) values times 2^e with e drawn per 1x128 group, times a per-column
+    factor in [1, 2): every row group, column group and 128x128 block of a tile
+    has its own magnitude."""
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal((M, K)).astype(np.float32)
+    e = rng.integers(-span, span + 1, size=(M, K // 128))
+    v *= np.exp2(e).repeat(128, axis=1).astype(np.float32)
+    v *= (1.0 + rng.random((1, K))).astype(np.float32)
+    return I.to_bf16_bits(v)
+
+
+@pytest.mark.parametrize("M,K", [(128, 256), (300, 512), (1000, 384)])
+def test_group_scales_differ_within_a_tile(M, K):
+    """A scale handed to the wrong group (row or column) or computed from the wrong
+    lanes changes codes here, since no two neighbouring groups share a magnitude."""
+    x = _group_scaled(31, M, K)
+    q, s, qT, sc = rlq.quant_act_1x128(to_dev(x), colwise=True)
+    _check_rows(x, q, s)
+    _check_cols(x, qT, sc)
+    q2, s2, _, _ = rlq.quant_act_1x128(to_dev(x))
+    _check_rows(x, q2, s2)
+
+
+def test_weight_block_scales_differ():
+    """Weight blocks with magnitudes 2^-30 .. 2^30 apart, with the transposed copy."""
+    w = _group_scaled(32, 640, 768)
+    q, s, qT = rlq.quant_weight_128x128(to_dev(w), transposed=True)
+    oq, os_, oqT = oracle.quant_weight_128x128(w, transposed=True)
+    assert np.array_equal(np_(s), os_), "block scales differ"
+    assert np.array_equal(np_(q), oq), "block codes differ"
+    assert np.array_equal(np_(qT), oqT), "transposed codes differ"
+
 def _edge_matrix(M=256, K=1024):
     """Groups that stress the corner cases: all-zero and signed-zero groups,
     subnormal bf16 (subnormal scales), the largest bf16, exact E4M3
