@@ -9,10 +9,12 @@ missing instead of falling back here.
 Contents
 --------
 * ``rlq_oracle.c`` (plain C, built on first use with gcc): E4M3 encode/decode,
-  the 1x128 / 128x1 / 128x128 group quantizers and the UAQ fold.  These are
-  bit-level definitions; the GPU must reproduce their bytes exactly.
-* This module: a ctypes binding for the C part and the fp64 block-scaled GEMMs
-  over dequantized operands (NumPy), for FProp, DGrad and WGrad.
+  the 1x128 / 128x1 / 128x128 group quantizers, the per-row (per-token /
+  per-channel) quantizer and the UAQ fold.  These are bit-level definitions;
+  the GPU must reproduce their bytes exactly.
+* This module: a ctypes binding for the C part and the fp64 GEMMs over
+  dequantized operands (NumPy): the block-scaled FProp, DGrad and WGrad, and
+  the per-token x per-channel FProp.
 
 Sources (the web pages on quantized RL rollout):
 * Jet-RL notes, section "细粒度 GEMM 量化方案" (Fig. 6): 128x128 per-block
@@ -21,6 +23,9 @@ Sources (the web pages on quantized RL rollout):
   configuration; WGrad takes a 1x128 first operand and a 128x1 second operand.
 * QuRL notes, section 关键设计 §1 (UAQ): WX = (W/s)(sX), s applied per column
   of W and per row of the previous activation.
+* QuRL notes, section "损失函数 / 训练策略": channel-wise weight and token-wise
+  activation quantization (INT8 or FP8; the FP8 form here): one group per row
+  over all K columns, the scales factored out of the GEMM's sum.
 * The FP8 sub-format (E4M3, max 448), the scale rule (amax/448, 1.0 for an
   all-zero group), RN-satfinite rounding and fp32 IEEE division are the
   plainest readings of what the pages leave open.
@@ -85,6 +90,7 @@ def lib() -> ctypes.CDLL:
             L.orc_quant_rows_1x128.argtypes = [_P, _I, _I, _I, _P, _I, _P, _I]
             L.orc_quant_cols_128x1.argtypes = [_P, _I, _I, _I, _P, _I, _P, _I]
             L.orc_quant_weight_128x128.argtypes = [_P, _I, _I, _I, _P, _I, _P, _I, _P, _I]
+            L.orc_quant_per_row.argtypes = [_P, _I, _I, _I, _P, _I, _P]
             L.orc_uaq_fold.argtypes = [_P, _I, _I, _I, _P, _P, _I, _I]
             L.orc_e4m3_encode_array.argtypes = [_P, _I, _P]
             L.orc_e4m3_decode_array.argtypes = [_P, _I, _P]
@@ -220,6 +226,21 @@ def quant_weight_128x128(w, transposed: bool = False):
     return q, s, qT
 
 
+def quant_per_row(x):
+    """One group per row over all K columns: per-token activations (rows of X)
+    or per-channel weights (rows of W, one per output channel).  QuRL notes,
+    "损失函数 / 训练策略" (channel-wise weights, token-wise activations).
+
+    x: bf16 bits [M,K] (any K >= 1).  Returns (q u8 [M,K], s f32 [M]).
+    """
+    x = _bf16_2d(x)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((M,), np.float32)
+    lib().orc_quant_per_row(_ptr(x), M, K, K, _ptr(q), K, _ptr(s))
+    return q, s
+
+
 def uaq_fold(w, s, prev=None):
     """UAQ fold on copies: returns (W / s per column, prev * s per column).
 
@@ -309,6 +330,20 @@ def gemm_wgrad(qdyT, sdyc, qxT, sxc, rows=None, cols=None) -> np.ndarray:
     rows = np.arange(qdyT.shape[0]) if rows is None else np.asarray(rows)
     cols = np.arange(qxT.shape[0]) if cols is None else np.asarray(cols)
     return block_scaled_gemm(qdyT[rows], sdyc[:, rows], qxT[cols], sxc[:, cols])
+
+
+def gemm_per_channel(qx, sx, qw, sw, rows=None, cols=None) -> np.ndarray:
+    """Y = diag(sx) (Qx Qw^T) diag(sw): per-token X codes qx [M,K] with sx [M],
+    per-channel W codes qw [N,K] with sw [N].  The scales are constant along K,
+    so they factor out of the sum: the code products and the K-term sum are exact
+    in fp64 (K <= 2^20), and only the two scalings round.
+    """
+    qx, qw = np.asarray(qx), np.asarray(qw)
+    sx, sw = np.asarray(sx, np.float64), np.asarray(sw, np.float64)
+    rows = np.arange(qx.shape[0]) if rows is None else np.asarray(rows)
+    cols = np.arange(qw.shape[0]) if cols is None else np.asarray(cols)
+    p = dequant_codes(qx[rows]) @ dequant_codes(qw[cols]).T
+    return sx[rows][:, None] * p * sw[cols][None, :]
 
 
 def dequant_rows(q, s) -> np.ndarray:

@@ -21,6 +21,10 @@
  *    Per group: amax = max |x|, s = fl32(amax / 448) (1.0 when amax == 0),
  *    q = encode(fl32(x / s)) with IEEE fp32 division.  Scales are dequant
  *    multipliers: x ~= decode(q) * s.
+ *  - Per-token activation and per-channel weight quantization (QuRL notes,
+ *    "损失函数 / 训练策略": channel-wise weight and token-wise activation
+ *    quantization, FP8 here): one group per row over all K columns, the same
+ *    scale rule and encoding.
  *  - The UAQ invariant-scaling fold WX = (W/s)(sX) (QuRL notes, 关键设计 §1):
  *    W'[n,k] = bf16_RN(fl32(W[n,k] / s_k)),  P'[r,k] = bf16_RN(fl32(P[r,k] * s_k)).
  *
@@ -154,6 +158,27 @@ void orc_quant_rows_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
             for (int i = 0; i < GRP; ++i)
                 q[m * ldq + kb * GRP + i] = orc_e4m3_encode(bf16_bits_to_f32(g[i]) / sc);
         }
+    }
+}
+
+/* One group per row over all K columns (per-token activations, per-channel
+ * weights).  x bf16 [M,K] (pitch ldx); q u8 [M,K] (pitch ldq); s f32 [M]. */
+void orc_quant_per_row(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                       uint8_t *q, int64_t ldq, float *s)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *row = x + m * ldx;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(bf16_bits_to_f32(row[k]));
+            if (a > amax)
+                amax = a;
+        }
+        float sc = group_scale(amax);
+        s[m] = sc;
+        for (int64_t k = 0; k < K; ++k)
+            q[m * ldq + k] = orc_e4m3_encode(bf16_bits_to_f32(row[k]) / sc);
     }
 }
 
