@@ -565,8 +565,9 @@ def run_sweep(args):
     def gemm_bytes(Mr, Nc, L):
         return Mr * L + Nc * L + 2 * Mr * Nc + 4 * (Mr + Nc) * ((L + 127) // 128)
 
-    def linear(cfg, x, w, dy=None, s=None, full=False):
-        """Time the quantizers, fold and GEMMs of one linear layer."""
+    def linear(cfg, x, w, dy=None, s=None, full=False, per_channel=False):
+        """Time the quantizers, fold and GEMMs of one linear layer (with
+        ``per_channel`` also the per-token / per-channel quantizers and FProp)."""
         M, K = x.shape
         N = w.shape[0]
         if s is not None:
@@ -597,6 +598,24 @@ def run_sweep(args):
             emit(cfg, "gemm_fprop_splitk",
                  _time_ms(lambda: rlq.gemm_fprop(qx, sx, qw, sw, out=y, split_k=True, workspace=ws), flush),
                  nbytes=gemm_bytes(M, N, K), flop=2.0 * M * N * K)
+        if per_channel:
+            # read 2 + write 1 bytes per element, the row scale and its K/128 copies
+            emit(cfg, "quant_per_row_x", _time_ms(lambda: rlq.quant_per_row(x), flush),
+                 nbytes=3 * M * K + 4 * M * (1 + K // 128))
+            emit(cfg, "quant_per_row_w", _time_ms(lambda: rlq.quant_per_row(w), flush),
+                 nbytes=3 * N * K + 4 * N * (1 + K // 128))
+            pqx, _, psx = rlq.quant_per_row(x)
+            pqw, _, psw = rlq.quant_per_row(w)
+            emit(cfg, "gemm_fprop_per_channel",
+                 _time_ms(lambda: rlq.gemm_fprop_per_channel(pqx, psx, pqw, psw, out=y), flush),
+                 nbytes=gemm_bytes(M, N, K), flop=2.0 * M * N * K)
+            ws = _splitk_ws(rlq.GEMM_FPROP, M, N, K)
+            if ws is not None:
+                emit(cfg, "gemm_fprop_per_channel_splitk",
+                     _time_ms(lambda: rlq.gemm_fprop_per_channel(pqx, psx, pqw, psw, out=y, split_k=True,
+                                                                 workspace=ws), flush),
+                     nbytes=gemm_bytes(M, N, K), flop=2.0 * M * N * K)
+            del pqx, pqw, psx, psw
         if full:
             emit(cfg, "quant_dual_dy", _time_ms(lambda: rlq.quant_act_1x128(dy, colwise=True), flush),
                  nbytes=B_DUAL * M * N)
@@ -639,7 +658,8 @@ def run_sweep(args):
         w = _dev_normal(gen, (N, K), 0.02)
         s = np.random.default_rng(3).uniform(1.5, 4.0, K).astype(np.float32)
         for M in I.QWEN7B_M:
-            linear(f"qwen7b_{which} M={M} N={N} K={K}", _dev_normal(gen, (M, K), 1.0, t_frac=0.01), w, s=s)
+            linear(f"qwen7b_{which} M={M} N={N} K={K}", _dev_normal(gen, (M, K), 1.0, t_frac=0.01), w, s=s,
+                   per_channel=True)
         del w
     # 32B sweep: all three passes per M
     gen.manual_seed(4)

@@ -115,6 +115,23 @@ rlq_status rlq_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t 
     return cuda_status(launch_quant_rows(x, M, K, ldx, q, ldq, s, lds, cs(stream)), "1x128 quantizer launch");
 }
 
+rlq_status rlq_quant_per_row(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, int64_t ldq, float *s,
+                             float *s_rep, int64_t ld_rep, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(M >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size (M=%lld, K=%lld)", (long long)M, (long long)K);
+    RLQ_REQUIRE(K % G == 0, RLQ_ERR_UNSUPPORTED, "K=%lld is not a multiple of 128", (long long)K);
+    RLQ_REQUIRE(M < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    if (M == 0 || K == 0)
+        return RLQ_OK;
+    RLQ_TRY(check_bf16("x", x, ldx, K));
+    RLQ_TRY(check_codes("q", q, ldq, K));
+    RLQ_TRY(check_scales("s", s, M, M));
+    if (s_rep)
+        RLQ_TRY(check_scales("s_rep", s_rep, ld_rep, M));
+    return cuda_status(launch_quant_per_row(x, M, K, ldx, q, ldq, s, s_rep, ld_rep, cs(stream)),
+                       "per-row quantizer launch");
+}
+
 rlq_status rlq_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
                                     float *s, int64_t lds, uint8_t *qT, int64_t ldqT, rlq_stream_t stream)
 {
@@ -266,6 +283,46 @@ rlq_status gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, in
     return launch_gemm(a, cs(stream));
 }
 
+rlq_status gemm_fprop_per_channel(const uint8_t *xq, int64_t ldxq, const float *xs_rep, int64_t ldxs, const uint8_t *wq,
+                                  int64_t ldwq, const float *ws_rep, int64_t ldws, uint16_t *y, int64_t ldy, int64_t M,
+                                  int64_t N, int64_t K, void *workspace, int64_t workspace_bytes, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
+    RLQ_REQUIRE(N % G == 0 && K % G == 0, RLQ_ERR_UNSUPPORTED, "N=%lld and K=%lld must be multiples of 128",
+                (long long)N, (long long)K);
+    RLQ_REQUIRE(M < MAX_DIM && N < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    if (M == 0 || N == 0)
+        return RLQ_OK;
+    RLQ_TRY(check_bf16("y", y, ldy, N));
+    if (K > 0) {
+        RLQ_TRY(check_codes("xq", xq, ldxq, K));
+        RLQ_TRY(check_codes("wq", wq, ldwq, K));
+        RLQ_TRY(check_scales("xs_rep", xs_rep, ldxs, M));
+        RLQ_TRY(check_scales("ws_rep", ws_rep, ldws, N));
+        RLQ_REQUIRE(al(ws_rep, 16) && ldws % 4 == 0, RLQ_ERR_MISALIGNED,
+                    "ws_rep rows must be 16-byte aligned (pointer 16-byte aligned, pitch a multiple of 4)");
+    }
+    GemmArgs a{};
+    a.A = xq;
+    a.lda = ldxq;
+    a.B = wq;
+    a.ldb = ldwq;
+    a.sa = xs_rep;
+    a.ld_sa = ldxs;
+    a.sb = ws_rep;
+    a.sb_bstride = ldws;
+    a.sb_cstride = 0;
+    a.per_col_sb = true;
+    a.out = y;
+    a.ldo = ldy;
+    a.R = M;
+    a.C = N;
+    a.L = K;
+    a.ws = static_cast<float *>(workspace);
+    a.ws_bytes = workspace_bytes;
+    return launch_gemm(a, cs(stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -290,6 +347,13 @@ rlq_status rlq_gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc
                           int64_t N, int64_t K, rlq_stream_t stream)
 {
     return gemm_wgrad(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K, nullptr, 0, stream);
+}
+
+rlq_status rlq_gemm_fprop_per_channel(const uint8_t *xq, int64_t ldxq, const float *xs_rep, int64_t ldxs,
+                                      const uint8_t *wq, int64_t ldwq, const float *ws_rep, int64_t ldws, uint16_t *y,
+                                      int64_t ldy, int64_t M, int64_t N, int64_t K, rlq_stream_t stream)
+{
+    return gemm_fprop_per_channel(xq, ldxq, xs_rep, ldxs, wq, ldwq, ws_rep, ldws, y, ldy, M, N, K, nullptr, 0, stream);
 }
 
 rlq_status rlq_gemm_splitk_workspace_bytes(rlq_gemm_kind kind, int64_t M, int64_t N, int64_t K, int64_t *bytes)
@@ -321,6 +385,16 @@ rlq_status rlq_gemm_fprop_splitk(const uint8_t *xq, int64_t ldxq, const float *x
 {
     RLQ_TRY(check_workspace(workspace, workspace_bytes));
     return gemm_fprop(xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, workspace, workspace_bytes, stream);
+}
+
+rlq_status rlq_gemm_fprop_per_channel_splitk(const uint8_t *xq, int64_t ldxq, const float *xs_rep, int64_t ldxs,
+                                             const uint8_t *wq, int64_t ldwq, const float *ws_rep, int64_t ldws,
+                                             uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                                             void *workspace, int64_t workspace_bytes, rlq_stream_t stream)
+{
+    RLQ_TRY(check_workspace(workspace, workspace_bytes));
+    return gemm_fprop_per_channel(xq, ldxq, xs_rep, ldxs, wq, ldwq, ws_rep, ldws, y, ldy, M, N, K, workspace,
+                                  workspace_bytes, stream);
 }
 
 rlq_status rlq_gemm_dgrad_splitk(const uint8_t *dyq, int64_t lddyq, const float *dys, int64_t lddys, const uint8_t *w,

@@ -536,6 +536,93 @@ __global__ void __launch_bounds__(256, 4) k_quant_weight(const uint16_t *__restr
 }
 
 // ---------------------------------------------------------------------------
+// Per-row quantization (QuRL notes, "损失函数 / 训练策略": per-token activations,
+// per-channel weights): one group per row over all K columns.  A row is taken
+// by one warp (kThreads = 32: enough rows to fill the GPU, or rows of at most
+// 4096 elements) or by a whole CTA (kThreads = 256: few, long rows).  Pass 1 reads the row (16-byte loads, four
+// in flight per lane) and takes the packed bf16 maximum, reduced by shuffles
+// (and across the CTA's warps through shared memory); one thread computes the
+// scale once and hands (r, s, f) to the others; pass 2 reads the row again,
+// from L2 (it was read moments before), encodes it and stores the codes.  With
+// s_rep set, the scale is also written to s_rep[kb * ld_rep + m] for every
+// K-block, the layout the column-scaled GEMM reads.
+template <bool kPrescale>
+__device__ __forceinline__ void per_row_codes(const uint16_t *__restrict__ row, int64_t K, int t, int stride,
+                                              const Quot &c, uint8_t *__restrict__ qrow)
+{
+#pragma unroll 4
+    for (int64_t k = (int64_t)t * 8; k < K; k += stride) {
+        float f[8];
+        unpack8(ld_stream(row + k), f);
+        *reinterpret_cast<uint2 *>(qrow + k) = encode8_t<kPrescale>(f, c);
+    }
+}
+
+template <int kThreads>
+__global__ void __launch_bounds__(256) k_quant_per_row(const uint16_t *__restrict__ x, int64_t M, int64_t K,
+                                                       int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
+                                                       float *__restrict__ s, float *__restrict__ s_rep,
+                                                       int64_t ld_rep)
+{
+    __shared__ uint32_t red[8];
+    __shared__ float sh[4];  // s, r, s*f, f of the CTA's row
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = threadIdx.x % kThreads;  // thread within the row's team
+    const int64_t team = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kThreads;
+    const int64_t nteams = ((int64_t)gridDim.x * blockDim.x) / kThreads;
+    for (int64_t m = team; m < M; m += nteams) {
+        const uint16_t *row = x + m * ldx;
+        uint32_t pm = 0;
+#pragma unroll 4
+        for (int64_t k = (int64_t)t * 8; k < K; k += 8 * kThreads) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(row + k);  // kept in L2 for pass 2
+            pm = bmaxabs2(pm, bmaxabs2(bmaxabs2(v.x, v.y), bmaxabs2(v.z, v.w)));
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            pm = bmaxabs2(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, o));
+        float sc = 0.0f;
+        Quot c{1.0f, 1.0f, 1.0f};
+        if (kThreads == 32) {
+            if (lane == 0) {
+                sc = group_scale(bmax_final(babs2(pm)));
+                c = make_quot(sc);
+                s[m] = sc;
+            }
+            sc = __shfl_sync(0xFFFFFFFFu, sc, 0);
+            c.r = __shfl_sync(0xFFFFFFFFu, c.r, 0);
+            c.sd = __shfl_sync(0xFFFFFFFFu, c.sd, 0);
+            c.f = __shfl_sync(0xFFFFFFFFu, c.f, 0);
+        } else {
+            if (lane == 0)
+                red[warp] = babs2(pm);
+            __syncthreads();
+            if (t == 0) {
+                uint32_t a = red[0];
+#pragma unroll
+                for (int w = 1; w < kThreads / 32; ++w)
+                    a = bmax2(a, red[w]);
+                const float v = group_scale(bmax_final(a));
+                const Quot cq = make_quot(v);
+                sh[0] = v, sh[1] = cq.r, sh[2] = cq.sd, sh[3] = cq.f;
+                s[m] = v;
+            }
+            __syncthreads();
+            sc = sh[0], c.r = sh[1], c.sd = sh[2], c.f = sh[3];
+        }
+        if (s_rep)
+            for (int64_t kb = t; kb < K / GRP; kb += kThreads)
+                s_rep[kb * ld_rep + m] = sc;
+        if (c.f == 1.0f)
+            per_row_codes<false>(row, K, t, 8 * kThreads, c, q + m * ldq);
+        else
+            per_row_codes<true>(row, K, t, 8 * kThreads, c, q + m * ldq);
+        if (kThreads > 32)
+            __syncthreads();  // red and sh are reused by the next row
+    }
+}
+
+// ---------------------------------------------------------------------------
 // UAQ fold, in place: divide (w) or multiply (prev) column k by s[k] in fp32,
 // round to bf16.  8 elements per thread and vector; each thread handles FOLD_ROWS
 // rows per iteration with all their loads issued first (bytes in flight hide
@@ -620,6 +707,21 @@ cudaError_t launch_quant_weight(const uint16_t *w, int64_t N, int64_t K, int64_t
     const int64_t NB = N / GRP, KB = K / GRP;
     const dim3 grid((unsigned)(NB < 0x7FFFFFFF ? NB : 0x7FFFFFFF), (unsigned)(KB < 65535 ? KB : 65535));
     k_quant_weight<<<grid, 256, 0, st>>>(w, ldw, q, ldq, s, lds, qT, ldqT, NB, KB);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_per_row(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, int64_t ldq,
+                                 float *s, float *s_rep, int64_t ld_rep, cudaStream_t st)
+{
+    const int64_t sms = sm_count();
+    if (M >= sms * 64 || K <= 4096) {  // enough rows for every resident warp, or short rows: a warp per row
+        int64_t blocks = (M + 7) / 8;
+        if (blocks > sms * 8 * 16)
+            blocks = sms * 8 * 16;
+        k_quant_per_row<32><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+    } else {  // few, long rows: a CTA per row
+        k_quant_per_row<256><<<(unsigned)M, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+    }
     return cudaGetLastError();
 }
 

@@ -34,6 +34,9 @@ _SIGS = {
     "rlq_gemm_dgrad_splitk": [_P, _I, _P, _I, _P, _I, ctypes.c_int, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_gemm_wgrad_splitk": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_gemm_fprop_splitk_static": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
+    "rlq_quant_per_row": [_P, _I, _I, _I, _P, _I, _P, _P, _I, _P],
+    "rlq_gemm_fprop_per_channel": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
+    "rlq_gemm_fprop_per_channel_splitk": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_uaq_fold": [_P, _I, _I, _I, _P, _P, _I, _I, _P],
     "rlq_check": [_P],
     "rlq_diag_bounded_wait": [_I, _P],
@@ -148,6 +151,21 @@ def rlq_gemm_fprop_splitk_static(xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy,
     return _call("rlq_gemm_fprop_splitk_static", xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, stream)
 
 
+def rlq_quant_per_row(x, M, K, ldx, q, ldq, s, s_rep, ld_rep, stream):
+    return _call("rlq_quant_per_row", x, M, K, ldx, q, ldq, s, s_rep, ld_rep, stream)
+
+
+def rlq_gemm_fprop_per_channel(xq, ldxq, xs_rep, ldxs, wq, ldwq, ws_rep, ldws, y, ldy, M, N, K, stream):
+    return _call("rlq_gemm_fprop_per_channel", xq, ldxq, xs_rep, ldxs, wq, ldwq, ws_rep, ldws, y, ldy, M, N, K,
+                 stream)
+
+
+def rlq_gemm_fprop_per_channel_splitk(xq, ldxq, xs_rep, ldxs, wq, ldwq, ws_rep, ldws, y, ldy, M, N, K, workspace,
+                                      workspace_bytes, stream):
+    return _call("rlq_gemm_fprop_per_channel_splitk", xq, ldxq, xs_rep, ldxs, wq, ldwq, ws_rep, ldws, y, ldy, M, N,
+                 K, workspace, workspace_bytes, stream)
+
+
 def rlq_uaq_fold(w, N, K, ldw, s, prev, R, ldp, stream):
     return _call("rlq_uaq_fold", w, N, K, ldw, s, prev, R, ldp, stream)
 
@@ -239,6 +257,43 @@ def quant_weight_128x128(w: torch.Tensor, transposed: bool = False, stream=None)
     rlq_quant_weight_128x128(w.data_ptr(), N, K, _ld(w), q.data_ptr(), K, s.data_ptr(), max(K // GRP, 1),
                              _ptr(qT), N if qT is not None else 0, _stream(stream))
     return q, s, qT
+
+
+def quant_per_row(x: torch.Tensor, replicate: bool = True, stream=None):
+    """Per-row FP8 quantization of bf16 x [M, K] (per-token activations, or
+    per-channel weights with x = W).
+
+    Returns (q [M,K] u8, s [M] f32, s_rep [K/128, M] f32 or None): s_rep holds
+    each row's scale once per K-block, the layout ``gemm_fprop_per_channel`` reads.
+    """
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    M, K = x.shape
+    dev = x.device
+    q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((max(M, 1),), dtype=torch.float32, device=dev)[:M]
+    Mp = _round_up(max(M, 1), 4)
+    s_rep = torch.empty((K // GRP, Mp), dtype=torch.float32, device=dev)[:, :M] if replicate else None
+    rlq_quant_per_row(x.data_ptr(), M, K, _ld(x), q.data_ptr(), K, s.data_ptr(), _ptr(s_rep),
+                      Mp if replicate else 0, _stream(stream))
+    return q, s, s_rep
+
+
+def gemm_fprop_per_channel(xq, xs_rep, wq, ws_rep, out=None, stream=None, split_k: bool = False, workspace=None):
+    """Y [M, N] bf16 = diag(sx) Qx Qw^T diag(sw) from per-token X codes and
+    per-channel W codes, with the scales in the replicated [K/128, rows] layout.
+    ``split_k`` as in ``gemm_fprop`` (the FProp plan)."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    args = (xq.data_ptr(), _ld(xq), xs_rep.data_ptr(), _ld(xs_rep), wq.data_ptr(), _ld(wq), ws_rep.data_ptr(),
+            _ld(ws_rep), y.data_ptr(), _ld(y), M, N, K)
+    if split_k:
+        rlq_gemm_fprop_per_channel_splitk(*args, *_workspace(GEMM_FPROP, M, N, K, workspace, xq.device),
+                                          _stream(stream))
+    else:
+        rlq_gemm_fprop_per_channel(*args, _stream(stream))
+    return y
 
 
 def _workspace(kind: int, M: int, N: int, K: int, workspace, device):

@@ -158,6 +158,58 @@ rlq_status rlq_gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc
                           rlq_stream_t stream);
 
 /*
+ * Per-token activations and per-channel weights, FP8.  QuRL notes, "损失函数 /
+ * 训练策略": the rollout model runs with channel-wise weight quantization and
+ * token-wise activation quantization (INT8 or FP8; the FP8 form is built here).
+ *
+ * rlq_quant_per_row: one group per row over all K columns, with the scale rule
+ * and encoding of the 128-groups above (s = fl32(amax / 448), 1.0 for an
+ * all-zero row; codes RN-even satfinite of fl32(x / s)).  Per-token
+ * activations: x = X [M, K].  Per-channel weights: x = W [N, K] (one row per
+ * output channel).
+ *
+ *   x      bf16 [M, K], pitch ldx >= K
+ *   q      E4M3 [M, K], pitch ldq >= K
+ *   s      f32 [M], s[m] = the row's scale (contiguous)
+ *   s_rep  optional (NULL to skip): f32, s_rep[kb * ld_rep + m] = s[m] for every
+ *          kb < K/128, ld_rep >= M — the layout rlq_gemm_fprop_per_channel reads
+ * K % 128 == 0; M any value >= 0.
+ *
+ * rlq_gemm_fprop_per_channel: Y = diag(sx) (Qx Qw^T) diag(sw), i.e.
+ *
+ *   Y[m, n] = bf16_RN( sum_kb xs_rep[kb, m] * ws_rep[kb, n] * sum_{k in kb} x[m,k] w[n,k] )
+ *
+ * which with replicated scales (xs_rep[kb, m] = sx[m], ws_rep[kb, n] = sw[n])
+ * equals sx[m] sw[n] sum_k x[m,k] w[n,k] up to the order of the fp32 sums.
+ * The column-scaled kernel of rlq_gemm_wgrad runs it.
+ *
+ *   xq  E4M3 [M, K], pitch ldxq;  xs_rep f32, xs_rep[kb * ldxs + m], ldxs >= M
+ *   wq  E4M3 [N, K], pitch ldwq;  ws_rep f32, ws_rep[kb * ldws + n], ldws >= N,
+ *       ws_rep 16-byte aligned and ldws % 4 == 0
+ *   y   bf16 [M, N], pitch ldy >= N (output, overwritten)
+ * N % 128 == 0, K % 128 == 0.  Errors as for the other calls.
+ */
+rlq_status rlq_quant_per_row(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                             uint8_t *q, int64_t ldq, float *s, float *s_rep, int64_t ld_rep,
+                             rlq_stream_t stream);
+
+rlq_status rlq_gemm_fprop_per_channel(const uint8_t *xq, int64_t ldxq, const float *xs_rep, int64_t ldxs,
+                                      const uint8_t *wq, int64_t ldwq, const float *ws_rep, int64_t ldws,
+                                      uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                                      rlq_stream_t stream);
+
+/*
+ * Split-K form of rlq_gemm_fprop_per_channel, for decode-sized M (the rollout
+ * case): workspace, workspace_bytes and the result's summation order as for
+ * the split-K GEMMs below; rlq_gemm_splitk_workspace_bytes(RLQ_GEMM_FPROP, M,
+ * N, K, ...) gives the size of its unconstrained plan.
+ */
+rlq_status rlq_gemm_fprop_per_channel_splitk(const uint8_t *xq, int64_t ldxq, const float *xs_rep, int64_t ldxs,
+                                             const uint8_t *wq, int64_t ldwq, const float *ws_rep, int64_t ldws,
+                                             uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                                             void *workspace, int64_t workspace_bytes, rlq_stream_t stream);
+
+/*
  * Split-K forms of the three GEMMs, for outputs too small to occupy every SM
  * (decode-sized M in FProp and DGrad, a narrow layer's WGrad).  The pages'
  * GEMMs do not prescribe a tiling; this is a scheduling choice of this

@@ -125,3 +125,30 @@ def test_splitk_and_static_validation():
     assert rlq.STATIC_SCRATCH_BYTES == 16 << 20
     header = open(HEADER).read()
     assert "#define RLQ_STATIC_SCRATCH_BYTES 16777216" in header
+
+
+def test_per_row_and_per_channel_validation():
+    """Per-token / per-channel entry points: host-side checks before any launch."""
+    q = rlq.rlq_quant_per_row
+    assert _status(q, FAKE, 4, 100, 128, FAKE, 128, FAKE, None, 0, None) == 2        # K % 128
+    assert _status(q, FAKE, -1, 128, 128, FAKE, 128, FAKE, None, 0, None) == 1       # negative M
+    assert _status(q, None, 4, 128, 128, FAKE, 128, FAKE, None, 0, None) == 1        # NULL x
+    assert _status(q, FAKE, 4, 128, 128, FAKE, 128, None, None, 0, None) == 1        # NULL s
+    assert _status(q, FAKE, 4, 128, 128, FAKE, 120, FAKE, None, 0, None) == 1        # ldq < K
+    assert _status(q, FAKE, 4, 128, 128, FAKE, 128, FAKE, FAKE, 3, None) == 1        # ld_rep < M
+    assert _status(q, FAKE + 2, 4, 128, 128, FAKE, 128, FAKE, None, 0, None) == 3    # x misaligned
+    assert _status(q, FAKE, 0, 128, 128, None, 0, None, None, 0, None) == 0          # empty: no-op
+    g = rlq.rlq_gemm_fprop_per_channel
+    ok = (FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 128, FAKE, 128, 4, 128, 128, None)
+    assert _status(g, FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 128, FAKE, 136, 4, 136, 128, None) == 2  # N % 128
+    assert _status(g, FAKE, 128, FAKE, 4, FAKE, 128, FAKE + 4, 128, FAKE, 128, 4, 128, 128, None) == 3  # ws_rep
+    assert _status(g, FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 126, FAKE, 128, 4, 128, 128, None) == 1  # ldws < N
+    assert _status(g, FAKE, 128, FAKE, 3, FAKE, 128, FAKE, 128, FAKE, 128, 4, 128, 128, None) == 1  # ldxs < M
+    assert _status(g, *ok[:10], -1, *ok[11:]) == 1                                                 # negative M
+
+
+def test_per_channel_splitk_validation():
+    g = rlq.rlq_gemm_fprop_per_channel_splitk
+    args = (FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 128, FAKE, 128, 4, 128, 128)
+    assert _status(g, *args, FAKE + 4, 1 << 20, None) == 3    # workspace not 16-byte aligned
+    assert _status(g, *args, FAKE, -1, None) == 1             # negative workspace size
