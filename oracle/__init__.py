@@ -10,7 +10,7 @@ Contents
 --------
 * ``rlq_oracle.c`` (plain C, built on first use with gcc): E4M3 encode/decode,
   the 1x128 / 128x1 / 128x128 group quantizers, the per-row (per-token /
-  per-channel) quantizer and the UAQ fold.  These are bit-level definitions;
+  per-channel) quantizer, the UAQ fold and the AQN perturbation.  These are bit-level definitions;
   the GPU must reproduce their bytes exactly.
 * This module: a ctypes binding for the C part and the fp64 GEMMs over
   dequantized operands (NumPy): the block-scaled FProp, DGrad and WGrad, and
@@ -23,6 +23,8 @@ Sources (the web pages on quantized RL rollout):
   configuration; WGrad takes a 1x128 first operand and a 128x1 second operand.
 * QuRL notes, section 关键设计 §1 (UAQ): WX = (W/s)(sX), s applied per column
   of W and per row of the previous activation.
+* QeRL news article: adaptive quantization noise (AQN), channel-wise Gaussian
+  noise mapped into the LayerNorm scale, decaying on an exponential schedule.
 * QuRL notes, section "损失函数 / 训练策略": channel-wise weight and token-wise
   activation quantization (INT8 or FP8; the FP8 form here): one group per row
   over all K columns, the scales factored out of the GEMM's sum.
@@ -91,6 +93,9 @@ def lib() -> ctypes.CDLL:
             L.orc_quant_cols_128x1.argtypes = [_P, _I, _I, _I, _P, _I, _P, _I]
             L.orc_quant_weight_128x128.argtypes = [_P, _I, _I, _I, _P, _I, _P, _I, _P, _I]
             L.orc_quant_per_row.argtypes = [_P, _I, _I, _I, _P, _I, _P]
+            L.orc_aqn_sigma.restype = ctypes.c_float
+            L.orc_aqn_sigma.argtypes = [ctypes.c_float, ctypes.c_float, _I, _I]
+            L.orc_aqn_perturb.argtypes = [_P, _I, _P, ctypes.c_float]
             L.orc_uaq_fold.argtypes = [_P, _I, _I, _I, _P, _P, _I, _I]
             L.orc_e4m3_encode_array.argtypes = [_P, _I, _P]
             L.orc_e4m3_decode_array.argtypes = [_P, _I, _P]
@@ -261,6 +266,27 @@ def uaq_fold(w, s, prev=None):
     lib().orc_uaq_fold(_ptr(w), N, K, K, _ptr(s),
                        _ptr(prev) if prev is not None else None, R, K)
     return w, prev
+
+
+def aqn_sigma(sigma_start: float, sigma_end: float, t: int, T: int) -> float:
+    """Noise level of AQN step t of T: geometric from sigma_start (t = 0) to
+    sigma_end (t = T - 1), as an fp32 value.  QeRL news article: adaptive
+    quantization noise decays on an exponential schedule."""
+    return float(lib().orc_aqn_sigma(sigma_start, sigma_end, t, T))
+
+
+def aqn_perturb(gamma, z, sigma: float):
+    """AQN on a copy of a norm scale: gamma'[k] = bf16_RN(fl32(gamma[k] + fl32(sigma * z[k]))).
+
+    gamma: bf16 bits [K]; z: f32 [K] (one standard-normal draw per channel, made
+    by the caller).  QeRL news article: channel-wise Gaussian perturbations
+    mapped into the LayerNorm scale parameters."""
+    g = np.ascontiguousarray(np.asarray(gamma, dtype=np.uint16)).copy()
+    z = np.ascontiguousarray(z, dtype=np.float32)
+    if g.ndim != 1 or z.shape != g.shape:
+        raise ValueError("gamma and z must be 1-D of the same length")
+    lib().orc_aqn_perturb(_ptr(g), g.size, _ptr(z), sigma)
+    return g
 
 
 # ------------------------------------------------------------ fp64 GEMMs ---

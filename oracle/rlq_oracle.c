@@ -25,6 +25,9 @@
  *    "损失函数 / 训练策略": channel-wise weight and token-wise activation
  *    quantization, FP8 here): one group per row over all K columns, the same
  *    scale rule and encoding.
+ *  - AQN (QeRL news article): channel-wise Gaussian noise added to a norm
+ *    scale, gamma'[k] = bf16_RN(gamma[k] + sigma_t z[k]), sigma_t decaying
+ *    geometrically from sigma_start to sigma_end; z is drawn by the caller.
  *  - The UAQ invariant-scaling fold WX = (W/s)(sX) (QuRL notes, 关键设计 §1):
  *    W'[n,k] = bf16_RN(fl32(W[n,k] / s_k)),  P'[r,k] = bf16_RN(fl32(P[r,k] * s_k)).
  *
@@ -234,6 +237,30 @@ void orc_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t l
                         qT[k * ldqT + n] = c;
                 }
         }
+    }
+}
+
+/* ----------------------------------------------------------------- AQN --- */
+
+/* Noise level of step t of T (QeRL news article: channel-wise Gaussian noise in
+ * the LayerNorm scale, decaying on an exponential schedule): geometric from
+ * sigma_start at t = 0 to sigma_end at t = T - 1, computed in double and
+ * rounded once to fp32; T == 1 gives sigma_start. */
+float orc_aqn_sigma(float sigma_start, float sigma_end, int64_t t, int64_t T)
+{
+    if (T <= 1 || sigma_start == sigma_end)
+        return sigma_start;
+    double r = (double)t / (double)(T - 1);
+    return (float)((double)sigma_start * pow((double)sigma_end / (double)sigma_start, r));
+}
+
+/* gamma'[k] = bf16_RN(fl32(gamma[k] + fl32(sigma * z[k]))), in place, for a norm
+ * scale gamma (bf16 [K]) and one standard-normal draw z[k] per channel. */
+void orc_aqn_perturb(uint16_t *gamma, int64_t K, const float *z, float sigma)
+{
+    for (int64_t k = 0; k < K; ++k) {
+        float noise = sigma * z[k];
+        gamma[k] = orc_f32_to_bf16_rn(bf16_bits_to_f32(gamma[k]) + noise);
     }
 }
 
