@@ -581,6 +581,11 @@ def run_sweep(args):
                 rlq.uaq_fold_(wf, st if par[0] == 0 else inv, xf)
                 par[0] ^= 1
             emit(cfg, "uaq_fold", _time_ms(fold, flush), nbytes=4 * (N * K + M * K))
+            if per_channel:
+                # AQN on a norm scale of K channels: read 2 + 4, write 2 bytes per channel
+                gam = torch.ones(K, dtype=torch.bfloat16, device=dev)
+                zz = torch.randn(K, generator=torch.Generator(device=dev).manual_seed(5), device=dev)
+                emit(cfg, "aqn_perturb", _time_ms(lambda: rlq.aqn_perturb_(gam, zz, 1e-3), flush), nbytes=8 * K)
         emit(cfg, "quant_rows_x", _time_ms(lambda: rlq.quant_act_1x128(x), flush), nbytes=B_ROWS * M * K)
         if full:
             emit(cfg, "quant_dual_x", _time_ms(lambda: rlq.quant_act_1x128(x, colwise=True), flush),

@@ -1,6 +1,7 @@
 // C ABI of librlq.so: host-side argument validation and dispatch to the
 // kernels.  Every check runs before any launch; a failing call launches
 // nothing and leaves a description for rlq_last_error().
+#include <cmath>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -431,6 +432,41 @@ rlq_status rlq_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, const fl
     if (prev && R > 0)
         RLQ_TRY(check_bf16("prev", prev, ldp, K));
     return cuda_status(launch_uaq_fold(w, N, K, ldw, s, prev, R, ldp, cs(stream)), "UAQ fold launch");
+}
+
+rlq_status rlq_aqn_sigma(float sigma_start, float sigma_end, int64_t t, int64_t T, float *sigma)
+{
+    RLQ_REQUIRE(sigma, RLQ_ERR_INVALID_ARG, "sigma is NULL");
+    RLQ_REQUIRE(T >= 1 && t >= 0 && t < T, RLQ_ERR_INVALID_ARG, "step t=%lld outside 0 .. T-1 (T=%lld)", (long long)t,
+                (long long)T);
+    RLQ_REQUIRE(std::isfinite(sigma_start) && std::isfinite(sigma_end) && sigma_start >= 0.0f && sigma_end >= 0.0f,
+                RLQ_ERR_INVALID_ARG, "noise levels must be finite and >= 0");
+    if (T == 1 || sigma_start == sigma_end || t == 0) {
+        *sigma = sigma_start;
+        return RLQ_OK;
+    }
+    if (t == T - 1) {
+        *sigma = sigma_end;
+        return RLQ_OK;
+    }
+    RLQ_REQUIRE(sigma_start > 0.0f && sigma_end > 0.0f, RLQ_ERR_INVALID_ARG,
+                "a decaying schedule needs sigma_start > 0 and sigma_end > 0");
+    // geometric: sigma_start * (sigma_end / sigma_start)^(t / (T - 1)), in double, rounded once
+    const double frac = (double)t / (double)(T - 1);
+    *sigma = (float)((double)sigma_start * std::exp(frac * std::log((double)sigma_end / (double)sigma_start)));
+    return RLQ_OK;
+}
+
+rlq_status rlq_aqn_perturb(uint16_t *gamma, int64_t K, const float *z, float sigma, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(K >= 0, RLQ_ERR_INVALID_ARG, "negative size K=%lld", (long long)K);
+    RLQ_REQUIRE(K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    RLQ_REQUIRE(std::isfinite(sigma), RLQ_ERR_INVALID_ARG, "sigma is not finite");
+    if (K == 0)
+        return RLQ_OK;
+    RLQ_REQUIRE(gamma && z, RLQ_ERR_INVALID_ARG, "gamma or z is NULL");
+    RLQ_REQUIRE(al(gamma, 2) && al(z, 4), RLQ_ERR_MISALIGNED, "gamma must be 2-byte and z 4-byte aligned");
+    return cuda_status(launch_aqn_perturb(gamma, K, z, sigma, cs(stream)), "AQN launch");
 }
 
 rlq_status rlq_check(rlq_stream_t stream) { return check_device_errors(cs(stream)); }

@@ -623,6 +623,21 @@ __global__ void __launch_bounds__(256) k_quant_per_row(const uint16_t *__restric
 }
 
 // ---------------------------------------------------------------------------
+// AQN (QeRL news article: channel-wise Gaussian noise in the LayerNorm scale):
+// gamma[k] = bf16_RN(fl32(gamma[k] + fl32(sigma * z[k]))), in place.  The product
+// and the sum are rounded separately (no contraction into an FMA).
+__global__ void __launch_bounds__(256) k_aqn_perturb(uint16_t *__restrict__ gamma, int64_t K,
+                                                     const float *__restrict__ z, float sigma)
+{
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < K; k += (int64_t)gridDim.x * blockDim.x) {
+        const float v = __fadd_rn(bf_lo(gamma[k]), __fmul_rn(sigma, z[k]));
+        uint16_t h;
+        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(v));
+        gamma[k] = h;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // UAQ fold, in place: divide (w) or multiply (prev) column k by s[k] in fp32,
 // round to bf16.  8 elements per thread and vector; each thread handles FOLD_ROWS
 // rows per iteration with all their loads issued first (bytes in flight hide
@@ -722,6 +737,15 @@ cudaError_t launch_quant_per_row(const uint16_t *x, int64_t M, int64_t K, int64_
     } else {  // few, long rows: a CTA per row
         k_quant_per_row<256><<<(unsigned)M, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_aqn_perturb(uint16_t *gamma, int64_t K, const float *z, float sigma, cudaStream_t st)
+{
+    int64_t blocks = (K + 255) / 256;
+    if (blocks > (int64_t)sm_count() * 8)
+        blocks = (int64_t)sm_count() * 8;
+    k_aqn_perturb<<<(unsigned)blocks, 256, 0, st>>>(gamma, K, z, sigma);
     return cudaGetLastError();
 }
 

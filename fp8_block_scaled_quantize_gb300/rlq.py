@@ -38,6 +38,8 @@ _SIGS = {
     "rlq_gemm_fprop_per_channel": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
     "rlq_gemm_fprop_per_channel_splitk": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_uaq_fold": [_P, _I, _I, _I, _P, _P, _I, _I, _P],
+    "rlq_aqn_sigma": [ctypes.c_float, ctypes.c_float, _I, _I, ctypes.POINTER(ctypes.c_float)],
+    "rlq_aqn_perturb": [_P, _I, _P, ctypes.c_float, _P],
     "rlq_check": [_P],
     "rlq_diag_bounded_wait": [_I, _P],
 }
@@ -164,6 +166,16 @@ def rlq_gemm_fprop_per_channel_splitk(xq, ldxq, xs_rep, ldxs, wq, ldwq, ws_rep, 
                                       workspace_bytes, stream):
     return _call("rlq_gemm_fprop_per_channel_splitk", xq, ldxq, xs_rep, ldxs, wq, ldwq, ws_rep, ldws, y, ldy, M, N,
                  K, workspace, workspace_bytes, stream)
+
+
+def rlq_aqn_sigma(sigma_start, sigma_end, t, T) -> float:
+    out = ctypes.c_float()
+    _call("rlq_aqn_sigma", sigma_start, sigma_end, t, T, ctypes.byref(out))
+    return out.value
+
+
+def rlq_aqn_perturb(gamma, K, z, sigma, stream):
+    return _call("rlq_aqn_perturb", gamma, K, z, sigma, stream)
 
 
 def rlq_uaq_fold(w, N, K, ldw, s, prev, R, ldp, stream):
@@ -361,6 +373,17 @@ def uaq_fold_(w: torch.Tensor, s: torch.Tensor, prev: torch.Tensor | None = None
     rlq_uaq_fold(w.data_ptr(), N, K, _ld(w), s.data_ptr(), _ptr(prev), R, _ld(prev) if prev is not None else 0,
                  _stream(stream))
     return w, prev
+
+
+def aqn_perturb_(gamma: torch.Tensor, z: torch.Tensor, sigma: float, stream=None):
+    """In-place AQN: gamma[k] = bf16(gamma[k] + sigma * z[k]) for a bf16 norm scale
+    gamma [K] and one standard-normal draw per channel z [K] (f32)."""
+    if gamma.dtype != torch.bfloat16 or z.dtype != torch.float32 or gamma.dim() != 1 or z.shape != gamma.shape:
+        raise TypeError("gamma must be 1-D bfloat16 and z float32 of the same length")
+    if not (gamma.is_contiguous() and z.is_contiguous()):
+        raise ValueError("gamma and z must be contiguous")
+    rlq_aqn_perturb(gamma.data_ptr(), gamma.numel(), z.data_ptr(), sigma, _stream(stream))
+    return gamma
 
 
 def check(stream=None):

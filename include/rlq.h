@@ -210,6 +210,27 @@ rlq_status rlq_gemm_fprop_per_channel_splitk(const uint8_t *xq, int64_t ldxq, co
                                              void *workspace, int64_t workspace_bytes, rlq_stream_t stream);
 
 /*
+ * AQN, adaptive quantization noise (QeRL news article: channel-wise Gaussian
+ * perturbations mapped into the LayerNorm scale parameters, decaying on an
+ * exponential schedule).  The pages give no formula; the one used here:
+ *
+ *   rlq_aqn_sigma:   *sigma = sigma_start * (sigma_end / sigma_start)^(t / (T - 1))
+ *                    for step t of T (0 <= t < T): sigma_start at t = 0, sigma_end
+ *                    at t = T - 1, geometric in between (computed in double,
+ *                    rounded once to fp32).  T == 1 or equal levels give
+ *                    sigma_start.  Levels must be finite and >= 0, and > 0 for a
+ *                    decaying schedule.  Host-only: no stream, no GPU.
+ *   rlq_aqn_perturb: gamma[k] = bf16_RN(fl32(gamma[k] + fl32(sigma * z[k]))), in
+ *                    place, for k < K: gamma the norm scale (bf16 [K], 2-byte
+ *                    aligned device memory), z one standard-normal draw per
+ *                    channel (f32 [K] device memory, drawn by the caller), sigma
+ *                    finite.  The product and the sum round separately.
+ */
+rlq_status rlq_aqn_sigma(float sigma_start, float sigma_end, int64_t t, int64_t T, float *sigma);
+
+rlq_status rlq_aqn_perturb(uint16_t *gamma, int64_t K, const float *z, float sigma, rlq_stream_t stream);
+
+/*
  * Split-K forms of the three GEMMs, for outputs too small to occupy every SM
  * (decode-sized M in FProp and DGrad, a narrow layer's WGrad).  The pages'
  * GEMMs do not prescribe a tiling; this is a scheduling choice of this

@@ -152,3 +152,26 @@ def test_per_channel_splitk_validation():
     args = (FAKE, 128, FAKE, 4, FAKE, 128, FAKE, 128, FAKE, 128, 4, 128, 128)
     assert _status(g, *args, FAKE + 4, 1 << 20, None) == 3    # workspace not 16-byte aligned
     assert _status(g, *args, FAKE, -1, None) == 1             # negative workspace size
+
+
+def test_aqn_validation_and_host_schedule():
+    """AQN: host-side checks of the perturbation, and the host-only noise schedule
+    against the oracle's."""
+    import oracle
+    p = rlq.rlq_aqn_perturb
+    assert _status(p, FAKE, -1, FAKE, 0.1, None) == 1                 # negative K
+    assert _status(p, None, 8, FAKE, 0.1, None) == 1                  # NULL gamma
+    assert _status(p, FAKE + 1, 8, FAKE, 0.1, None) == 3              # gamma not 2-byte aligned
+    assert _status(p, FAKE, 8, FAKE + 2, 0.1, None) == 3              # z not 4-byte aligned
+    assert _status(p, FAKE, 8, FAKE, float("nan"), None) == 1         # sigma not finite
+    assert _status(p, None, 0, None, 0.1, None) == 0                  # empty: no-op
+    with pytest.raises(rlq.RlqError):
+        rlq.rlq_aqn_sigma(1e-2, 5e-4, 10, 10)                         # t outside 0 .. T-1
+    with pytest.raises(rlq.RlqError):
+        rlq.rlq_aqn_sigma(0.0, 5e-4, 1, 10)                           # decaying from zero
+    for s0, s1, T in ((1e-2, 5e-4, 11), (0.05, 1e-3, 100), (0.3, 0.3, 5), (0.02, 0.01, 1)):
+        for t in range(T):
+            a, b = rlq.rlq_aqn_sigma(s0, s1, t, T), oracle.aqn_sigma(s0, s1, t, T)
+            assert abs(a - b) <= 1e-6 * b
+        assert rlq.rlq_aqn_sigma(s0, s1, 0, T) == oracle.aqn_sigma(s0, s1, 0, T)
+        assert rlq.rlq_aqn_sigma(s0, s1, T - 1, T) == oracle.aqn_sigma(s0, s1, T - 1, T)
