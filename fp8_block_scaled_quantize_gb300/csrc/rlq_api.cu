@@ -388,6 +388,57 @@ rlq_status rlq_gemm_fprop_splitk(const uint8_t *xq, int64_t ldxq, const float *x
     return gemm_fprop(xq, ldxq, xs, ldxs, wq, ldwq, ws, ldws, y, ldy, M, N, K, workspace, workspace_bytes, stream);
 }
 
+rlq_status rlq_gemm_wgrad_accumulate(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, int64_t lddysc,
+                                     const uint8_t *xqT, int64_t ldxqT, const float *xsc, int64_t ldxsc, float *dw_acc,
+                                     int64_t ld_acc, int64_t M, int64_t N, int64_t K, void *workspace,
+                                     int64_t workspace_bytes, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
+    RLQ_REQUIRE(N % G == 0 && K % G == 0, RLQ_ERR_UNSUPPORTED, "N=%lld and K=%lld must be multiples of 128",
+                (long long)N, (long long)K);
+    RLQ_REQUIRE(M < MAX_DIM && N < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    if (N == 0 || K == 0 || M == 0)
+        return RLQ_OK;  // nothing to add
+    RLQ_REQUIRE(M > G, RLQ_ERR_UNSUPPORTED, "M=%lld: accumulation needs more than one 128-token block", (long long)M);
+    RLQ_REQUIRE(dw_acc, RLQ_ERR_INVALID_ARG, "dw_acc is NULL");
+    RLQ_REQUIRE(ld_acc >= K, RLQ_ERR_INVALID_ARG, "dw_acc: pitch %lld < %lld", (long long)ld_acc, (long long)K);
+    RLQ_REQUIRE(al(dw_acc, 16) && ld_acc % 4 == 0, RLQ_ERR_MISALIGNED,
+                "dw_acc rows must be 16-byte aligned (pointer 16-byte aligned, pitch a multiple of 4)");
+    RLQ_TRY(check_workspace(workspace, workspace_bytes));
+    RLQ_REQUIRE(workspace && workspace_bytes >= 2 * N * K * 4, RLQ_ERR_INVALID_ARG,
+                "workspace of %lld bytes: accumulation needs at least 2 * N * K * 4 = %lld", (long long)workspace_bytes,
+                (long long)(2 * N * K * 4));
+    RLQ_TRY(check_codes("dyqT", dyqT, lddyqT, M));
+    RLQ_TRY(check_codes("xqT", xqT, ldxqT, M));
+    RLQ_TRY(check_scales("dysc", dysc, lddysc, N));
+    RLQ_TRY(check_scales("xsc", xsc, ldxsc, K));
+    RLQ_REQUIRE(al(xsc, 16) && ldxsc % 4 == 0, RLQ_ERR_MISALIGNED,
+                "xsc rows must be 16-byte aligned (pointer 16-byte aligned, pitch a multiple of 4)");
+    GemmArgs a{};
+    a.A = dyqT;
+    a.lda = lddyqT;
+    a.B = xqT;
+    a.ldb = ldxqT;
+    a.sa = dysc;
+    a.ld_sa = lddysc;
+    a.sb = xsc;
+    a.sb_bstride = ldxsc;
+    a.sb_cstride = 0;
+    a.per_col_sb = true;
+    // the kernel writes only fp32 partials in split mode; its bf16 output map is
+    // laid over the workspace so that it describes valid memory, and never written
+    a.out = static_cast<uint16_t *>(workspace);
+    a.ldo = K;
+    a.R = N;
+    a.C = K;
+    a.L = M;
+    a.ws = static_cast<float *>(workspace);
+    a.ws_bytes = workspace_bytes;
+    a.acc = dw_acc;
+    a.ld_acc = ld_acc;
+    return launch_gemm(a, cs(stream));
+}
+
 rlq_status rlq_gemm_fprop_per_channel_splitk(const uint8_t *xq, int64_t ldxq, const float *xs_rep, int64_t ldxs,
                                              const uint8_t *wq, int64_t ldwq, const float *ws_rep, int64_t ldws,
                                              uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,

@@ -945,6 +945,28 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(const float *__restrict__
     }
 }
 
+// acc[r][c] += the split sums added in split order (fp32), for an fp32
+// gradient that accumulates several GEMMs (micro-batches).
+__global__ void __launch_bounds__(256) k_splitk_reduce_acc(const float *__restrict__ ws, int splits, int R, int C,
+                                                           float *__restrict__ acc, int64_t ld_acc)
+{
+    const int64_t per_row = C / 4;
+    const int64_t total = (int64_t)R * per_row;
+    const int64_t plane = (int64_t)R * C;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / per_row, c = (i - r * per_row) * 4;
+        float4 a = *reinterpret_cast<const float4 *>(ws + r * C + c);
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4 x = *reinterpret_cast<const float4 *>(ws + sp * plane + r * C + c);
+            a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+        }
+        float4 *d = reinterpret_cast<float4 *>(acc + r * ld_acc + c);
+        float4 v = *d;
+        v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+        *d = v;
+    }
+}
+
 // ---------------------------------------------------------------- host ---
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
@@ -1199,7 +1221,10 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
     int64_t rgrid = (total + 255) / 256;
     if (rgrid > (int64_t)di.sms * 8)
         rgrid = (int64_t)di.sms * 8;
-    k_splitk_reduce<<<(int)rgrid, 256, 0, st>>>(a.ws, p.splits, p.R, p.C, a.out, a.ldo);
+    if (a.acc)
+        k_splitk_reduce_acc<<<(int)rgrid, 256, 0, st>>>(a.ws, p.splits, p.R, p.C, a.acc, a.ld_acc);
+    else
+        k_splitk_reduce<<<(int)rgrid, 256, 0, st>>>(a.ws, p.splits, p.R, p.C, a.out, a.ldo);
     return cuda_status(cudaGetLastError(), "split-K reduction launch");
 }
 
@@ -1230,6 +1255,14 @@ rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st)
         const rlq_status rs = plan_splitk(a.R, a.C, a.L, a.ws_bytes, &splits, &bytes);
         if (rs != RLQ_OK)
             return rs;
+    }
+    if (a.acc) {
+        // the fp32 result comes from the split-K partials: at least two splits
+        // (the caller checked that two planes fit and that L spans two blocks)
+        if (a.ws == nullptr || a.ws_bytes < 2 * a.R * a.C * 4 || a.L <= BK)
+            return fail(RLQ_ERR_INVALID_ARG, "accumulate mode needs two workspace planes and L > 128");
+        if (splits < 2)
+            splits = 2;
     }
     // CTA pairs for tiles of 256 output rows; one CTA per 128 rows when the output
     // has fewer rows or the contraction is split

@@ -59,6 +59,10 @@ struct GemmArgs {
     // split-K workspace (16-byte aligned fp32), or NULL for the single-pass GEMM
     float *ws;
     int64_t ws_bytes;
+    // accumulate mode: acc[r * ld_acc + c] += the fp32 result (out is not written);
+    // needs ws with room for two planes and at least two contraction blocks
+    float *acc;
+    int64_t ld_acc;
 };
 rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st);
 

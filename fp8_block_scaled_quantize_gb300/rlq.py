@@ -38,6 +38,7 @@ _SIGS = {
     "rlq_gemm_fprop_per_channel": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
     "rlq_gemm_fprop_per_channel_splitk": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_uaq_fold": [_P, _I, _I, _I, _P, _P, _I, _I, _P],
+    "rlq_gemm_wgrad_accumulate": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_aqn_sigma": [ctypes.c_float, ctypes.c_float, _I, _I, ctypes.POINTER(ctypes.c_float)],
     "rlq_aqn_perturb": [_P, _I, _P, ctypes.c_float, _P],
     "rlq_check": [_P],
@@ -166,6 +167,12 @@ def rlq_gemm_fprop_per_channel_splitk(xq, ldxq, xs_rep, ldxs, wq, ldwq, ws_rep, 
                                       workspace_bytes, stream):
     return _call("rlq_gemm_fprop_per_channel_splitk", xq, ldxq, xs_rep, ldxs, wq, ldwq, ws_rep, ldws, y, ldy, M, N,
                  K, workspace, workspace_bytes, stream)
+
+
+def rlq_gemm_wgrad_accumulate(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw_acc, ld_acc, M, N, K,
+                              workspace, workspace_bytes, stream):
+    return _call("rlq_gemm_wgrad_accumulate", dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw_acc, ld_acc,
+                 M, N, K, workspace, workspace_bytes, stream)
 
 
 def rlq_aqn_sigma(sigma_start, sigma_end, t, T) -> float:
@@ -364,6 +371,23 @@ def gemm_wgrad(dyqT, dysc, xqT, xsc, out=None, stream=None, split_k: bool = Fals
     else:
         rlq_gemm_wgrad(*args, _stream(stream))
     return dw
+
+
+def gemm_wgrad_accumulate_(dw_acc: torch.Tensor, dyqT, dysc, xqT, xsc, workspace=None, stream=None):
+    """dw_acc [N, K] fp32 += dY^T X (the WGrad product, kept in fp32).  The
+    workspace (uint8 device tensor) defaults to the larger of two fp32 planes and
+    the library's split-K plan."""
+    if dw_acc.dtype != torch.float32:
+        raise TypeError("dw_acc must be float32")
+    N, M = dyqT.shape
+    K = xqT.shape[0]
+    if workspace is None:
+        nbytes = max(2 * N * K * 4, rlq_gemm_splitk_workspace_bytes(GEMM_WGRAD, M, N, K))
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dw_acc.device)
+    rlq_gemm_wgrad_accumulate(dyqT.data_ptr(), _ld(dyqT), dysc.data_ptr(), _ld(dysc), xqT.data_ptr(), _ld(xqT),
+                              xsc.data_ptr(), _ld(xsc), dw_acc.data_ptr(), _ld(dw_acc), M, N, K,
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    return dw_acc
 
 
 def uaq_fold_(w: torch.Tensor, s: torch.Tensor, prev: torch.Tensor | None = None, stream=None):

@@ -210,6 +210,31 @@ rlq_status rlq_gemm_fprop_per_channel_splitk(const uint8_t *xq, int64_t ldxq, co
                                              void *workspace, int64_t workspace_bytes, rlq_stream_t stream);
 
 /*
+ * WGrad accumulated into an fp32 gradient, for micro-batch accumulation (the
+ * pages' GEMMs write bf16; this keeps the sum over micro-batches in fp32):
+ *
+ *   dw_acc[n, k] += sum_mb dysc[mb, n] * xsc[mb, k] * sum_{m in mb} dy[m,n] x[m,k]
+ *
+ * with the operands of rlq_gemm_wgrad.  The product is formed as in the split-K
+ * WGrad (each split's sum in fp32, the splits added in split order) and then added
+ * to dw_acc in fp32; nothing is rounded to bf16.
+ *
+ *   dw_acc     f32 [N, K], pitch ld_acc >= K, 16-byte aligned rows (pointer
+ *              16-byte aligned, ld_acc % 4 == 0); read and written
+ *   workspace  device scratch, 16-byte aligned, at least 2 * N * K * 4 bytes
+ *              (more lets the library use its split-K plan); contents on entry
+ *              do not matter; not to be used by anything else until the call
+ *              has completed on `stream`
+ * M == 0 adds nothing.  M must exceed 128 (the fp32 result is assembled from at
+ * least two contraction splits), else RLQ_ERR_UNSUPPORTED.  N % 128 == 0,
+ * K % 128 == 0.
+ */
+rlq_status rlq_gemm_wgrad_accumulate(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, int64_t lddysc,
+                                     const uint8_t *xqT, int64_t ldxqT, const float *xsc, int64_t ldxsc,
+                                     float *dw_acc, int64_t ld_acc, int64_t M, int64_t N, int64_t K,
+                                     void *workspace, int64_t workspace_bytes, rlq_stream_t stream);
+
+/*
  * AQN, adaptive quantization noise (QeRL news article: channel-wise Gaussian
  * perturbations mapped into the LayerNorm scale parameters, decaying on an
  * exponential schedule).  The pages give no formula; the one used here:
