@@ -636,6 +636,16 @@ def run_sweep(args):
                      nbytes=gemm_bytes(M, K, N), flop=2.0 * M * N * K)
             emit(cfg, "gemm_wgrad", _time_ms(lambda: rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc, out=dw), flush),
                  nbytes=gemm_bytes(N, K, M), flop=2.0 * M * N * K)
+            if cfg.startswith("train_step_8b"):
+                # fp32 accumulation (micro-batches): the operands, two fp32 planes written
+                # and read, and the fp32 gradient read and written
+                acc = torch.zeros((N, K), dtype=torch.float32, device=dev)
+                wsa = torch.empty(max(2 * N * K * 4, rlq.rlq_gemm_splitk_workspace_bytes(rlq.GEMM_WGRAD, M, N, K)),
+                                  dtype=torch.uint8, device=dev)
+                emit(cfg, "gemm_wgrad_accumulate",
+                     _time_ms(lambda: rlq.gemm_wgrad_accumulate_(acc, qdyT, sdyc, qxT, sxc, workspace=wsa), flush),
+                     nbytes=gemm_bytes(N, K, M) - 2 * N * K + 16 * N * K + 8 * N * K, flop=2.0 * M * N * K)
+                del acc, wsa
             ws = _splitk_ws(rlq.GEMM_WGRAD, M, N, K)
             if ws is not None:
                 emit(cfg, "gemm_wgrad_splitk",
