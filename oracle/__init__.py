@@ -10,7 +10,8 @@ Contents
 --------
 * ``rlq_oracle.c`` (plain C, built on first use with gcc): E4M3 encode/decode,
   the 1x128 / 128x1 / 128x128 group quantizers, the per-row (per-token /
-  per-channel) quantizer, the UAQ fold and the AQN perturbation.  These are bit-level definitions;
+  per-channel) quantizer, the UAQ fold, the AQN perturbation and the NVFP4
+  weight quantizer (E2M1 codes, E4M3 block scales, fp32 tensor scale).  These are bit-level definitions;
   the GPU must reproduce their bytes exactly.
 * This module: a ctypes binding for the C part and the fp64 GEMMs over
   dequantized operands (NumPy): the block-scaled FProp, DGrad and WGrad, and
@@ -93,6 +94,11 @@ def lib() -> ctypes.CDLL:
             L.orc_quant_cols_128x1.argtypes = [_P, _I, _I, _I, _P, _I, _P, _I]
             L.orc_quant_weight_128x128.argtypes = [_P, _I, _I, _I, _P, _I, _P, _I, _P, _I]
             L.orc_quant_per_row.argtypes = [_P, _I, _I, _I, _P, _I, _P]
+            L.orc_e2m1_decode.restype = ctypes.c_double
+            L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+            L.orc_e2m1_encode.restype = ctypes.c_uint8
+            L.orc_e2m1_encode.argtypes = [ctypes.c_float]
+            L.orc_quant_nvfp4.argtypes = [_P, _I, _I, _I, _P, _I, _P, _I, _P]
             L.orc_aqn_sigma.restype = ctypes.c_float
             L.orc_aqn_sigma.argtypes = [ctypes.c_float, ctypes.c_float, _I, _I]
             L.orc_aqn_perturb.argtypes = [_P, _I, _P, ctypes.c_float]
@@ -266,6 +272,44 @@ def uaq_fold(w, s, prev=None):
     lib().orc_uaq_fold(_ptr(w), N, K, K, _ptr(s),
                        _ptr(prev) if prev is not None else None, R, K)
     return w, prev
+
+
+NVFP4_BLOCK = 16
+
+
+def e2m1_decode(code: int) -> float:
+    """Value of a 4-bit E2M1 code (the NVFP4 element format)."""
+    return float(lib().orc_e2m1_decode(int(code) & 0xF))
+
+
+def e2m1_encode(v: float) -> int:
+    """RN-even, saturating (+-6) fp32 -> E2M1 code; the sign of zero is kept."""
+    return int(lib().orc_e2m1_encode(float(v)))
+
+
+def quant_nvfp4(w):
+    """NVFP4 weight quantization (QeRL news article: 4-bit floats with two-level
+    scaling, FP8 E4M3 block scales and an FP32 tensor scale).  w: bf16 bits [N,K],
+    K % 16 == 0.  Returns (q u8 [N,K] one E2M1 code per byte, sb u8 [N, K/16]
+    E4M3 block-scale codes, st fp32 tensor scale); x ~= e2m1(q) * e4m3(sb) * st.
+    """
+    w = _bf16_2d(w)
+    N, K = w.shape
+    if K % NVFP4_BLOCK:
+        raise ValueError("K must be a multiple of 16")
+    q = np.empty((N, K), np.uint8)
+    sb = np.empty((N, K // NVFP4_BLOCK), np.uint8)
+    st = np.empty((1,), np.float32)
+    lib().orc_quant_nvfp4(_ptr(w), N, K, K, _ptr(q), K, _ptr(sb), K // NVFP4_BLOCK, _ptr(st))
+    return q, sb, float(st[0])
+
+
+def dequant_nvfp4(q, sb, st) -> np.ndarray:
+    """fp64 values of NVFP4 codes: e2m1(q) * e4m3(sb) (per 16-block) * st."""
+    lut4 = np.array([e2m1_decode(c) for c in range(16)])
+    v = lut4[np.asarray(q) & 0xF]
+    s = dequant_codes(np.asarray(sb)).repeat(NVFP4_BLOCK, axis=1)
+    return v * s * float(st)
 
 
 def aqn_sigma(sigma_start: float, sigma_end: float, t: int, T: int) -> float:

@@ -25,6 +25,9 @@
  *    "损失函数 / 训练策略": channel-wise weight and token-wise activation
  *    quantization, FP8 here): one group per row over all K columns, the same
  *    scale rule and encoding.
+ *  - NVFP4 weight quantization (QeRL news article: FP4 with two-level scaling,
+ *    E4M3 block scales and an FP32 tensor scale): E2M1 codes, blocks of 16
+ *    along K, tensor scale amax / (6 * 448).
  *  - AQN (QeRL news article): channel-wise Gaussian noise added to a norm
  *    scale, gamma'[k] = bf16_RN(gamma[k] + sigma_t z[k]), sigma_t decaying
  *    geometrically from sigma_start to sigma_end; z is drawn by the caller.
@@ -236,6 +239,78 @@ void orc_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t l
                     if (qT)
                         qT[k * ldqT + n] = c;
                 }
+        }
+    }
+}
+
+/* --------------------------------------------------------------- NVFP4 --- */
+
+/* FP4 E2M1 (the element format of NVFP4; QeRL news article: NVFP4 is a 4-bit
+ * float with two-level scaling, FP8 E4M3 block scales and an FP32 tensor scale).
+ * Code: sign = bit 3, e = bits 2..1, m = bit 0; e = 0 gives +-m/2, otherwise
+ * +-(1 + m/2) 2^(e-1): the magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double orc_e2m1_decode(uint8_t c)
+{
+    int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = (e == 0) ? 0.5 * m : (1.0 + 0.5 * m) * ldexp(1.0, e - 1);
+    return sign ? -v : v;
+}
+
+/* Round-to-nearest-even onto the E2M1 grid with saturation to +-6; the sign of
+ * zero is kept.  Ties go to the code with an even mantissa bit. */
+uint8_t orc_e2m1_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 8 : 0;
+    double a = fabs((double)v);
+    if (isnan(v))
+        return sign | 7;  /* out of contract: saturate */
+    if (a >= 6.0)
+        return sign | 7;
+    uint8_t best = 0;
+    for (uint8_t c = 1; c < 8; ++c) {
+        double d = fabs(orc_e2m1_decode(c) - a), db = fabs(orc_e2m1_decode(best) - a);
+        if (d < db || (d == db && (c & 1) == 0))
+            best = c;
+    }
+    return sign | best;
+}
+
+/* NVFP4 quantization of a weight matrix w bf16 [N,K] (K % 16 == 0), two-level:
+ *   tensor scale  st = fl32(amax(w) / (6 * 448)), or 1 when w is all zero;
+ *   block of 16 consecutive elements along K: sb = E4M3_RNsat(fl32(fl32(amax_b / 6) / st)),
+ *   effective block scale S = fl32(decode(sb) * st);
+ *   element code q = E2M1_RNsat(fl32(x / S)), or +-0 when S == 0.
+ * Outputs: q one code per byte (low nibble) [N,K] (pitch ldq), sb E4M3 codes
+ * [N, K/16] (pitch ldsb), *st. */
+void orc_quant_nvfp4(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+                     uint8_t *sb, int64_t ldsb, float *st)
+{
+    float amax = 0.0f;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(bf16_bits_to_f32(w[n * ldw + k]));
+            if (a > amax)
+                amax = a;
+        }
+    float t = (amax == 0.0f) ? 1.0f : amax / (6.0f * 448.0f);
+    *st = t;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t kb = 0; kb < K / 16; ++kb) {
+            const uint16_t *g = w + n * ldw + kb * 16;
+            float ab = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                float a = fabsf(bf16_bits_to_f32(g[i]));
+                if (a > ab)
+                    ab = a;
+            }
+            uint8_t e = orc_e4m3_encode((ab / 6.0f) / t);
+            sb[n * ldsb + kb] = e;
+            float S = (float)orc_e4m3_decode(e) * t;
+            for (int i = 0; i < 16; ++i) {
+                float x = bf16_bits_to_f32(g[i]);
+                q[n * ldq + kb * 16 + i] = (S == 0.0f) ? (signbit(x) ? 8 : 0) : orc_e2m1_encode(x / S);
+            }
         }
     }
 }
