@@ -133,6 +133,25 @@ rlq_status rlq_quant_per_row(const uint16_t *x, int64_t M, int64_t K, int64_t ld
                        "per-row quantizer launch");
 }
 
+rlq_status rlq_quant_nvfp4(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq, uint8_t *sb,
+                           int64_t ldsb, float *st, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size (N=%lld, K=%lld)", (long long)N, (long long)K);
+    RLQ_REQUIRE(K % 16 == 0, RLQ_ERR_UNSUPPORTED, "K=%lld is not a multiple of 16", (long long)K);
+    RLQ_REQUIRE(N < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    RLQ_REQUIRE(st, RLQ_ERR_INVALID_ARG, "st is NULL");
+    RLQ_REQUIRE(al(st, 4), RLQ_ERR_MISALIGNED, "st is not 4-byte aligned");
+    if (N == 0 || K == 0)
+        return RLQ_OK;
+    RLQ_TRY(check_bf16("w", w, ldw, K));
+    RLQ_REQUIRE(q, RLQ_ERR_INVALID_ARG, "q is NULL");
+    RLQ_REQUIRE(ldq >= K / 2, RLQ_ERR_INVALID_ARG, "q: pitch %lld < %lld bytes", (long long)ldq, (long long)(K / 2));
+    RLQ_REQUIRE(al(q, 8) && ldq % 8 == 0, RLQ_ERR_MISALIGNED, "q rows must be 8-byte aligned");
+    RLQ_REQUIRE(sb, RLQ_ERR_INVALID_ARG, "sb is NULL");
+    RLQ_REQUIRE(ldsb >= K / 16, RLQ_ERR_INVALID_ARG, "sb: pitch %lld < %lld", (long long)ldsb, (long long)(K / 16));
+    return cuda_status(launch_quant_nvfp4(w, N, K, ldw, q, ldq, sb, ldsb, st, cs(stream)), "NVFP4 quantizer launch");
+}
+
 rlq_status rlq_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
                                     float *s, int64_t lds, uint8_t *qT, int64_t ldqT, rlq_stream_t stream)
 {

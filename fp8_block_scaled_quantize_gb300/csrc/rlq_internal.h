@@ -28,6 +28,8 @@ cudaError_t launch_quant_weight(const uint16_t *w, int64_t N, int64_t K, int64_t
                                 cudaStream_t st);
 cudaError_t launch_quant_per_row(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
                                  int64_t ldq, float *s, float *s_rep, int64_t ld_rep, cudaStream_t st);
+cudaError_t launch_quant_nvfp4(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+                               uint8_t *sb, int64_t ldsb, float *st, cudaStream_t st_stream);
 cudaError_t launch_aqn_perturb(uint16_t *gamma, int64_t K, const float *z, float sigma, cudaStream_t st);
 cudaError_t launch_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, const float *s,
                             uint16_t *prev, int64_t R, int64_t ldp, cudaStream_t st);

@@ -623,6 +623,91 @@ __global__ void __launch_bounds__(256) k_quant_per_row(const uint16_t *__restric
 }
 
 // ---------------------------------------------------------------------------
+// NVFP4 weight quantization (QeRL news article: 4-bit floats with two-level
+// scaling, FP8 E4M3 block scales and an FP32 tensor scale).  E2M1 elements, blocks
+// of 16 consecutive elements along K, tensor scale st = amax / (6 * 448):
+//   block code  sb = E4M3_RNsat(fl32(fl32(amax_b / 6) / st)),
+//   element     q  = E2M1_RNsat(fl32(x / fl32(decode(sb) * st))), +-0 when that is 0.
+// Three launches: the tensor amax (packed maxima, one atomic max per warp, the
+// bits of a non-negative float ordering as unsigned integers), the block pass
+// (one thread per block), and one thread that turns the amax into st.
+
+// E2M1 code of r: RN-even onto 0, 0.5, 1, 1.5, 2, 3, 4, 6 with saturation; each
+// threshold is a midpoint, strict where the tie goes down to the even code.
+__device__ __forceinline__ uint32_t e2m1_code(float r)
+{
+    const float a = fabsf(r);
+    const uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+                       (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
+    return c | (signbit(r) ? 8u : 0u);
+}
+
+// Exact fp32 value of a finite E4M3 code.
+__device__ __forceinline__ float e4m3_value(uint32_t e)
+{
+    const uint32_t ex = (e >> 3) & 15u, m = e & 7u;
+    const float v = ex == 0 ? (float)m * 0x1p-9f : __uint_as_float(((ex + 120u) << 23) | (m << 20));
+    return (e & 0x80u) ? -v : v;
+}
+
+__global__ void __launch_bounds__(256) k_nvfp4_amax(const uint16_t *__restrict__ w, int64_t N, int64_t K, int64_t ldw,
+                                                    unsigned int *__restrict__ amax_bits)
+{
+    const int64_t K8 = K / 8, total = N * K8;
+    uint32_t pm = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / K8, k = (i - n * K8) * 8;
+        const uint4 v = ld_stream(w + n * ldw + k);
+        pm = bmaxabs2(pm, bmaxabs2(bmaxabs2(v.x, v.y), bmaxabs2(v.z, v.w)));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        pm = bmaxabs2(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, o));
+    if ((threadIdx.x & 31) == 0)
+        atomicMax(amax_bits, __float_as_uint(bmax_final(babs2(pm))));
+}
+
+__global__ void __launch_bounds__(256) k_nvfp4_quant(const uint16_t *__restrict__ w, int64_t N, int64_t K,
+                                                     int64_t ldw, uint8_t *__restrict__ q, int64_t ldq,
+                                                     uint8_t *__restrict__ sb, int64_t ldsb,
+                                                     const unsigned int *__restrict__ amax_bits)
+{
+    const float amax = __uint_as_float(*amax_bits);
+    const float st = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);  // 6 * 448
+    const int64_t KB = K / 16, total = N * KB;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / KB, kb = i - n * KB;
+        const uint16_t *src = w + n * ldw + kb * 16;
+        float f[16];
+        float lo8[8], hi8[8];
+        unpack8(ld_stream(src), lo8);
+        unpack8(ld_stream(src + 8), hi8);
+        float ab = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            f[j] = lo8[j], f[j + 8] = hi8[j];
+            ab = fmaxf(ab, fmaxf(fabsf(lo8[j]), fabsf(hi8[j])));
+        }
+        const uint32_t e = e4m3x2(__fdiv_rn(__fdiv_rn(ab, 6.0f), st), 0.0f) & 0xFFu;
+        sb[n * ldsb + kb] = (uint8_t)e;
+        const float S = __fmul_rn(e4m3_value(e), st);
+        uint32_t word[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint32_t c = S == 0.0f ? (signbit(f[j]) ? 8u : 0u) : e2m1_code(__fdiv_rn(f[j], S));
+            word[j >> 3] |= c << (4 * (j & 7));
+        }
+        *reinterpret_cast<uint2 *>(q + n * ldq + kb * 8) = make_uint2(word[0], word[1]);
+    }
+}
+
+__global__ void k_nvfp4_tensor_scale(float *st)
+{
+    const float amax = *st;  // the amax pass left its bits here
+    *st = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+}
+
+// ---------------------------------------------------------------------------
 // AQN (QeRL news article: channel-wise Gaussian noise in the LayerNorm scale):
 // gamma[k] = bf16_RN(fl32(gamma[k] + fl32(sigma * z[k]))), in place.  The product
 // and the sum are rounded separately (no contraction into an FMA).
@@ -737,6 +822,24 @@ cudaError_t launch_quant_per_row(const uint16_t *x, int64_t M, int64_t K, int64_
     } else {  // few, long rows: a CTA per row
         k_quant_per_row<256><<<(unsigned)M, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_nvfp4(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+                               uint8_t *sb, int64_t ldsb, float *st, cudaStream_t st_stream)
+{
+    cudaError_t e = cudaMemsetAsync(st, 0, sizeof(float), st_stream);
+    if (e != cudaSuccess)
+        return e;
+    unsigned int *amax_bits = reinterpret_cast<unsigned int *>(st);
+    const int64_t cap = (int64_t)sm_count() * 8;
+    int64_t g1 = (N * (K / 8) + 255) / 256;
+    g1 = g1 > cap ? cap : (g1 < 1 ? 1 : g1);
+    k_nvfp4_amax<<<(unsigned)g1, 256, 0, st_stream>>>(w, N, K, ldw, amax_bits);
+    int64_t g2 = (N * (K / 16) + 255) / 256;
+    g2 = g2 > cap * 4 ? cap * 4 : (g2 < 1 ? 1 : g2);
+    k_nvfp4_quant<<<(unsigned)g2, 256, 0, st_stream>>>(w, N, K, ldw, q, ldq, sb, ldsb, amax_bits);
+    k_nvfp4_tensor_scale<<<1, 1, 0, st_stream>>>(st);
     return cudaGetLastError();
 }
 

@@ -39,6 +39,7 @@ _SIGS = {
     "rlq_gemm_fprop_per_channel_splitk": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_uaq_fold": [_P, _I, _I, _I, _P, _P, _I, _I, _P],
     "rlq_gemm_wgrad_accumulate": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
+    "rlq_quant_nvfp4": [_P, _I, _I, _I, _P, _I, _P, _I, _P, _P],
     "rlq_aqn_sigma": [ctypes.c_float, ctypes.c_float, _I, _I, ctypes.POINTER(ctypes.c_float)],
     "rlq_aqn_perturb": [_P, _I, _P, ctypes.c_float, _P],
     "rlq_check": [_P],
@@ -173,6 +174,10 @@ def rlq_gemm_wgrad_accumulate(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc
                               workspace, workspace_bytes, stream):
     return _call("rlq_gemm_wgrad_accumulate", dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw_acc, ld_acc,
                  M, N, K, workspace, workspace_bytes, stream)
+
+
+def rlq_quant_nvfp4(w, N, K, ldw, q, ldq, sb, ldsb, st, stream):
+    return _call("rlq_quant_nvfp4", w, N, K, ldw, q, ldq, sb, ldsb, st, stream)
 
 
 def rlq_aqn_sigma(sigma_start, sigma_end, t, T) -> float:
@@ -397,6 +402,24 @@ def uaq_fold_(w: torch.Tensor, s: torch.Tensor, prev: torch.Tensor | None = None
     rlq_uaq_fold(w.data_ptr(), N, K, _ld(w), s.data_ptr(), _ptr(prev), R, _ld(prev) if prev is not None else 0,
                  _stream(stream))
     return w, prev
+
+
+def quant_nvfp4(w: torch.Tensor, stream=None):
+    """NVFP4 quantization of bf16 w [N, K] (K % 16 == 0).
+
+    Returns (q [N, K/2] u8 packed E2M1 codes, low nibble first; sb [N, K/16] u8
+    E4M3 block-scale codes; st [1] f32 tensor scale)."""
+    if w.dtype != torch.bfloat16:
+        raise TypeError("w must be bfloat16")
+    N, K = w.shape
+    dev = w.device
+    kq = _round_up(max(K // 2, 1), 8)
+    q = torch.empty((N, kq), dtype=torch.uint8, device=dev)[:, :K // 2]
+    sb = torch.empty((N, max(K // 16, 1)), dtype=torch.uint8, device=dev)[:, :K // 16]
+    st = torch.empty((1,), dtype=torch.float32, device=dev)
+    rlq_quant_nvfp4(w.data_ptr(), N, K, _ld(w), q.data_ptr(), kq, sb.data_ptr(), max(K // 16, 1), st.data_ptr(),
+                    _stream(stream))
+    return q, sb, st
 
 
 def aqn_perturb_(gamma: torch.Tensor, z: torch.Tensor, sigma: float, stream=None):

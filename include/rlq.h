@@ -235,6 +235,30 @@ rlq_status rlq_gemm_wgrad_accumulate(const uint8_t *dyqT, int64_t lddyqT, const 
                                      void *workspace, int64_t workspace_bytes, rlq_stream_t stream);
 
 /*
+ * NVFP4 weight quantization (QeRL news article: a hardware 4-bit float with
+ * two-level scaling, FP8 E4M3 block scales and an FP32 tensor scale, used for
+ * the policy weights).  The pages fix neither the block size nor the scale rule;
+ * this call uses E2M1 elements, blocks of 16 consecutive elements along K and
+ *
+ *   st = fl32(amax(w) / (6 * 448)), or 1 for an all-zero w
+ *   sb[n, kb] = E4M3_RNsat(fl32(fl32(amax of the block / 6) / st))
+ *   q = E2M1_RNsat(fl32(x / fl32(decode(sb) * st)))  (+-0 when that scale is 0)
+ *
+ * so that x ~= e2m1(q) * e4m3(sb) * st.  E2M1 rounding is to nearest, ties to
+ * the even code, saturating at +-6; the sign of zero is kept.
+ *
+ *   w   bf16 [N, K], pitch ldw >= K (elements, a multiple of 8)
+ *   q   packed E2M1 codes, two per byte: byte b of row n holds element 2b in its
+ *       low nibble and 2b + 1 in its high nibble; pitch ldq >= K/2 bytes, rows
+ *       8-byte aligned (ldq % 8 == 0)
+ *   sb  E4M3 block-scale codes [N, K/16], pitch ldsb >= K/16 bytes
+ *   st  one fp32 in device memory (written; used as scratch during the call)
+ * K % 16 == 0; N any value >= 0.
+ */
+rlq_status rlq_quant_nvfp4(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+                           uint8_t *sb, int64_t ldsb, float *st, rlq_stream_t stream);
+
+/*
  * AQN, adaptive quantization noise (QeRL news article: channel-wise Gaussian
  * perturbations mapped into the LayerNorm scale parameters, decaying on an
  * exponential schedule).  The pages give no formula; the one used here:

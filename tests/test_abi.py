@@ -186,3 +186,13 @@ def test_wgrad_accumulate_validation():
     assert _status(g, *ok[:8], FAKE + 4, *ok[9:]) == 3              # dw_acc not 16-byte aligned
     assert _status(g, *ok[:9], 126, *ok[10:]) == 1                  # ld_acc < K
     assert _status(g, *ok[:10], 0, *ok[11:]) == 0                   # M = 0: nothing to add
+
+
+def test_nvfp4_validation():
+    f = rlq.rlq_quant_nvfp4
+    assert _status(f, FAKE, 4, 24, 24, FAKE, 16, FAKE, 2, FAKE, None) == 2      # K % 16
+    assert _status(f, FAKE, 4, 32, 32, FAKE, 16, FAKE, 2, None, None) == 1      # NULL st
+    assert _status(f, FAKE, 4, 32, 32, FAKE, 12, FAKE, 2, FAKE, None) == 1      # ldq < K/2
+    assert _status(f, FAKE, 4, 32, 32, FAKE + 4, 16, FAKE, 2, FAKE, None) == 3  # q rows not 8-byte aligned
+    assert _status(f, FAKE, 4, 32, 32, FAKE, 16, FAKE, 1, FAKE, None) == 1      # ldsb < K/16
+    assert _status(f, FAKE, 0, 32, 32, None, 0, None, 0, FAKE, None) == 0       # empty: no-op

@@ -1,0 +1,70 @@
+"""GPU parity of the NVFP4 weight quantizer (QeRL news article: 4-bit floats,
+E4M3 block scales, FP32 tensor scale) through the C ABI: element codes, block
+codes and the tensor scale bit-exact against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_block_scaled_quantize_gb300 import inputs as I
+from fp8_block_scaled_quantize_gb300 import rlq
+from gpu_util import normal_bits, np_, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _unpack(qp: np.ndarray) -> np.ndarray:
+    lo, hi = qp & 0xF, qp >> 4
+    return np.stack([lo, hi], axis=-1).reshape(qp.shape[0], -1)
+
+
+def _check(w_bits, q, sb, st):
+    oq, osb, ost = oracle.quant_nvfp4(w_bits)
+    assert np_(st)[0] == np.float32(ost), "tensor scale differs"
+    assert np.array_equal(np_(sb), osb), "block scales differ"
+    assert np.array_equal(_unpack(np_(q)), oq), "element codes differ"
+
+
+@pytest.mark.parametrize("N,K,std", [(1, 16, 1.0), (7, 48, 0.02), (128, 512, 3e-3), (14336, 4096, 0.02)])
+def test_nvfp4_parity(N, K, std):
+    w = normal_bits(70, (N, K), std=std)
+    q, sb, st = rlq.quant_nvfp4(to_dev(w))
+    rlq.check()
+    _check(w, q, sb, st)
+
+
+def test_nvfp4_edge_blocks():
+    """Blocks 2^-40 .. 2^20 apart (the smallest flush to zero), all-zero and
+    signed-zero blocks, exact E2M1 midpoints, and the zero tensor."""
+    rng = np.random.default_rng(71)
+    N, K = 64, 256
+    v = rng.standard_normal((N, K)).astype(np.float32)
+    v *= np.exp2(rng.integers(-40, 21, size=(N, K // 16))).repeat(16, axis=1).astype(np.float32)
+    v[0, :16] = 0.0
+    v[0, 16:32] = -0.0
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0], np.float32)
+    v[1, :16] = np.concatenate([mids, -mids])  # block amax 6: block scale 1 * st when st makes it exact
+    w = I.to_bf16_bits(v)
+    q, sb, st = rlq.quant_nvfp4(to_dev(w))
+    rlq.check()
+    _check(w, q, sb, st)
+    z = np.zeros((16, 64), np.uint16)
+    qz, sbz, stz = rlq.quant_nvfp4(to_dev(z))
+    rlq.check()
+    _check(z, qz, sbz, stz)
+
+
+def test_nvfp4_pitched():
+    N, K = 40, 96
+    w = normal_bits(72, (N, K), std=0.5)
+    dev = "cuda"
+    wb = torch.zeros((N, K + 8), dtype=torch.bfloat16, device=dev)
+    wb[:, :K] = to_dev(w)
+    qb = torch.full((N, K // 2 + 16), 0xA5, dtype=torch.uint8, device=dev)
+    sbb = torch.full((N, K // 16 + 3), 0x5A, dtype=torch.uint8, device=dev)
+    st = torch.empty(1, dtype=torch.float32, device=dev)
+    rlq.rlq_quant_nvfp4(wb.data_ptr(), N, K, K + 8, qb.data_ptr(), K // 2 + 16, sbb.data_ptr(), K // 16 + 3,
+                        st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    rlq.check()
+    _check(w, qb[:, :K // 2], sbb[:, :K // 16], st)
+    assert torch.all(qb[:, K // 2:] == 0xA5) and torch.all(sbb[:, K // 16:] == 0x5A)
