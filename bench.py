@@ -609,6 +609,8 @@ def run_sweep(args):
                  nbytes=3 * M * K + 4 * M * (1 + K // 128))
             emit(cfg, "quant_per_row_w", _time_ms(lambda: rlq.quant_per_row(w), flush),
                  nbytes=3 * N * K + 4 * N * (1 + K // 128))
+            # NVFP4 weights: read 2, write 0.5 (codes) + 1/16 (block scales) bytes per element
+            emit(cfg, "quant_nvfp4_w", _time_ms(lambda: rlq.quant_nvfp4(w), flush), nbytes=2.5625 * N * K)
             pqx, _, psx = rlq.quant_per_row(x)
             pqw, _, psw = rlq.quant_per_row(w)
             emit(cfg, "gemm_fprop_per_channel",
@@ -637,6 +639,7 @@ def run_sweep(args):
             emit(cfg, "gemm_wgrad", _time_ms(lambda: rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc, out=dw), flush),
                  nbytes=gemm_bytes(N, K, M), flop=2.0 * M * N * K)
             if cfg.startswith("train_step_8b"):
+                emit(cfg, "quant_nvfp4_w", _time_ms(lambda: rlq.quant_nvfp4(w), flush), nbytes=2.5625 * N * K)
                 # fp32 accumulation (micro-batches): the operands, two fp32 planes written
                 # and read, and the fp32 gradient read and written
                 acc = torch.zeros((N, K), dtype=torch.float32, device=dev)
