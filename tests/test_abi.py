@@ -196,3 +196,11 @@ def test_nvfp4_validation():
     assert _status(f, FAKE, 4, 32, 32, FAKE + 4, 16, FAKE, 2, FAKE, None) == 3  # q rows not 8-byte aligned
     assert _status(f, FAKE, 4, 32, 32, FAKE, 16, FAKE, 1, FAKE, None) == 1      # ldsb < K/16
     assert _status(f, FAKE, 0, 32, 32, None, 0, None, 0, FAKE, None) == 0       # empty: no-op
+
+
+def test_binding_covers_every_declared_function():
+    """Every entry point of include/rlq.h has a ctypes signature in the binding
+    (the string-returning ones are typed when the library loads)."""
+    typed_at_load = {"rlq_status_string", "rlq_last_error", "rlq_version"}
+    missing = [n for n in declared_functions() if n not in rlq._SIGS and n not in typed_at_load]
+    assert not missing, f"no ctypes signature for {missing}"
