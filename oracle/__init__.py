@@ -312,6 +312,21 @@ def dequant_nvfp4(q, sb, st) -> np.ndarray:
     return v * s * float(st)
 
 
+def gemm_nvfp4_weight_only(x, q, sb, st, rows=None, cols=None) -> np.ndarray:
+    """Y = X W^T with bf16 activations and NVFP4 weights (QeRL news article: the
+    rollout runs FP4 x BF16 kernels): W[n, k] = e2m1(q[n, k]) * e4m3(sb[n, k/16]) * st.
+    x: bf16 bits [M, K]; q: one E2M1 code per byte [N, K] (as ``quant_nvfp4``
+    returns); sb [N, K/16]; st fp32.  fp64: the bf16 values, the E2M1 x E4M3
+    products and their K-term sums are exact for moderate K, then one scaling by st.
+    """
+    xr = bf16_to_f32(np.asarray(x))
+    rows = np.arange(xr.shape[0]) if rows is None else np.asarray(rows)
+    cols = np.arange(np.asarray(q).shape[0]) if cols is None else np.asarray(cols)
+    lut4 = np.array([e2m1_decode(c) for c in range(16)])
+    wq = lut4[np.asarray(q)[cols] & 0xF] * dequant_codes(np.asarray(sb)[cols]).repeat(NVFP4_BLOCK, axis=1)
+    return (xr[rows].astype(np.float64) @ wq.T) * float(st)
+
+
 def aqn_sigma(sigma_start: float, sigma_end: float, t: int, T: int) -> float:
     """Noise level of AQN step t of T: geometric from sigma_start (t = 0) to
     sigma_end (t = T - 1), as an fp32 value.  QeRL news article: adaptive

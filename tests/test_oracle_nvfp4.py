@@ -108,3 +108,46 @@ def test_nvfp4_scale_covariance_and_zero():
         assert np.array_equal(q2, q) and np.array_equal(sb2, sb) and st2 == np.float32(st * 2.0 ** j)
     qz, sbz, stz = oracle.quant_nvfp4(np.zeros((4, 32), np.uint16))
     assert stz == 1.0 and np.all(qz == 0) and np.all(sbz == 0)
+
+
+def _frac_e2m1(c):
+    from fractions import Fraction
+    v = Fraction(E2M1[c & 7]).limit_denominator(2)
+    return -v if c & 8 else v
+
+
+def test_weight_only_gemm_exact_rationals():
+    """Tiny shapes in exact rationals: sum_k x[m,k] * e2m1(q) * e4m3(sb), times st."""
+    from fractions import Fraction
+    rng = np.random.default_rng(8)
+    M, N, K = 3, 4, 48
+    x = oracle.f32_to_bf16(rng.standard_normal((M, K)).astype(np.float32))
+    w = oracle.f32_to_bf16((rng.standard_normal((N, K)) * 0.3).astype(np.float32))
+    q, sb, st = oracle.quant_nvfp4(w)
+    y = oracle.gemm_nvfp4_weight_only(x, q, sb, st)
+    xf = oracle.bf16_to_f32(x)
+    lut = oracle.e4m3_lut()
+    for m in range(M):
+        for n in range(N):
+            acc = sum((Fraction(float(xf[m, k])) * _frac_e2m1(int(q[n, k])) * Fraction(float(lut[sb[n, k // 16]]))
+                       for k in range(K)), Fraction(0))
+            exact = acc * Fraction(st)
+            assert abs(Fraction(float(y[m, n])) - exact) <= abs(exact) * Fraction(1, 2 ** 51) + Fraction(1, 2 ** 1074)
+
+
+def test_weight_only_gemm_matches_dequantized_weight_and_integer_case():
+    rng = np.random.default_rng(9)
+    x = oracle.f32_to_bf16(rng.standard_normal((20, 64)).astype(np.float32))
+    w = oracle.f32_to_bf16((rng.standard_normal((12, 64)) * 0.1).astype(np.float32))
+    q, sb, st = oracle.quant_nvfp4(w)
+    y = oracle.gemm_nvfp4_weight_only(x, q, sb, st)
+    ref = oracle.bf16_to_f32(x).astype(np.float64) @ oracle.dequant_nvfp4(q, sb, st).T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-300)
+    # integers: x in {-2..2}, every block scale 1 and st 1 -> exact integer products
+    xi = rng.integers(-2, 3, size=(5, 32)).astype(np.float32)
+    qi = rng.integers(0, 16, size=(6, 32)).astype(np.uint8)
+    sbi = np.full((6, 2), 0x38, np.uint8)  # E4M3 code of 1.0
+    yi = oracle.gemm_nvfp4_weight_only(oracle.f32_to_bf16(xi), qi, sbi, 1.0)
+    lut4 = np.array([oracle.e2m1_decode(c) for c in range(16)])
+    assert np.array_equal(yi, xi.astype(np.float64) @ lut4[qi].T)
+    assert oracle.dequant_codes(np.array([0x38], np.uint8))[0] == 1.0
