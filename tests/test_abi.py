@@ -1,7 +1,6 @@
 """CPU-side checks of the C ABI: the library builds, loads and exports every
 entry point that include/rlq.h declares, and host-side validation returns the
 documented status codes before anything is launched (no GPU needed)."""
-import ctypes
 import os
 import re
 

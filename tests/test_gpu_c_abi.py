@@ -10,7 +10,6 @@ import numpy as np
 import pytest
 import torch
 
-from fp8_block_scaled_quantize_gb300 import build as B
 from fp8_block_scaled_quantize_gb300 import rlq
 
 pytestmark = pytest.mark.gpu
