@@ -10,7 +10,8 @@ Contents
 --------
 * ``rlq_oracle.c`` (plain C, built on first use with gcc): E4M3 encode/decode,
   the 1x128 / 128x1 / 128x128 group quantizers, the per-row (per-token /
-  per-channel) quantizer, the UAQ fold, the AQN perturbation and the NVFP4
+  per-channel) quantizer, the UAQ fold, the RMSNorm whose weight carries the
+  folded UAQ scale, the AQN perturbation and the NVFP4
   weight quantizer (E2M1 codes, E4M3 block scales, fp32 tensor scale).  These are bit-level definitions;
   the GPU must reproduce their bytes exactly.
 * This module: a ctypes binding for the C part and the fp64 GEMMs over
@@ -103,6 +104,7 @@ def lib() -> ctypes.CDLL:
             L.orc_aqn_sigma.argtypes = [ctypes.c_float, ctypes.c_float, _I, _I]
             L.orc_aqn_perturb.argtypes = [_P, _I, _P, ctypes.c_float]
             L.orc_uaq_fold.argtypes = [_P, _I, _I, _I, _P, _P, _I, _I]
+            L.orc_rmsnorm.argtypes = [_P, _I, _I, _I, _P, ctypes.c_float, _P, _I, _P]
             L.orc_e4m3_encode_array.argtypes = [_P, _I, _P]
             L.orc_e4m3_decode_array.argtypes = [_P, _I, _P]
             L.orc_f32_to_bf16_array.argtypes = [_P, _I, _P]
@@ -272,6 +274,32 @@ def uaq_fold(w, s, prev=None):
     lib().orc_uaq_fold(_ptr(w), N, K, K, _ptr(s),
                        _ptr(prev) if prev is not None else None, R, K)
     return w, prev
+
+
+def rmsnorm(h, gamma, eps: float):
+    """RMSNorm of a bf16 hidden state with the (UAQ-folded) weight gamma, the
+    activation the linear layer quantizes.  QuRL notes, 关键设计 §1: the UAQ
+    scale s can be folded straight into the norm's scale (gamma' = gamma * s,
+    e.g. with ``uaq_fold``).  Reading of the norm (the pages give no formula):
+    x = h / sqrt(mean(h^2) + eps) * gamma in fp32 steps, the sum of squares
+    accumulated by fused multiply-adds in index order, one rounding to bf16:
+
+      acc = fma-sum of h[m,k]^2 over k in order;  ms = fl32(acc / K)
+      r   = fl32(1 / fl32(sqrt(fl32(ms + eps))))
+      x   = bf16_RN(fl32(fl32(h * r) * gamma[k]))
+
+    h: bf16 bits [M,K]; gamma: bf16 bits [K]; eps fp32 (>= 0).
+    Returns (x bf16 bits [M,K], rstd f32 [M] = r per row).
+    """
+    h = _bf16_2d(h)
+    M, K = h.shape
+    g = np.ascontiguousarray(np.asarray(gamma, dtype=np.uint16).reshape(-1))
+    if g.shape != (K,):
+        raise ValueError("gamma must have K entries")
+    x = np.empty((M, K), np.uint16)
+    rstd = np.empty((M,), np.float32)
+    lib().orc_rmsnorm(_ptr(h), M, K, K, _ptr(g), float(eps), _ptr(x), K, _ptr(rstd))
+    return x, rstd
 
 
 NVFP4_BLOCK = 16

@@ -33,6 +33,9 @@
  *    geometrically from sigma_start to sigma_end; z is drawn by the caller.
  *  - The UAQ invariant-scaling fold WX = (W/s)(sX) (QuRL notes, 关键设计 §1):
  *    W'[n,k] = bf16_RN(fl32(W[n,k] / s_k)),  P'[r,k] = bf16_RN(fl32(P[r,k] * s_k)).
+ *  - RMSNorm with the UAQ scale folded into its weight (same section: s can be
+ *    folded into the norm's scale), the activation that the 1x128 quantizer then
+ *    takes; its fp32 steps are spelled out at orc_rmsnorm.
  *
  * The fp64 GEMMs over dequantized operands live in oracle.py (NumPy).
  *
@@ -336,6 +339,45 @@ void orc_aqn_perturb(uint16_t *gamma, int64_t K, const float *z, float sigma)
     for (int64_t k = 0; k < K; ++k) {
         float noise = sigma * z[k];
         gamma[k] = orc_f32_to_bf16_rn(bf16_bits_to_f32(gamma[k]) + noise);
+    }
+}
+
+/* ----------------------------------------------------------- RMSNorm --- */
+
+/* RMSNorm of the hidden state ahead of the linear layer, with the UAQ scale
+ * already folded into its weight (QuRL notes, 关键设计 §1: the per-channel s
+ * that multiplies the previous activation can be folded straight into the
+ * LayerNorm / RMSNorm scale, gamma' = gamma * s).  The pages give no formula
+ * for the norm itself; the reading used here is the standard one,
+ * x = h / sqrt(mean(h^2) + eps) * gamma, with every step in fp32 and one final
+ * rounding to bf16 (the activation the layer quantizes):
+ *
+ *   acc  = sum over k = 0 .. K-1, in index order, of h[m,k]^2, accumulated as
+ *          acc = fmaf(h, h, acc) in fp32 from acc = 0
+ *   ms   = fl32(acc / K)
+ *   d    = fl32(sqrt(fl32(ms + eps)))
+ *   r    = fl32(1 / d)                       (written to rstd[m])
+ *   x    = bf16_RN(fl32(fl32(h[m,k] * r) * gamma[k]))
+ *
+ * h [M,K] bf16 (pitch ldh), gamma [K] bf16, x [M,K] bf16 (pitch ldx), rstd [M]. */
+void orc_rmsnorm(const uint16_t *h, int64_t M, int64_t K, int64_t ldh, const uint16_t *gamma, float eps,
+                 uint16_t *x, int64_t ldx, float *rstd)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        float acc = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = bf16_bits_to_f32(h[m * ldh + k]);
+            acc = fmaf(v, v, acc);
+        }
+        float ms = acc / (float)K;
+        float d = sqrtf(ms + eps);
+        float r = 1.0f / d;
+        rstd[m] = r;
+        for (int64_t k = 0; k < K; ++k) {
+            float hr = bf16_bits_to_f32(h[m * ldh + k]) * r;
+            x[m * ldx + k] = orc_f32_to_bf16_rn(hr * bf16_bits_to_f32(gamma[k]));
+        }
     }
 }
 
