@@ -57,6 +57,10 @@ B_FOLD_W = 4  # read + write bf16 per weight element
 B_ROWS = 2 + 1 + 4 / 128
 B_WEIGHT = 2 + 1 + 4 / 16384
 
+# Rate a probe of back-to-back tcgen05.mma.kind::f8f6f4 from shared memory sustained on
+# all SMs of a GB300 (no TMA, no epilogue): reported as context beside the roofline.
+FP8_MMA_PROBE_TFLOPS = 4860.0
+
 
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -290,7 +294,9 @@ def run_ours(args):
     flop_step = 3 * 2.0 * M_ * N_ * K_
     value = world * flop_step / (ms_max * 1e-3) / 1e12
 
-    fp8_peak = 2.0 * peaks["bf16_sustained"]  # dense FP8 = 2 x dense bf16 (nominal 4.5 / 2.25 PF)
+    # Each kernel is timed per launch inside a ~1.4 ms step, so the burst peak is the
+    # denominator: dense FP8 = 2 x the measured dense bf16 burst (nominal 4.5 / 2.25 PF).
+    fp8_peak = 2.0 * peaks["bf16_burst"]
     kern = {}
     for k, (kind, amount) in kernel_work().items():
         t = statistics.mean(per_kernel[k])
@@ -308,7 +314,9 @@ def run_ours(args):
         ach = damount / (dt * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1),
                 "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 3), "traffic": traffic,
-                "peak_source": f"{peaks['source']}: 2 x bf16 sustained {peaks['bf16_sustained']} TFLOP/s"}
+                "peak_source": f"{peaks['source']}: 2 x bf16 burst {peaks['bf16_burst']} TFLOP/s",
+                "context": {"frac_of_2x_bf16_sustained": round(ach / (2.0 * peaks["bf16_sustained"]), 3),
+                            "frac_of_fp8_mma_probe_4860": round(ach / FP8_MMA_PROBE_TFLOPS, 3)}}
     else:
         ach = damount / (dt * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -537,7 +545,7 @@ def run_sweep(args):
     rlq.lib()
     peaks = _peaks()
     bw = peaks["hbm_gbs"]
-    fp8 = 2.0 * peaks["bf16_sustained"]
+    fp8 = 2.0 * peaks["bf16_burst"]  # kernels are timed one at a time: burst peak
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     rows = []
 
@@ -703,7 +711,7 @@ def run_sweep(args):
 
 CASE_DOC = """Run one kernel of the path on one shape --case-reps times (after 2 warm-up
 calls), for profiler captures of a small case: gemm_fprop, gemm_dgrad,
-gemm_wgrad (optionally --split-k), quant_rows, quant_dual, quant_weight, uaq_fold.  Prints the
+gemm_dgrad_mn (untransposed weight codes), gemm_wgrad (optionally --split-k), quant_rows, quant_dual, quant_weight, uaq_fold.  Prints the
 median CUDA-event time; no JSON line."""
 
 
@@ -724,7 +732,7 @@ def run_case(args):
         qw, sw, _ = rlq.quant_weight_128x128(w)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         fn = lambda: rlq.gemm_fprop(qx, sx, qw, sw, out=y, split_k=args.split_k)
-    elif name in ("gemm_dgrad", "gemm_wgrad"):
+    elif name in ("gemm_dgrad", "gemm_dgrad_mn", "gemm_wgrad"):
         dy = _dev_normal(gen, (M, N), 1e-3)
         qw, sw, qwT = rlq.quant_weight_128x128(w, transposed=True)
         qx, sx, qxT, sxc = rlq.quant_act_1x128(x, colwise=True)
@@ -732,6 +740,9 @@ def run_case(args):
         if name == "gemm_dgrad":
             dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
             fn = lambda: rlq.gemm_dgrad(qdy, sdy, qwT, sw, out=dx, split_k=args.split_k)
+        elif name == "gemm_dgrad_mn":  # the FProp weight codes read MN-major, no transposed copy
+            dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+            fn = lambda: rlq.gemm_dgrad(qdy, sdy, qw, sw, transposed=False, out=dx, split_k=args.split_k)
         else:
             dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
             fn = lambda: rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc, out=dw, split_k=args.split_k)

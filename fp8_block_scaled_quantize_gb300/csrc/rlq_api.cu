@@ -547,6 +547,12 @@ rlq_status rlq_diag_bounded_wait(int64_t timeout_us, rlq_stream_t stream)
     return launch_diag_wait(timeout_us, cs(stream));
 }
 
+rlq_status rlq_diag_arm_gemm_stall(void)
+{
+    arm_gemm_stall();
+    return RLQ_OK;
+}
+
 const char *rlq_status_string(rlq_status status)
 {
     switch (status) {

@@ -467,6 +467,9 @@ struct Params {
     int splits, kbps, num_units;
     float *ws;
     uint64_t timeout_ns;
+    // diagnostic (single CTA only): the producer withholds the loads of the CTA's
+    // first stage, so the MMA warp's bounded wait on it runs out
+    int withhold_first_load;
 };
 
 struct Unit {
@@ -609,6 +612,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         else
                             tma_load_2d_pair(b_stage(s), &tmB, fb, kb * BK, nt * BN + row_offset<kPair>());
                     } else {
+                        if (p.withhold_first_load && it == 0)
+                            continue;  // nothing arrives on this stage's barrier
                         mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
                         tma_load_2d(a_stage(s), &tmA, full_bar(s), kb * BK, mt * BM);
                         if (kBMajorMN) {
@@ -621,20 +626,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            if (!ok) {
-                if constexpr (kPair) {
+            if constexpr (kPair) {
+                if (!ok) {
                     // the copies complete on the even CTA's barriers: give them time to land
                     const uint64_t t0 = global_timer_ns();
                     while (global_timer_ns() - t0 < 200000ull)
                         __nanosleep(1000);
-                } else {
-                    // drain: the copies issued into the last stages complete on their own
-                    const int first = it > STAGES ? it - STAGES : 0;
-                    for (int j = first; j < it; ++j) {
-                        volatile uint32_t never = 0;
+                }
+            }
+            if constexpr (!kPair) {
+                // A CTA that aborted may still have copies in flight into stages no
+                // MMA consumed: they complete on their own, and are waited for
+                // (bounded) before the CTA's shared memory goes away.  Once both MMA
+                // warps have made their final commit, every stage they did not
+                // consume is known: if they finished normally they consumed all.
+                volatile uint32_t never = 0;
+                mbar_wait(teardown_bar, 0, &never, p.timeout_ns, SITE_TEARDOWN);
+                if (!ok || *abort_flag || p.withhold_first_load) {
+                    int first = it > STAGES ? it - STAGES : 0;
+                    if (p.withhold_first_load && first == 0)
+                        first = 1;  // the withheld stage has nothing in flight
+                    for (int j = first; j < it; ++j)
                         mbar_wait(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, &never, 20000000ull,
                                   SITE_DRAIN);
-                    }
                 }
             }
         }
@@ -1128,7 +1142,7 @@ bool pair_mode_enabled()
 }
 
 template <bool kCol, bool kBMN, bool kPair>
-rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
+rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool withhold_first_load = false)
 {
     using Cf = Cfg<kPair>;
     CUtensorMap tmA, tmB, tmO;
@@ -1177,7 +1191,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
             di.max_clusters[variant] = n < 1 ? -1 : n;  // -1: no pair fits, use single CTAs
         }
         if (di.max_clusters[variant] < 0)
-            return launch_impl<kCol, kBMN, false>(a, splits, st);
+            return launch_impl<kCol, kBMN, false>(a, splits, st, withhold_first_load);
     }
     Params p;
     p.sa = a.sa;
@@ -1196,6 +1210,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
     // keep the smaller operand resident in L2: sweep the tiles along it
     p.m_fastest = (a.R * a.L <= a.C * a.L) ? 1 : 0;
     p.timeout_ns = wait_limit_ns();
+    p.withhold_first_load = (!kPair && withhold_first_load) ? 1 : 0;
     p.kbps = (p.kblocks + splits - 1) / splits;
     p.splits = (p.kblocks + p.kbps - 1) / p.kbps;
     p.num_units = p.num_tiles * p.splits;
@@ -1227,6 +1242,9 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st)
         k_splitk_reduce<<<(int)rgrid, 256, 0, st>>>(a.ws, p.splits, p.R, p.C, a.out, a.ldo);
     return cuda_status(cudaGetLastError(), "split-K reduction launch");
 }
+
+// One-shot diagnostic armed by arm_gemm_stall() for the calling thread.
+thread_local bool t_stall_armed = false;
 
 rlq_status current_sms(int *sms)
 {
@@ -1264,15 +1282,22 @@ rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st)
         if (splits < 2)
             splits = 2;
     }
+    // the armed stall diagnostic applies to this launch only, on single CTAs
+    const bool stall = t_stall_armed;
+    t_stall_armed = false;
     // CTA pairs for tiles of 256 output rows; one CTA per 128 rows when the output
     // has fewer rows or the contraction is split
-    const bool pair = splits == 1 && a.R >= 2 * BM && pair_mode_enabled();
+    const bool pair = splits == 1 && a.R >= 2 * BM && pair_mode_enabled() && !stall;
     if (a.per_col_sb)
-        return pair ? launch_impl<true, false, true>(a, splits, st) : launch_impl<true, false, false>(a, splits, st);
+        return pair ? launch_impl<true, false, true>(a, splits, st)
+                    : launch_impl<true, false, false>(a, splits, st, stall);
     if (a.b_mn_major)
-        return pair ? launch_impl<false, true, true>(a, splits, st) : launch_impl<false, true, false>(a, splits, st);
-    return pair ? launch_impl<false, false, true>(a, splits, st) : launch_impl<false, false, false>(a, splits, st);
+        return pair ? launch_impl<false, true, true>(a, splits, st)
+                    : launch_impl<false, true, false>(a, splits, st, stall);
+    return pair ? launch_impl<false, false, true>(a, splits, st) : launch_impl<false, false, false>(a, splits, st, stall);
 }
+
+void arm_gemm_stall() { t_stall_armed = true; }
 
 rlq_status plan_splitk(int64_t R, int64_t C, int64_t L, int64_t ws_cap, int *splits, int64_t *ws_bytes)
 {
@@ -1307,8 +1332,9 @@ rlq_status check_device_errors(cudaStream_t st)
         return cuda_status(e, "clearing the device error word");
     const uint32_t code = (uint32_t)word, site = (uint32_t)(word >> 32);
     static const char *names[] = {"?", "TMA producer (stage free)", "MMA issuer (TMEM buffer free)",
-                                  "MMA issuer (stage loaded)", "epilogue (partial ready)", "teardown", "drain"};
-    const char *where = site == SITE_DIAG ? "diagnostic wait" : (site < 7 ? names[site] : "?");
+                                  "MMA issuer (stage loaded)", "epilogue (partial ready)", "teardown", "drain",
+                                  "scale loader (slot free)", "epilogue (scales ready)"};
+    const char *where = site == SITE_DIAG ? "diagnostic wait" : (site < 9 ? names[site] : "?");
     return fail((rlq_status)code, "device-side wait ran out at site %u (%s)", site, where);
 }
 

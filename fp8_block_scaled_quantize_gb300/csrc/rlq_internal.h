@@ -78,4 +78,9 @@ rlq_status plan_splitk(int64_t R, int64_t C, int64_t L, int64_t ws_cap, int *spl
 rlq_status check_device_errors(cudaStream_t st);
 rlq_status launch_diag_wait(int64_t timeout_us, cudaStream_t st);
 
+// Arms, for the calling thread, a one-shot stall of the next block-scaled GEMM
+// launch: it runs on single CTAs and its producer withholds the first stage's
+// loads, so the MMA warp's bounded wait runs out and the CTA takes its abort path.
+void arm_gemm_stall();
+
 }  // namespace rlq

@@ -12,8 +12,16 @@
 // The scratch is a file-scope __device__ array of RLQ_STATIC_SCRATCH_BYTES;
 // every device that loads the library holds it until the process exits.  In
 // host code `g_static_scratch` is only a host-side stand-in for the symbol:
-// its device address comes from cudaGetSymbolAddress, once per device, with
-// that device current, on the first call made on it.
+// its device address comes from cudaGetSymbolAddress, with the device current,
+// on the first call made on that device in a given CUDA context.  The address
+// is remembered per device together with the context it was looked up in: a
+// call under another context (after cudaDeviceReset rebuilt the primary
+// context, or under a context the caller made current with the driver API)
+// looks it up again, since the module, and with it the array, may then sit
+// elsewhere.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "rlq_internal.h"
@@ -30,6 +38,7 @@ constexpr int MAX_DEVICES = 64;
 struct ScratchTable {
     std::mutex mu;
     void *ptr[MAX_DEVICES] = {};
+    CUcontext ctx[MAX_DEVICES] = {};  // context each address was looked up in
 };
 
 ScratchTable &scratch_table()
@@ -38,7 +47,28 @@ ScratchTable &scratch_table()
     return t;
 }
 
-// Device address of the static scratch on the current device (set up once).
+// The calling thread's current CUDA context (NULL if none), through the
+// driver entry point the runtime exposes; no library beyond the runtime is
+// linked for it.
+CUcontext current_context()
+{
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    });
+    CUcontext c = nullptr;
+    if (fn == nullptr || fn(&c) != CUDA_SUCCESS)
+        return nullptr;
+    return c;
+}
+
+// Device address of the static scratch on the current device, looked up on
+// the first call in each context.
 rlq_status static_scratch(void **out)
 {
     int dev = 0;
@@ -50,14 +80,18 @@ rlq_status static_scratch(void **out)
                     MAX_DEVICES);
     ScratchTable &t = scratch_table();
     std::lock_guard<std::mutex> g(t.mu);
-    if (t.ptr[dev] == nullptr) {
+    CUcontext ctx = current_context();
+    if (t.ptr[dev] == nullptr || ctx == nullptr || ctx != t.ctx[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess)
             return cuda_status(e, "cudaGetSymbolAddress(static split-K scratch)");
         if (p == nullptr || ((uintptr_t)p & 255u) != 0)
             return fail(RLQ_ERR_CUDA, "static split-K scratch has an unexpected device address %p", p);
+        // the lookup made the device's primary context current if none was
+        ctx = current_context();
         t.ptr[dev] = p;
+        t.ctx[dev] = ctx;
     }
     *out = t.ptr[dev];
     return RLQ_OK;

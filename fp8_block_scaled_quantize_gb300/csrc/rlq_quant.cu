@@ -81,7 +81,12 @@ __device__ __forceinline__ Quot make_quot(float s)
 
 
 // fl32(x / s) for two elements at once, as described at the top of this file:
-// q0 = x*r, e = x - q0*s (one FMA, rounded toward -inf), q1 = q0 + e*r.  The
+// q0 = x*r, e = x - q0*s (one FMA, rounded toward -inf), q1 = q0 + e*r.  This is
+// the quotient-correction step of Markstein's division (P. Markstein, IBM J. Res.
+// Dev. 34(1), 1990; "IA-64 and Elementary Functions", 2000): with an FMA the
+// residual x - q0*s is exact, and one multiply-add of it by the reciprocal moves
+// q0 to the correctly rounded quotient under conditions that the enumeration
+// below checks for this input domain.  The
 // downward-rounded residual keeps the sign of a zero quotient (x = -0 gives -0);
 // every (x, amax) bf16 pair was enumerated: q1 equals the IEEE quotient wherever
 // the E4M3 code depends on it, sign included.  Each packed operation rounds

@@ -44,6 +44,7 @@ _SIGS = {
     "rlq_aqn_perturb": [_P, _I, _P, ctypes.c_float, _P],
     "rlq_check": [_P],
     "rlq_diag_bounded_wait": [_I, _P],
+    "rlq_diag_arm_gemm_stall": [],
 }
 
 STATUS = {0: "RLQ_OK", 1: "RLQ_ERR_INVALID_ARG", 2: "RLQ_ERR_UNSUPPORTED", 3: "RLQ_ERR_MISALIGNED",
@@ -200,6 +201,10 @@ def rlq_check(stream):
 
 def rlq_diag_bounded_wait(timeout_us, stream):
     return _call("rlq_diag_bounded_wait", timeout_us, stream)
+
+
+def rlq_diag_arm_gemm_stall():
+    return _call("rlq_diag_arm_gemm_stall")
 
 
 def rlq_status_string(status: int) -> str:

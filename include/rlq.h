@@ -336,17 +336,23 @@ rlq_status rlq_gemm_wgrad_splitk(const uint8_t *dyqT, int64_t lddyqT, const floa
  * because of its implicit synchronisation.  The caller still owns and passes
  * every input and output.
  *
- *   Arguments, shapes, result and errors are those of rlq_gemm_fprop_splitk
- *   with a workspace of RLQ_STATIC_SCRATCH_BYTES, with one more error: when
- *   the split-K plan for (M, N, K) needs more scratch than that (see
- *   rlq_gemm_splitk_workspace_bytes), the call returns RLQ_ERR_UNSUPPORTED
- *   and launches nothing.  A plan of one pass uses no scratch.
+ *   Arguments and shapes are those of rlq_gemm_fprop_splitk.  The call runs
+ *   the library's unconstrained split-K plan for (M, N, K) (the one
+ *   rlq_gemm_splitk_workspace_bytes sizes), so its result is that of
+ *   rlq_gemm_fprop_splitk given a workspace of at least that size.  When that
+ *   plan needs more than RLQ_STATIC_SCRATCH_BYTES, the call returns
+ *   RLQ_ERR_UNSUPPORTED and launches nothing; it does not fall back to a
+ *   smaller plan (rlq_gemm_fprop_splitk with a caller's workspace of that
+ *   size would).  A plan of one pass uses no scratch.
  *   The scratch (RLQ_STATIC_SCRATCH_BYTES, 16 MiB, in device memory) is held
  *   on every device that loads the library until the process exits.  The
  *   call itself calls no cudaMalloc, cudaFree or other allocating routine.
- *   The first call on a device looks up the scratch's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   The first call on a device in each CUDA context looks up the scratch's
+ *   device address (cudaGetSymbolAddress, with that device current) and
+ *   remembers it with the context; a call under a different context (after
+ *   cudaDeviceReset, or under a context made current with the driver API)
+ *   looks it up again.  Make the first call in a context before any stream
+ *   capture.
  *   All calls on a device share the one scratch, which keeps whatever the
  *   last call left there; each call writes every scratch element it reads, so
  *   nothing needs clearing.  Calls whose executions overlap on the GPU (other
@@ -388,6 +394,20 @@ rlq_status rlq_check(rlq_stream_t stream);
  * returns RLQ_ERR_TIMEOUT and the context stays usable.
  */
 rlq_status rlq_diag_bounded_wait(int64_t timeout_us, rlq_stream_t stream);
+
+/*
+ * Diagnostic for the block-scaled GEMM's own abort path: arms, for the calling
+ * host thread, a one-shot fault in the next GEMM call it makes (any of the
+ * FProp / DGrad / WGrad entry points).  That launch runs on single CTAs, and
+ * the TMA producer of every CTA withholds the loads of its first pipeline
+ * stage, so nothing ever arrives on that stage's barrier: the MMA warp's
+ * bounded wait runs out (RLQ_WAIT_TIMEOUT_MS, 1 s by default), it records a
+ * timeout and raises the CTA's abort flag, and the CTA drains its copies in
+ * flight, frees its tensor memory and exits.  The output of that call is
+ * undefined; the following rlq_check returns RLQ_ERR_TIMEOUT, and later calls
+ * run normally.  Nothing faults, traps or hangs.  Host-only; always RLQ_OK.
+ */
+rlq_status rlq_diag_arm_gemm_stall(void);
 
 /* Static description of a status code. */
 const char *rlq_status_string(rlq_status status);

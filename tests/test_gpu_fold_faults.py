@@ -96,3 +96,43 @@ def test_invalid_arguments_raise_before_launch():
         rlq.quant_act_1x128(x)
     assert e.value.status == 2
     rlq.check()
+
+
+@pytest.mark.parametrize("kind", ["fprop", "wgrad"])
+def test_gemm_abort_path_reports_timeout_and_context_survives(kind):
+    """The block-scaled GEMM's own bounded waits: with the stall diagnostic
+    armed, the next GEMM runs on single CTAs whose producer withholds its first
+    stage's loads.  The MMA warp's wait runs out, the CTA raises its abort flag,
+    drains its copies, frees its tensor memory and exits; rlq_check reports the
+    timeout, the error word clears, and the same GEMM then matches the oracle."""
+    M, N, K = 1024, 512, 1024  # 8 contraction blocks per tile either way: one stage withheld, three in flight
+    x = I.to_bf16_bits(I.normal(11, "x", (M, K), 1.0))
+    w = I.to_bf16_bits(I.normal(11, "w", (N, K), 0.02))
+    qx, sx, qxT, sxc = rlq.quant_act_1x128(to_dev(x), colwise=True)
+    qw, sw, _ = rlq.quant_weight_128x128(to_dev(w))
+    rlq.check()
+
+    def run():
+        if kind == "fprop":
+            return rlq.gemm_fprop(qx, sx, qw, sw)
+        return rlq.gemm_wgrad(qxT, sxc, qxT, sxc)  # dX^T X-shaped: [K, K] over M tokens
+
+    rlq.rlq_diag_arm_gemm_stall()
+    run()
+    with pytest.raises(rlq.RlqError) as e:
+        rlq.check()
+    assert e.value.status == 5 and "device-side wait ran out" in str(e.value)
+    rlq.check()  # cleared
+    got = run()
+    rlq.check()
+    oqx, osx = oracle.quant_rows_1x128(x)
+    if kind == "fprop":
+        oqw, osw, _ = oracle.quant_weight_128x128(w)
+        ref = oracle.gemm_fprop(oqx, osx, oqw, osw)
+    else:
+        oqxT, osxc = oracle.quant_cols_128x1(x)
+        assert np.array_equal(np_(qxT), oqxT)
+        ref = oracle.gemm_wgrad(oqxT, osxc, oqxT, osxc)
+    g = got.float().cpu().numpy().astype(np.float64)
+    assert np.linalg.norm(g - ref) <= 2e-3 * np.linalg.norm(ref)
+    assert not (np.abs(g - ref) > 1e-2 * (np.abs(ref) + 1)).any()

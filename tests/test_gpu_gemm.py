@@ -16,7 +16,8 @@ import torch
 import oracle
 from fp8_block_scaled_quantize_gb300 import inputs as I
 from fp8_block_scaled_quantize_gb300 import rlq
-from gpu_util import assert_gemm_close, normal_bits, np_, to_dev, u16
+from gpu_util import (assert_gemm_close, idx, normal_bits, np_, quant_act_checked, quant_weight_checked,
+                      strata, to_dev, u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -178,57 +179,47 @@ def test_all_zero_operands_give_zero():
 
 # ---------------------------------------------------- full-size, sampled ---
 
-def _sample(n, k, rng):
-    return np.sort(rng.choice(n, size=min(n, k), replace=False))
-
-
 def test_full_size_train_step_8b_sampled():
     """The 8B-shaped training step (M=8192, N=14336, K=4096): all three GEMMs
-    in the bench's launch configuration, checked on sampled outputs."""
+    in the bench's launch configuration, checked on outputs sampled in every
+    128-row stratum against the oracle's GEMMs over the oracle's own codes
+    (the GPU's codes, column-wise ones included, are asserted equal first)."""
     d = I.train_step_8b()
-    xg, wg, dyg = to_dev(d["x"]), to_dev(d["w"]), to_dev(d["dy"])
-    qx, sx, qxT, sxc = rlq.quant_act_1x128(xg, colwise=True)
-    qdy, sdy, qdyT, sdyc = rlq.quant_act_1x128(dyg, colwise=True)
-    qw, sw, qwT = rlq.quant_weight_128x128(wg, transposed=True)
-    del xg, wg, dyg
+    (qx, sx, qxT, sxc), (oqx, osx, oqxT, osxc) = quant_act_checked(d["x"], colwise=True)
+    (qdy, sdy, qdyT, sdyc), (oqdy, osdy, oqdyT, osdyc) = quant_act_checked(d["dy"], colwise=True)
+    (qw, sw, qwT), (oqw, osw, _) = quant_weight_checked(d["w"], transposed=True)
+    del d
     y = rlq.gemm_fprop(qx, sx, qw, sw)
     dx = rlq.gemm_dgrad(qdy, sdy, qwT, sw, transposed=True)
     dw = rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc)
     rlq.check()
     rng = np.random.default_rng(5)
     M, N, K = 8192, 14336, 4096
-    rows = _sample(M, 96, rng)
-    rows_n = _sample(N, 96, rng)
-    hqx, hsx, hqw, hsw = np_(qx), np_(sx), np_(qw), np_(sw)
-    assert_gemm_close(y[torch.from_numpy(rows).cuda()], oracle.gemm_fprop(hqx, hsx, hqw, hsw, rows=rows),
-                      "FProp 8B")
-    assert_gemm_close(dx[torch.from_numpy(rows).cuda()],
-                      oracle.gemm_dgrad(np_(qdy), np_(sdy), hqw, hsw, rows=rows), "DGrad 8B")
-    assert_gemm_close(dw[torch.from_numpy(rows_n).cuda()],
-                      oracle.gemm_wgrad(np_(qdyT), np_(sdyc), np_(qxT), np_(sxc), rows=rows_n), "WGrad 8B")
+    rows = strata(M, 128, rng)
+    rows_n = strata(N, 128, rng)
+    assert_gemm_close(y[idx(rows)], oracle.gemm_fprop(oqx, osx, oqw, osw, rows=rows), "FProp 8B")
+    assert_gemm_close(dx[idx(rows)], oracle.gemm_dgrad(oqdy, osdy, oqw, osw, rows=rows), "DGrad 8B")
+    assert_gemm_close(dw[idx(rows_n)], oracle.gemm_wgrad(oqdyT, osdyc, oqxT, osxc, rows=rows_n), "WGrad 8B")
 
 
 @pytest.mark.parametrize("M", [1, 16, 64, 256, 1024])
 def test_sweep_32b_small_and_mid_M(M):
     d = I.sweep_32b(M, "up")
-    xg, wg, dyg = to_dev(d["x"]), to_dev(d["w"]), to_dev(d["dy"])
-    qx, sx, qxT, sxc = rlq.quant_act_1x128(xg, colwise=True)
-    qdy, sdy, qdyT, sdyc = rlq.quant_act_1x128(dyg, colwise=True)
-    qw, sw, qwT = rlq.quant_weight_128x128(wg, transposed=True)
+    (qx, sx, qxT, sxc), (oqx, osx, oqxT, osxc) = quant_act_checked(d["x"], colwise=True)
+    (qdy, sdy, qdyT, sdyc), (oqdy, osdy, oqdyT, osdyc) = quant_act_checked(d["dy"], colwise=True)
+    (qw, sw, qwT), (oqw, osw, _) = quant_weight_checked(d["w"], transposed=True)
+    del d
     y = rlq.gemm_fprop(qx, sx, qw, sw)
     dx = rlq.gemm_dgrad(qdy, sdy, qwT, sw, transposed=True)
     dw = rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc)
     rlq.check()
     rng = np.random.default_rng(M)
-    hqw, hsw = np_(qw), np_(sw)
-    rows = _sample(M, 64, rng)
-    assert_gemm_close(y[torch.from_numpy(rows).cuda()],
-                      oracle.gemm_fprop(np_(qx), np_(sx), hqw, hsw, rows=rows), f"FProp 32B M={M}")
-    assert_gemm_close(dx[torch.from_numpy(rows).cuda()],
-                      oracle.gemm_dgrad(np_(qdy), np_(sdy), hqw, hsw, rows=rows), f"DGrad 32B M={M}")
-    rows_n = _sample(27648, 64, rng)
-    assert_gemm_close(dw[torch.from_numpy(rows_n).cuda()],
-                      oracle.gemm_wgrad(np_(qdyT), np_(sdyc), np_(qxT), np_(sxc), rows=rows_n), f"WGrad 32B M={M}")
+    rows = np.arange(M) if M <= 256 else strata(M, 16, rng)
+    assert_gemm_close(y[idx(rows)], oracle.gemm_fprop(oqx, osx, oqw, osw, rows=rows), f"FProp 32B M={M}")
+    assert_gemm_close(dx[idx(rows)], oracle.gemm_dgrad(oqdy, osdy, oqw, osw, rows=rows), f"DGrad 32B M={M}")
+    rows_n = strata(27648, 128, rng)
+    assert_gemm_close(dw[idx(rows_n)], oracle.gemm_wgrad(oqdyT, osdyc, oqxT, osxc, rows=rows_n),
+                      f"WGrad 32B M={M}")
 
 
 _MODE_SCRIPT = r"""

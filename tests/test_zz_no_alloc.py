@@ -20,11 +20,12 @@ def _quantized(M, N, K, seed):
     return qx, sx, qw, sw
 
 
-def _static_fprop(qx, sx, qw, sw, y):
+def _static_fprop(qx, sx, qw, sw, y, stream=None):
     M, K = qx.shape
     N = qw.shape[0]
+    st = (stream or torch.cuda.current_stream()).cuda_stream
     rlq.rlq_gemm_fprop_splitk_static(qx.data_ptr(), K, sx.data_ptr(), M, qw.data_ptr(), K, sw.data_ptr(), K // 128,
-                                     y.data_ptr(), N, M, N, K, torch.cuda.current_stream().cuda_stream)
+                                     y.data_ptr(), N, M, N, K, st)
 
 
 def _assert_close(got, ref, what):
@@ -47,6 +48,23 @@ def test_static_scratch_matches_workspace_entry_point_twice(M, N, K):
         _static_fprop(qx, sx, qw, sw, y)
         rlq.check()
         _assert_close(y, ref, f"static-scratch FProp, seed {seed}")
+
+
+def test_static_scratch_on_a_side_stream_twice():
+    """Two calls in a row on a stream other than the default one, each synced
+    and checked: the scratch's address holds for every stream of the context."""
+    M, N, K = 64, 512, 4096
+    side = torch.cuda.Stream()
+    for seed in (72, 73):
+        qx, sx, qw, sw = _quantized(M, N, K, seed)
+        ref = rlq.gemm_fprop(qx, sx, qw, sw, split_k=True)
+        torch.cuda.synchronize()
+        y = torch.full((M, N), -3.0, dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+        _static_fprop(qx, sx, qw, sw, y, stream=side)
+        rlq.check(side)
+        torch.cuda.synchronize()
+        _assert_close(y, ref, f"static-scratch FProp on a side stream, seed {seed}")
 
 
 def test_plan_beyond_static_scratch_is_rejected():
