@@ -573,7 +573,7 @@ def run_sweep(args):
     def gemm_bytes(Mr, Nc, L):
         return Mr * L + Nc * L + 2 * Mr * Nc + 4 * (Mr + Nc) * ((L + 127) // 128)
 
-    def linear(cfg, x, w, dy=None, s=None, full=False, per_channel=False):
+    def linear(cfg, x, w, dy=None, s=None, full=False, per_channel=False, norm=False):
         """Time the quantizers, fold and GEMMs of one linear layer (with
         ``per_channel`` also the per-token / per-channel quantizers and FProp)."""
         M, K = x.shape
@@ -595,6 +595,16 @@ def run_sweep(args):
                 zz = torch.randn(K, generator=torch.Generator(device=dev).manual_seed(5), device=dev)
                 emit(cfg, "aqn_perturb", _time_ms(lambda: rlq.aqn_perturb_(gam, zz, 1e-3), flush), nbytes=8 * K)
         emit(cfg, "quant_rows_x", _time_ms(lambda: rlq.quant_act_1x128(x), flush), nbytes=B_ROWS * M * K)
+        if norm:
+            # RMSNorm of a hidden state of X's shape fused with the quantizer (x here
+            # stands in for the hidden state): one read of h, the codes, the scales
+            # and the per-row factors
+            gam = torch.ones(K, dtype=torch.bfloat16, device=dev)
+            emit(cfg, "rmsnorm_quant_rows_x", _time_ms(lambda: rlq.rmsnorm_quant_act_1x128(x, gam, 1e-5), flush),
+                 nbytes=B_ROWS * M * K + 4 * M)
+            emit(cfg, "rmsnorm_quant_dual_x",
+                 _time_ms(lambda: rlq.rmsnorm_quant_act_1x128(x, gam, 1e-5, colwise=True), flush),
+                 nbytes=B_DUAL * M * K + 4 * M)
         if full:
             emit(cfg, "quant_dual_x", _time_ms(lambda: rlq.quant_act_1x128(x, colwise=True), flush),
                  nbytes=B_DUAL * M * K)
@@ -677,7 +687,7 @@ def run_sweep(args):
     # 8B training step
     gen.manual_seed(2)
     linear("train_step_8b M=8192 N=14336 K=4096", _dev_normal(gen, (8192, 4096), 1.0),
-           _dev_normal(gen, (14336, 4096), 0.02), dy=_dev_normal(gen, (8192, 14336), 1e-3), full=True)
+           _dev_normal(gen, (14336, 4096), 0.02), dy=_dev_normal(gen, (8192, 14336), 1e-3), full=True, norm=True)
     # Qwen2.5-7B layer set: fold + quant + FProp
     gen.manual_seed(3)
     for which, (N, K) in (("gate_up", (18944, 3584)), ("down", (3584, 18944))):
@@ -685,7 +695,7 @@ def run_sweep(args):
         s = np.random.default_rng(3).uniform(1.5, 4.0, K).astype(np.float32)
         for M in I.QWEN7B_M:
             linear(f"qwen7b_{which} M={M} N={N} K={K}", _dev_normal(gen, (M, K), 1.0, t_frac=0.01), w, s=s,
-                   per_channel=True)
+                   per_channel=True, norm=(which == "gate_up"))
         del w
     # 32B sweep: all three passes per M
     gen.manual_seed(4)
@@ -694,7 +704,7 @@ def run_sweep(args):
         for M in I.SWEEP_32B_M:
             x = _dev_normal(gen, (M, K), 1.0, 0.005, 50.0)
             dy = _dev_normal(gen, (M, N), 1e-3)
-            linear(f"sweep_32b_{orient} M={M} N={N} K={K}", x, w, dy=dy, full=True)
+            linear(f"sweep_32b_{orient} M={M} N={N} K={K}", x, w, dy=dy, full=True, norm=(orient == "up"))
             del x, dy
             torch.cuda.empty_cache()
         del w
@@ -711,7 +721,8 @@ def run_sweep(args):
 
 CASE_DOC = """Run one kernel of the path on one shape --case-reps times (after 2 warm-up
 calls), for profiler captures of a small case: gemm_fprop, gemm_dgrad,
-gemm_dgrad_mn (untransposed weight codes), gemm_wgrad (optionally --split-k), quant_rows, quant_dual, quant_weight, uaq_fold.  Prints the
+gemm_dgrad_mn (untransposed weight codes), gemm_wgrad (optionally --split-k), quant_rows, quant_dual,
+rmsnorm_quant, rmsnorm_quant_dual, quant_weight, uaq_fold.  Prints the
 median CUDA-event time; no JSON line."""
 
 
@@ -748,6 +759,9 @@ def run_case(args):
             fn = lambda: rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc, out=dw, split_k=args.split_k)
     elif name == "quant_rows":
         fn = lambda: rlq.quant_act_1x128(x)
+    elif name in ("rmsnorm_quant", "rmsnorm_quant_dual"):
+        gam = torch.ones(K, dtype=torch.bfloat16, device=dev)
+        fn = lambda: rlq.rmsnorm_quant_act_1x128(x, gam, 1e-5, colwise=name.endswith("dual"))
     elif name == "quant_dual":
         fn = lambda: rlq.quant_act_1x128(x, colwise=True)
     elif name == "quant_weight":
@@ -767,9 +781,21 @@ def run_case(args):
         e1.record()
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
+    # back to back: the host enqueues ahead of the GPU, so host-side overhead of the
+    # helpers (output allocation, argument marshalling) drops out; inputs below the
+    # L2 size stay warm between calls
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.case_reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    b2b = e0.elapsed_time(e1) / args.case_reps
     rlq.check()
     ts.sort()
-    print(f"{name} M={M} N={N} K={K} split_k={args.split_k}: median {ts[len(ts) // 2] * 1e3:.1f} us")
+    print(f"{name} M={M} N={N} K={K} split_k={args.split_k}: median {ts[len(ts) // 2] * 1e3:.1f} us, "
+          f"back-to-back {b2b * 1e3:.1f} us")
 
 
 def main():

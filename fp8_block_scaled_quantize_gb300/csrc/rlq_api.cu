@@ -116,6 +116,36 @@ rlq_status rlq_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t 
     return cuda_status(launch_quant_rows(x, M, K, ldx, q, ldq, s, lds, cs(stream)), "1x128 quantizer launch");
 }
 
+rlq_status rlq_rmsnorm_quant_act_1x128(const uint16_t *h, int64_t M, int64_t K, int64_t ldh, const uint16_t *gamma,
+                                      float eps, float *rstd, uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                                      uint8_t *qT, int64_t ldqT, float *sc, int64_t ldsc, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(M >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size (M=%lld, K=%lld)", (long long)M, (long long)K);
+    RLQ_REQUIRE(K % G == 0, RLQ_ERR_UNSUPPORTED, "K=%lld is not a multiple of 128", (long long)K);
+    RLQ_REQUIRE((qT == nullptr) == (sc == nullptr), RLQ_ERR_INVALID_ARG,
+                "qT and sc must be both NULL (row-wise only) or both set (fused 128x1)");
+    RLQ_REQUIRE(M < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    RLQ_REQUIRE(std::isfinite(eps) && eps >= 0.0f, RLQ_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (M == 0 || K == 0)
+        return RLQ_OK;
+    RLQ_TRY(check_bf16("h", h, ldh, K));
+    RLQ_REQUIRE(gamma, RLQ_ERR_INVALID_ARG, "gamma is NULL");
+    RLQ_REQUIRE(al(gamma, 16), RLQ_ERR_MISALIGNED, "gamma is not 16-byte aligned");
+    RLQ_TRY(check_scales("rstd", rstd, M, M));
+    RLQ_TRY(check_codes("q", q, ldq, K));
+    RLQ_TRY(check_scales("s", s, lds, M));
+    if (qT) {
+        RLQ_TRY(check_codes("qT", qT, ldqT, M));
+        RLQ_TRY(check_scales("sc", sc, ldsc, K));
+    }
+    RLQ_TRY(cuda_status(launch_rms_rstd(h, M, K, ldh, eps, rstd, cs(stream)), "RMSNorm row-factor launch"));
+    if (qT)
+        return cuda_status(launch_quant_dual(h, M, K, ldh, q, ldq, s, lds, qT, ldqT, sc, ldsc, cs(stream), rstd, gamma),
+                           "RMSNorm + 1x128 + 128x1 quantizer launch");
+    return cuda_status(launch_quant_rows(h, M, K, ldh, q, ldq, s, lds, cs(stream), rstd, gamma),
+                       "RMSNorm + 1x128 quantizer launch");
+}
+
 rlq_status rlq_quant_per_row(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, int64_t ldq, float *s,
                              float *s_rep, int64_t ld_rep, rlq_stream_t stream)
 {

@@ -18,11 +18,18 @@ const char *last_error_text();
 rlq_status cuda_status(cudaError_t err, const char *what);
 
 // ---- quantizers and fold (rlq_quant.cu); arguments already validated ----
+// With rstd and gamma set, x is a hidden state normalised on the fly
+// (x = bf16_RN(fl32(fl32(h * rstd[m]) * gamma[k]))) before quantization.
 cudaError_t launch_quant_rows(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
-                              int64_t ldq, float *s, int64_t lds, cudaStream_t st);
+                              int64_t ldq, float *s, int64_t lds, cudaStream_t st,
+                              const float *rstd = nullptr, const uint16_t *gamma = nullptr);
 cudaError_t launch_quant_dual(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
                               int64_t ldq, float *s, int64_t lds, uint8_t *qT, int64_t ldqT,
-                              float *sc, int64_t ldsc, cudaStream_t st);
+                              float *sc, int64_t ldsc, cudaStream_t st,
+                              const float *rstd = nullptr, const uint16_t *gamma = nullptr);
+// rstd[m] = fl32(1 / sqrt(fl32(fl32(sum_k h[m,k]^2 / K) + eps))), the sum in index order.
+cudaError_t launch_rms_rstd(const uint16_t *h, int64_t M, int64_t K, int64_t ldh, float eps, float *rstd,
+                            cudaStream_t st);
 cudaError_t launch_quant_weight(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q,
                                 int64_t ldq, float *s, int64_t lds, uint8_t *qT, int64_t ldqT,
                                 cudaStream_t st);

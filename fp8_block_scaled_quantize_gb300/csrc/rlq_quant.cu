@@ -49,6 +49,29 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
     }
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float2 v)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(v.y), "f"(v.x));
+    return d;
+}
+
+// RMSNorm of 8 consecutive bf16 elements of one row with that row's r and the
+// matching 8 norm weights: x = bf16_RN(fl32(fl32(h * r) * gamma)), each product
+// rounded on its own (packed fp32 multiplies round each lane as the scalar op).
+__device__ __forceinline__ uint4 norm8(const uint4 &v, float r, const uint4 &g)
+{
+    const float2 r2 = make_float2(r, r);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 hr = __fmul2_rn(make_float2(bf_lo(w[i]), bf_hi(w[i])), r2);
+        o[i] = pack_bf16x2(__fmul2_rn(hr, make_float2(bf_lo(gw[i]), bf_hi(gw[i]))));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Two E4M3 codes, RN-even with saturation to +-448: `lo` in bits 0..7.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
 {
@@ -206,9 +229,14 @@ __device__ __forceinline__ void row_groups2(const uint4 &va, const uint4 &vb, bo
 // 1x128 row-wise: each half-warp takes a group; a warp owns two consecutive
 // groups per slot and two slots per iteration (four 16-byte loads in flight
 // per lane pair).  Group g = m * KB + kb, advanced incrementally.
+// kNorm: x is a hidden state h, normalised on the fly (rmsnorm row factor rstd[m],
+// weight gamma[k]) before it is quantized.
+template <bool kNorm>
 __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t *__restrict__ x, int64_t M, int KB,
                                                     int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
-                                                    float *__restrict__ s, int64_t lds)
+                                                    float *__restrict__ s, int64_t lds,
+                                                    const float *__restrict__ rstd,
+                                                    const uint16_t *__restrict__ gamma)
 {
     const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -247,6 +275,12 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t *__restrict__
         second(mn, kbn, mn1, kbn1);
         const uint4 an = mn < M ? ld_stream(x + mn * ldx + (int64_t)kbn * GRP + l16 * 8) : zero;
         const uint4 bn = mn1 < M ? ld_stream(x + mn1 * ldx + (int64_t)kbn1 * GRP + l16 * 8) : zero;
+        if (kNorm) {
+            const uint4 ga = *reinterpret_cast<const uint4 *>(gamma + (int64_t)kb * GRP + l16 * 8);
+            const uint4 gb = *reinterpret_cast<const uint4 *>(gamma + (int64_t)kb1 * GRP + l16 * 8);
+            a = norm8(a, m < M ? rstd[m] : 0.0f, ga);
+            b = norm8(b, m1 < M ? rstd[m1] : 0.0f, gb);
+        }
         row_groups2(a, b, m < M, m1 < M, m, kb, m1, kb1, lane, q, ldq, s, lds);
         a = an;
         b = bn;
@@ -304,11 +338,14 @@ __device__ __forceinline__ void dual_row_codes(const uint16_t *tile, const Quot 
     }
 }
 
+template <bool kNorm>
 __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restrict__ x, int64_t M, int64_t ldx,
                                                     uint8_t *__restrict__ q, int64_t ldq,
                                                     float *__restrict__ s, int64_t lds,
                                                     uint8_t *__restrict__ qT, int64_t ldqT,
-                                                    float *__restrict__ sc, int64_t ldsc, int64_t MB, int64_t KB)
+                                                    float *__restrict__ sc, int64_t ldsc, int64_t MB, int64_t KB,
+                                                    const float *__restrict__ rstd,
+                                                    const uint16_t *__restrict__ gamma)
 {
     __shared__ __align__(16) uint16_t tile[GRP * TP];
     __shared__ __align__(16) uint32_t ccm[8][GRP / 2];  // per-warp column-pair maxima
@@ -329,9 +366,16 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
             const int r = hw16 + 16 * i;
             v[i] = (r < rows) ? ld_stream(x + (m0 + r) * ldx + kb * GRP + l16 * 8) : make_uint4(0, 0, 0, 0);
         }
+        uint4 g = make_uint4(0, 0, 0, 0);
+        if (kNorm)
+            g = *reinterpret_cast<const uint4 *>(gamma + kb * GRP + l16 * 8);
         uint32_t pm[8], cm[4];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
+            if (kNorm) {
+                const int r = hw16 + 16 * i;
+                v[i] = norm8(v[i], r < rows ? __ldg(rstd + m0 + r) : 0.0f, g);
+            }
             const uint32_t a0 = babs2(v[i].x), a1 = babs2(v[i].y), a2 = babs2(v[i].z), a3 = babs2(v[i].w);
             pm[i] = bmax2(bmax2(a0, a1), bmax2(a2, a3));
             if (i == 0) {
@@ -426,6 +470,80 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
             }
         }
         __syncthreads();  // tile, ccm and the column scales are reused by the next mb
+    }
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm row factor (QuRL notes, 关键设计 §1: the UAQ scale is folded into the
+// norm's weight, so the normalised activation is what the quantizers take):
+//   acc = sum of h[m,k]^2 over k in index order, by fused multiply-adds in fp32
+//   rstd[m] = fl32(1 / fl32(sqrt(fl32(fl32(acc / K) + eps))))
+// The index order makes the sum, and so every code downstream, independent of
+// the launch shape.  One thread owns one row and runs its chain of K FMAs; a
+// one-warp CTA stages 32 rows x 128 columns per step in shared memory (16-byte
+// cp.async copies, a ring RMS_STAGES deep so that enough bytes are in flight to
+// keep HBM busy while the chains run).  Row pitch 272 bytes: the 16-byte reads
+// of each quarter-warp fall in distinct bank groups.
+constexpr int RMS_ROWS = 32;
+constexpr int RMS_PITCH = GRP * 2 + 16;
+constexpr int RMS_STAGES = 6;
+constexpr int RMS_SMEM = RMS_STAGES * RMS_ROWS * RMS_PITCH;
+
+__device__ __forceinline__ void cp_async16_q(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__global__ void __launch_bounds__(RMS_ROWS) k_rms_rstd(const uint16_t *__restrict__ h, int64_t M, int64_t K,
+                                                       int64_t ldh, float eps, float *__restrict__ rstd)
+{
+    extern __shared__ __align__(16) uint8_t rms_buf[];
+    const int t = threadIdx.x;
+    const int64_t m0 = (int64_t)blockIdx.x * RMS_ROWS;
+    const int rows = (int)((M - m0) < RMS_ROWS ? (M - m0) : RMS_ROWS);
+    const int chunks = (int)(K / GRP);
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(rms_buf);
+    // chunk c of the CTA's rows into ring slot c % RMS_STAGES: 32 rows x 16 pieces
+    // of 16 bytes, thread t copying pieces t, t + 32, ...; rows beyond M read as 0
+    auto issue = [&](int c) {
+        if (c < chunks) {
+            const uint32_t slot = base + (uint32_t)((c % RMS_STAGES) * RMS_ROWS * RMS_PITCH);
+#pragma unroll 4
+            for (int i = t; i < RMS_ROWS * 16; i += RMS_ROWS) {
+                const int r = i >> 4, piece = i & 15;
+                const uint16_t *src = h + (m0 + r) * ldh + (int64_t)c * GRP + piece * 8;
+                cp_async16_q(slot + (uint32_t)(r * RMS_PITCH + piece * 16), r < rows ? src : h, r < rows ? 16u : 0u);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");  // one group per chunk, empty past the end
+    };
+#pragma unroll 1
+    for (int c = 0; c < RMS_STAGES - 1; ++c)
+        issue(c);
+    float acc = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < chunks; ++c) {
+        issue(c + RMS_STAGES - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(RMS_STAGES - 1) : "memory");  // chunk c has landed
+        __syncwarp();
+        const uint8_t *row = rms_buf + (c % RMS_STAGES) * RMS_ROWS * RMS_PITCH + t * RMS_PITCH;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * j);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = bf_lo(w[i]), hi = bf_hi(w[i]);
+                acc = __fmaf_rn(lo, lo, acc);
+                acc = __fmaf_rn(hi, hi, acc);
+            }
+        }
+        __syncwarp();  // every lane is done with the slot before it is refilled
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (t < rows) {
+        const float ms = __fdiv_rn(acc, (float)K);
+        rstd[m0 + t] = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
     }
 }
 
@@ -781,7 +899,7 @@ int sm_count()
 }  // namespace
 
 cudaError_t launch_quant_rows(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, int64_t ldq,
-                              float *s, int64_t lds, cudaStream_t st)
+                              float *s, int64_t lds, cudaStream_t st, const float *rstd, const uint16_t *gamma)
 {
     const int KB = (int)(K / GRP);
     const int64_t groups = M * KB;
@@ -792,17 +910,39 @@ cudaError_t launch_quant_rows(const uint16_t *x, int64_t M, int64_t K, int64_t l
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
-    k_quant_rows<<<(unsigned)blocks, 256, 0, st>>>(x, M, KB, ldx, q, ldq, s, lds);
+    if (rstd)
+        k_quant_rows<true><<<(unsigned)blocks, 256, 0, st>>>(x, M, KB, ldx, q, ldq, s, lds, rstd, gamma);
+    else
+        k_quant_rows<false><<<(unsigned)blocks, 256, 0, st>>>(x, M, KB, ldx, q, ldq, s, lds, nullptr, nullptr);
     return cudaGetLastError();
 }
 
 cudaError_t launch_quant_dual(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, int64_t ldq,
                               float *s, int64_t lds, uint8_t *qT, int64_t ldqT, float *sc, int64_t ldsc,
-                              cudaStream_t st)
+                              cudaStream_t st, const float *rstd, const uint16_t *gamma)
 {
     const int64_t MB = (M + GRP - 1) / GRP, KB = K / GRP;
     const dim3 grid((unsigned)(MB < 0x7FFFFFFF ? MB : 0x7FFFFFFF), (unsigned)(KB < 65535 ? KB : 65535));
-    k_quant_dual<<<grid, 256, 0, st>>>(x, M, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, MB, KB);
+    if (rstd)
+        k_quant_dual<true><<<grid, 256, 0, st>>>(x, M, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, MB, KB, rstd, gamma);
+    else
+        k_quant_dual<false><<<grid, 256, 0, st>>>(x, M, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, MB, KB, nullptr,
+                                                  nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rms_rstd(const uint16_t *h, int64_t M, int64_t K, int64_t ldh, float eps, float *rstd,
+                            cudaStream_t st)
+{
+    static bool attr = false;  // benign race: every thread sets the same value
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(k_rms_rstd, cudaFuncAttributeMaxDynamicSharedMemorySize, RMS_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        attr = true;
+    }
+    const int64_t blocks = (M + RMS_ROWS - 1) / RMS_ROWS;
+    k_rms_rstd<<<(unsigned)blocks, RMS_ROWS, RMS_SMEM, st>>>(h, M, K, ldh, eps, rstd);
     return cudaGetLastError();
 }
 

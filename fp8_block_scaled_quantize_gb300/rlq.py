@@ -26,6 +26,7 @@ _I = ctypes.c_int64
 _SIGS = {
     "rlq_quant_act_1x128": [_P, _I, _I, _I, _P, _I, _P, _I, _P, _I, _P, _I, _P],
     "rlq_quant_weight_128x128": [_P, _I, _I, _I, _P, _I, _P, _I, _P, _I, _P],
+    "rlq_rmsnorm_quant_act_1x128": [_P, _I, _I, _I, _P, ctypes.c_float, _P, _P, _I, _P, _I, _P, _I, _P, _I, _P],
     "rlq_gemm_fprop": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
     "rlq_gemm_dgrad": [_P, _I, _P, _I, _P, _I, ctypes.c_int, _P, _I, _P, _I, _I, _I, _I, _P],
     "rlq_gemm_wgrad": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P],
@@ -100,6 +101,11 @@ def _call(name: str, *args) -> int:
 
 def rlq_quant_act_1x128(x, M, K, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, stream):
     return _call("rlq_quant_act_1x128", x, M, K, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, stream)
+
+
+def rlq_rmsnorm_quant_act_1x128(h, M, K, ldh, gamma, eps, rstd, q, ldq, s, lds, qT, ldqT, sc, ldsc, stream):
+    return _call("rlq_rmsnorm_quant_act_1x128", h, M, K, ldh, gamma, eps, rstd, q, ldq, s, lds, qT, ldqT, sc, ldsc,
+                 stream)
 
 
 def rlq_quant_weight_128x128(w, N, K, ldw, q, ldq, s, lds, qT, ldqT, stream):
@@ -269,6 +275,31 @@ def quant_act_1x128(x: torch.Tensor, colwise: bool = False, stream=None):
                         _ptr(qT), _ld(qT) if qT is not None else 0, _ptr(sc), K if sc is not None else 0,
                         _stream(stream))
     return q, s, qT, sc
+
+
+def rmsnorm_quant_act_1x128(h: torch.Tensor, gamma: torch.Tensor, eps: float, colwise: bool = False, stream=None):
+    """RMSNorm of the bf16 hidden state h [M, K] with the (UAQ-folded) bf16 norm
+    weight gamma [K], quantized 1x128 (and with ``colwise`` 128x1) without
+    writing the normalised activation.
+
+    Returns (q, s, qT, sc) as ``quant_act_1x128`` and rstd [M] f32."""
+    if h.dtype != torch.bfloat16 or gamma.dtype != torch.bfloat16:
+        raise TypeError("h and gamma must be bfloat16")
+    M, K = h.shape
+    if gamma.shape != (K,) or not gamma.is_contiguous():
+        raise ValueError("gamma must be a contiguous [K] tensor")
+    dev = h.device
+    q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((K // GRP, M), dtype=torch.float32, device=dev)
+    rstd = torch.empty((max(M, 1),), dtype=torch.float32, device=dev)[:M]
+    qT = sc = None
+    if colwise:
+        qT = empty_codes_T(K, M, dev)
+        sc = torch.empty(((M + GRP - 1) // GRP, K), dtype=torch.float32, device=dev)
+    rlq_rmsnorm_quant_act_1x128(h.data_ptr(), M, K, _ld(h), gamma.data_ptr(), eps, rstd.data_ptr(), q.data_ptr(), K,
+                                s.data_ptr(), max(M, 1), _ptr(qT), _ld(qT) if qT is not None else 0, _ptr(sc),
+                                K if sc is not None else 0, _stream(stream))
+    return q, s, qT, sc, rstd
 
 
 def quant_weight_128x128(w: torch.Tensor, transposed: bool = False, stream=None):

@@ -84,6 +84,40 @@ rlq_status rlq_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t 
                                rlq_stream_t stream);
 
 /*
+ * RMSNorm fused with the activation quantization above, the UAQ scale carried
+ * by the norm weight.  QuRL notes, 关键设计 §1: the per-channel s that
+ * multiplies the previous activation can be folded straight into the norm's
+ * scale (gamma' = gamma * s: rlq_uaq_fold with prev = gamma, R = 1).  Jet-RL
+ * notes, 细粒度 GEMM 量化方案 / 实践建议: the forward activation is kept as its
+ * 1x128 (and, for WGrad, 128x1) FP8 codes.  This call reads the hidden state
+ * once from HBM, normalises it and quantizes the result, without writing the
+ * bf16 activation; its codes and scales are exactly those of rlq_quant_act_1x128
+ * applied to
+ *
+ *   x[m, k] = bf16_RN( fl32( fl32(h[m, k] * rstd[m]) * gamma[k] ) ),
+ *   rstd[m] = fl32( 1 / fl32(sqrt( fl32( fl32(acc_m / K) + eps ) )) ),
+ *   acc_m   = sum over k = 0 .. K-1, in index order, of h[m, k]^2 by fp32 fused
+ *             multiply-adds from 0 (the order makes the result independent of
+ *             the launch shape).
+ *
+ * The pages give no formula for the norm; this is the standard RMSNorm with
+ * every step in fp32 and one rounding to bf16.
+ *
+ *   h      bf16 [M, K], pitch ldh >= K                   (input, the hidden state)
+ *   gamma  bf16 [K], 16-byte aligned                     (input, the folded norm weight)
+ *   eps    finite, >= 0; a row of zeros with eps == 0 is outside the contract
+ *   rstd   f32 [M]                                        (output) rstd[m] above,
+ *          also read back by the call's second kernel
+ *   q, s, qT, ldqT, sc, ldsc: as in rlq_quant_act_1x128   (outputs)
+ * K % 128 == 0.  Two launches on `stream`: the row factors, then the quantizer.
+ */
+rlq_status rlq_rmsnorm_quant_act_1x128(const uint16_t *h, int64_t M, int64_t K, int64_t ldh,
+                                      const uint16_t *gamma, float eps, float *rstd,
+                                      uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                                      uint8_t *qT, int64_t ldqT, float *sc, int64_t ldsc,
+                                      rlq_stream_t stream);
+
+/*
  * Weight quantization, 128x128 blocks.  Jet-RL notes, "细粒度 GEMM 量化方案":
  * weights 128x128 per block; "系统实现": weights are quantized at the
  * parameter-update step.

@@ -69,6 +69,27 @@ def test_quant_act_validation():
     assert _status(q, None, 5, 0, 0, None, 0, None, 0, None, 0, None, 0, None) == 0
 
 
+def test_rmsnorm_quant_validation():
+    r = rlq.rlq_rmsnorm_quant_act_1x128
+    ok = (FAKE, 4, 128, 128, FAKE, 1e-6, FAKE, FAKE, 128, FAKE, 4, None, 0, None, 0, None)
+
+    def with_(i, v):
+        a = list(ok)
+        a[i] = v
+        return a
+
+    assert _status(r, *with_(2, 100)) == 2            # K % 128
+    assert _status(r, *with_(4, None)) == 1           # gamma NULL
+    assert _status(r, *with_(4, FAKE + 8)) == 3       # gamma not 16-byte aligned
+    assert _status(r, *with_(5, float("inf"))) == 1   # eps not finite
+    assert _status(r, *with_(5, -1.0)) == 1           # eps negative
+    assert _status(r, *with_(6, None)) == 1           # rstd NULL
+    assert _status(r, *with_(6, FAKE + 2)) == 3       # rstd alignment
+    assert _status(r, *with_(3, 64)) == 1             # ldh < K
+    assert _status(r, *with_(11, FAKE)) == 1          # qT without sc
+    assert _status(r, None, 0, 128, 128, None, 0.0, None, None, 0, None, 0, None, 0, None, 0, None) == 0
+
+
 def test_weight_and_fold_validation():
     w = rlq.rlq_quant_weight_128x128
     assert _status(w, FAKE, 100, 128, 128, FAKE, 128, FAKE, 1, None, 0, None) == 2
