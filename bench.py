@@ -7,7 +7,8 @@ workload (X bf16 [8192, 4096], W bf16 [14336, 4096], dY bf16 [8192, 14336]):
      (the channel scale alternates between s and 1/s so W stays stationary)
   2. fused 1x128 + 128x1 quantization of X
   3. fused 1x128 + 128x1 quantization of dY
-  4. 128x128 quantization of W, with the transposed copy for DGrad
+  4. 128x128 quantization of W (no transposed copy: DGrad reads the FProp codes
+     MN-major, as fast as the K-major copy and 58.7 MB of writes cheaper)
   5. FProp  Y  = X W^T
   6. DGrad  dX = dY W
   7. WGrad  dW = dY^T X
@@ -186,7 +187,6 @@ class Step:
         self.sdyc = torch.empty((M // 128, N), dtype=f32, device=dev)
         self.qw = torch.empty((N, K), dtype=u8, device=dev)
         self.sw = torch.empty((N // 128, K // 128), dtype=f32, device=dev)
-        self.qwT = torch.empty((K, N), dtype=u8, device=dev)
         self.y = torch.empty((M, N), dtype=bf, device=dev)
         self.dx = torch.empty((M, K), dtype=bf, device=dev)
         self.dw = torch.empty((N, K), dtype=bf, device=dev)
@@ -214,12 +214,12 @@ class Step:
                               self.qdyT.data_ptr(), M, self.sdyc.data_ptr(), N, stream)
         rec(3)
         r.rlq_quant_weight_128x128(self.w.data_ptr(), N, K, K, self.qw.data_ptr(), K, self.sw.data_ptr(), K // 128,
-                                   self.qwT.data_ptr(), N, stream)
+                                   None, 0, stream)
         rec(4)
         r.rlq_gemm_fprop(self.qx.data_ptr(), K, self.sx.data_ptr(), M, self.qw.data_ptr(), K, self.sw.data_ptr(),
                          K // 128, self.y.data_ptr(), N, M, N, K, stream)
         rec(5)
-        r.rlq_gemm_dgrad(self.qdy.data_ptr(), N, self.sdy.data_ptr(), M, self.qwT.data_ptr(), N, 1,
+        r.rlq_gemm_dgrad(self.qdy.data_ptr(), N, self.sdy.data_ptr(), M, self.qw.data_ptr(), K, 0,
                          self.sw.data_ptr(), K // 128, self.dx.data_ptr(), K, M, N, K, stream)
         rec(6)
         r.rlq_gemm_wgrad(self.qdyT.data_ptr(), M, self.sdyc.data_ptr(), N, self.qxT.data_ptr(), M,
@@ -238,7 +238,7 @@ def kernel_work():
         "uaq_fold": ("bytes", B_FOLD_W * N * K + 4 * K + 4 * K),
         "quant_dual_x": ("bytes", B_DUAL * M * K),
         "quant_dual_dy": ("bytes", B_DUAL * M * N),
-        "quant_weight_128x128": ("bytes", B_WEIGHT_T * N * K),
+        "quant_weight_128x128": ("bytes", B_WEIGHT * N * K),
         "gemm_fprop": ("flop", 2.0 * M * N * K),
         "gemm_dgrad": ("flop", 2.0 * M * N * K),
         "gemm_wgrad": ("flop", 2.0 * M * N * K),
@@ -573,7 +573,26 @@ def run_sweep(args):
     def gemm_bytes(Mr, Nc, L):
         return Mr * L + Nc * L + 2 * Mr * Nc + 4 * (Mr + Nc) * ((L + 127) // 128)
 
-    def linear(cfg, x, w, dy=None, s=None, full=False, per_channel=False, norm=False):
+    def nvfp4_gemm_row(cfg, x, w):
+        """NVFP4 weight-only GEMM (bf16 X, FP4 weights): bytes X + codes + block
+        scales + bf16 Y; bound by HBM or by the bf16 tensor rate."""
+        M, K = x.shape
+        N = w.shape[0]
+        q4, sb4, st4 = rlq.quant_nvfp4(w)
+        y4 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        nbytes = 2 * M * K + N * K // 2 + N * K // 16 + 2 * M * N
+        ms = _time_ms(lambda: rlq.gemm_nvfp4_weight_only(x, q4, sb4, st4, out=y4), flush)
+        flop = 2.0 * M * N * K
+        r = {"sweep": True, "config": cfg, "kernel": "gemm_nvfp4_weight_only", "ms": round(ms, 4),
+             "tflops": round(flop / (ms * 1e-3) / 1e12, 1), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        t_roof = max(flop / (peaks["bf16_burst"] * 1e12), nbytes / (bw * 1e9)) * 1e3
+        r["bound"] = "tensor (bf16)" if flop / (peaks["bf16_burst"] * 1e12) >= nbytes / (bw * 1e9) else "hbm"
+        r["frac_roofline"] = round(t_roof / ms, 3)
+        rows.append(r)
+        print(json.dumps(r), flush=True)
+        del q4, sb4, st4, y4
+
+    def linear(cfg, x, w, dy=None, s=None, full=False, per_channel=False, norm=False, nvfp4=False):
         """Time the quantizers, fold and GEMMs of one linear layer (with
         ``per_channel`` also the per-token / per-channel quantizers and FProp)."""
         M, K = x.shape
@@ -611,6 +630,8 @@ def run_sweep(args):
         emit(cfg, "quant_weight" + ("_t" if full else ""),
              _time_ms(lambda: rlq.quant_weight_128x128(w, transposed=full), flush),
              nbytes=(B_WEIGHT_T if full else B_WEIGHT) * N * K)
+        if nvfp4:
+            nvfp4_gemm_row(cfg, x, w)
         qx, sx, qxT, sxc = rlq.quant_act_1x128(x, colwise=full)
         qw, sw, qwT = rlq.quant_weight_128x128(w, transposed=full)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -649,6 +670,9 @@ def run_sweep(args):
             dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
             emit(cfg, "gemm_dgrad", _time_ms(lambda: rlq.gemm_dgrad(qdy, sdy, qwT, sw, out=dx), flush),
                  nbytes=gemm_bytes(M, K, N), flop=2.0 * M * N * K)
+            emit(cfg, "gemm_dgrad_mn",
+                 _time_ms(lambda: rlq.gemm_dgrad(qdy, sdy, qw, sw, transposed=False, out=dx), flush),
+                 nbytes=gemm_bytes(M, K, N), flop=2.0 * M * N * K)
             ws = _splitk_ws(rlq.GEMM_DGRAD, M, N, K)
             if ws is not None:
                 emit(cfg, "gemm_dgrad_splitk",
@@ -658,15 +682,13 @@ def run_sweep(args):
                  nbytes=gemm_bytes(N, K, M), flop=2.0 * M * N * K)
             if cfg.startswith("train_step_8b"):
                 emit(cfg, "quant_nvfp4_w", _time_ms(lambda: rlq.quant_nvfp4(w), flush), nbytes=2.5625 * N * K)
-                # fp32 accumulation (micro-batches): the operands, two fp32 planes written
-                # and read, and the fp32 gradient read and written
+                # fp32 accumulation (micro-batches): the operands, and the fp32 gradient
+                # read and written by the epilogue (no bf16 output)
                 acc = torch.zeros((N, K), dtype=torch.float32, device=dev)
-                wsa = torch.empty(max(2 * N * K * 4, rlq.rlq_gemm_splitk_workspace_bytes(rlq.GEMM_WGRAD, M, N, K)),
-                                  dtype=torch.uint8, device=dev)
                 emit(cfg, "gemm_wgrad_accumulate",
-                     _time_ms(lambda: rlq.gemm_wgrad_accumulate_(acc, qdyT, sdyc, qxT, sxc, workspace=wsa), flush),
-                     nbytes=gemm_bytes(N, K, M) - 2 * N * K + 16 * N * K + 8 * N * K, flop=2.0 * M * N * K)
-                del acc, wsa
+                     _time_ms(lambda: rlq.gemm_wgrad_accumulate_(acc, qdyT, sdyc, qxT, sxc), flush),
+                     nbytes=gemm_bytes(N, K, M) - 2 * N * K + 8 * N * K, flop=2.0 * M * N * K)
+                del acc
             ws = _splitk_ws(rlq.GEMM_WGRAD, M, N, K)
             if ws is not None:
                 emit(cfg, "gemm_wgrad_splitk",
@@ -683,7 +705,7 @@ def run_sweep(args):
     # decode up-projection, 8B shapes
     gen.manual_seed(1)
     linear("decode_upproj_8b M=256 N=14336 K=4096", _dev_normal(gen, (256, 4096), 1.0, 0.01, 20.0),
-           _dev_normal(gen, (14336, 4096), 0.02))
+           _dev_normal(gen, (14336, 4096), 0.02), nvfp4=True)
     # 8B training step
     gen.manual_seed(2)
     linear("train_step_8b M=8192 N=14336 K=4096", _dev_normal(gen, (8192, 4096), 1.0),
@@ -695,7 +717,7 @@ def run_sweep(args):
         s = np.random.default_rng(3).uniform(1.5, 4.0, K).astype(np.float32)
         for M in I.QWEN7B_M:
             linear(f"qwen7b_{which} M={M} N={N} K={K}", _dev_normal(gen, (M, K), 1.0, t_frac=0.01), w, s=s,
-                   per_channel=True, norm=(which == "gate_up"))
+                   per_channel=True, norm=(which == "gate_up"), nvfp4=True)
         del w
     # 32B sweep: all three passes per M
     gen.manual_seed(4)
@@ -704,7 +726,8 @@ def run_sweep(args):
         for M in I.SWEEP_32B_M:
             x = _dev_normal(gen, (M, K), 1.0, 0.005, 50.0)
             dy = _dev_normal(gen, (M, N), 1e-3)
-            linear(f"sweep_32b_{orient} M={M} N={N} K={K}", x, w, dy=dy, full=True, norm=(orient == "up"))
+            linear(f"sweep_32b_{orient} M={M} N={N} K={K}", x, w, dy=dy, full=True, norm=(orient == "up"),
+                   nvfp4=(M <= 1024))
             del x, dy
             torch.cuda.empty_cache()
         del w
@@ -721,7 +744,8 @@ def run_sweep(args):
 
 CASE_DOC = """Run one kernel of the path on one shape --case-reps times (after 2 warm-up
 calls), for profiler captures of a small case: gemm_fprop, gemm_dgrad,
-gemm_dgrad_mn (untransposed weight codes), gemm_wgrad (optionally --split-k), quant_rows, quant_dual,
+gemm_dgrad_mn (untransposed weight codes), gemm_wgrad (optionally --split-k), gemm_wgrad_accumulate,
+gemm_fprop_per_channel, gemm_nvfp4, quant_rows, quant_dual,
 rmsnorm_quant, rmsnorm_quant_dual, quant_weight, uaq_fold.  Prints the
 median CUDA-event time; no JSON line."""
 
@@ -743,6 +767,21 @@ def run_case(args):
         qw, sw, _ = rlq.quant_weight_128x128(w)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         fn = lambda: rlq.gemm_fprop(qx, sx, qw, sw, out=y, split_k=args.split_k)
+    elif name == "gemm_nvfp4":
+        q4, sb4, st4 = rlq.quant_nvfp4(w)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: rlq.gemm_nvfp4_weight_only(x, q4, sb4, st4, out=y)
+    elif name == "gemm_fprop_per_channel":
+        qx, _, sx = rlq.quant_per_row(x)
+        qw, _, sw = rlq.quant_per_row(w)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: rlq.gemm_fprop_per_channel(qx, sx, qw, sw, out=y, split_k=args.split_k)
+    elif name == "gemm_wgrad_accumulate":
+        dy = _dev_normal(gen, (M, N), 1e-3)
+        _, _, qxT, sxc = rlq.quant_act_1x128(x, colwise=True)
+        _, _, qdyT, sdyc = rlq.quant_act_1x128(dy, colwise=True)
+        acc = torch.zeros((N, K), dtype=torch.float32, device=dev)
+        fn = lambda: rlq.gemm_wgrad_accumulate_(acc, qdyT, sdyc, qxT, sxc)
     elif name in ("gemm_dgrad", "gemm_dgrad_mn", "gemm_wgrad"):
         dy = _dev_normal(gen, (M, N), 1e-3)
         qw, sw, qwT = rlq.quant_weight_128x128(w, transposed=True)

@@ -363,6 +363,7 @@ rlq_status gemm_fprop_per_channel(const uint8_t *xq, int64_t ldxq, const float *
     a.sb_bstride = ldws;
     a.sb_cstride = 0;
     a.per_col_sb = true;
+    a.scale_once = true;  // the scales are the same for every K-block: scale the whole sum once
     a.out = y;
     a.ldo = ldy;
     a.R = M;
@@ -448,15 +449,11 @@ rlq_status rlq_gemm_wgrad_accumulate(const uint8_t *dyqT, int64_t lddyqT, const 
     RLQ_REQUIRE(M < MAX_DIM && N < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
     if (N == 0 || K == 0 || M == 0)
         return RLQ_OK;  // nothing to add
-    RLQ_REQUIRE(M > G, RLQ_ERR_UNSUPPORTED, "M=%lld: accumulation needs more than one 128-token block", (long long)M);
     RLQ_REQUIRE(dw_acc, RLQ_ERR_INVALID_ARG, "dw_acc is NULL");
     RLQ_REQUIRE(ld_acc >= K, RLQ_ERR_INVALID_ARG, "dw_acc: pitch %lld < %lld", (long long)ld_acc, (long long)K);
     RLQ_REQUIRE(al(dw_acc, 16) && ld_acc % 4 == 0, RLQ_ERR_MISALIGNED,
                 "dw_acc rows must be 16-byte aligned (pointer 16-byte aligned, pitch a multiple of 4)");
     RLQ_TRY(check_workspace(workspace, workspace_bytes));
-    RLQ_REQUIRE(workspace && workspace_bytes >= 2 * N * K * 4, RLQ_ERR_INVALID_ARG,
-                "workspace of %lld bytes: accumulation needs at least 2 * N * K * 4 = %lld", (long long)workspace_bytes,
-                (long long)(2 * N * K * 4));
     RLQ_TRY(check_codes("dyqT", dyqT, lddyqT, M));
     RLQ_TRY(check_codes("xqT", xqT, ldxqT, M));
     RLQ_TRY(check_scales("dysc", dysc, lddysc, N));
@@ -474,10 +471,10 @@ rlq_status rlq_gemm_wgrad_accumulate(const uint8_t *dyqT, int64_t lddyqT, const 
     a.sb_bstride = ldxsc;
     a.sb_cstride = 0;
     a.per_col_sb = true;
-    // the kernel writes only fp32 partials in split mode; its bf16 output map is
-    // laid over the workspace so that it describes valid memory, and never written
-    a.out = static_cast<uint16_t *>(workspace);
-    a.ldo = K;
+    // the epilogue adds into dw_acc (or, where the split-K plan splits, writes
+    // fp32 partials that a reduction adds); no bf16 output
+    a.out = nullptr;
+    a.ldo = 0;
     a.R = N;
     a.C = K;
     a.L = M;
@@ -532,6 +529,28 @@ rlq_status rlq_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, const fl
     if (prev && R > 0)
         RLQ_TRY(check_bf16("prev", prev, ldp, K));
     return cuda_status(launch_uaq_fold(w, N, K, ldw, s, prev, R, ldp, cs(stream)), "UAQ fold launch");
+}
+
+rlq_status rlq_gemm_nvfp4_weight_only(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq,
+                                     const uint8_t *wsb, int64_t ldwsb, const float *wst, uint16_t *y, int64_t ldy,
+                                     int64_t M, int64_t N, int64_t K, rlq_stream_t stream)
+{
+    RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
+    RLQ_REQUIRE(N % G == 0 && K % 64 == 0, RLQ_ERR_UNSUPPORTED,
+                "N=%lld must be a multiple of 128 and K=%lld a multiple of 64", (long long)N, (long long)K);
+    RLQ_REQUIRE(M < MAX_DIM && N < MAX_DIM && K < MAX_DIM, RLQ_ERR_UNSUPPORTED, "dimension beyond 2^31");
+    if (M == 0 || N == 0)
+        return RLQ_OK;
+    RLQ_TRY(check_bf16("y", y, ldy, N));
+    if (K == 0)  // empty contraction: the sum is zero
+        return cuda_status(cudaMemset2DAsync(y, (size_t)ldy * 2, 0, (size_t)N * 2, (size_t)M, cs(stream)),
+                           "cudaMemset2DAsync (empty contraction)");
+    RLQ_TRY(check_bf16("x", x, ldx, K));
+    RLQ_TRY(check_codes("wq", wq, ldwq, K / 2));
+    RLQ_TRY(check_codes("wsb", wsb, ldwsb, K / 16));
+    RLQ_REQUIRE(wst, RLQ_ERR_INVALID_ARG, "wst is NULL");
+    RLQ_REQUIRE(al(wst, 4), RLQ_ERR_MISALIGNED, "wst is not 4-byte aligned");
+    return launch_gemm_nvfp4w(x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, cs(stream));
 }
 
 rlq_status rlq_aqn_sigma(float sigma_start, float sigma_end, int64_t t, int64_t T, float *sigma)

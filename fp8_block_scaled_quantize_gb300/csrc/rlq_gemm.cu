@@ -48,11 +48,9 @@
 #include <mutex>
 
 #include "rlq_internal.h"
+#include "rlq_tc.cuh"
 
 namespace rlq {
-
-// First error recorded on this device: bits 0..31 status code, 32..63 site.
-__device__ unsigned long long g_rlq_error_word;
 
 namespace {
 
@@ -68,26 +66,38 @@ constexpr int A_BYTES = BM * BK;           // 16 KB
 constexpr int NUM_THREADS = 384;
 constexpr int FIRST_EPI_WARP = 4;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int NUM_EPI_WARPS_C = NUM_EPI_WARPS;
 constexpr int REGS_PRODUCER = 40;
 constexpr int REGS_EPILOGUE = 232;
 constexpr int TMEM_COLS = 2 * BN;          // two partial buffers
-constexpr int STG_BYTES = NUM_EPI_WARPS_C * 2 * 32 * 128;  // output staging: per warp two 32x64 bf16 boxes
 constexpr int SCALE_SLOTS = 8;             // scale ring depth (contraction blocks)
 constexpr int SLOT_FLOATS = BM + BN;       // 128 row scales + up to 256 column scales
 constexpr int RING_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
 
 // Per-mode shared-memory plan.  Single CTA: the CTA holds the whole 256-row B tile
-// (48 KB stages, 3 of them).  CTA pair (cta_group::2): an output tile is 256 x 256,
-// each CTA holds its 128 rows of A and half of the B tile (32 KB stages, 4 of them);
-// the pair's MMA reads both halves of B, so each byte of B is staged in one SM only.
-// A single CTA (outputs of fewer than 256 rows, split-K) stores its rows straight to
-// global memory instead of through a staging tile: the 64 KB buys a fourth stage,
-// which decode-sized GEMMs, bound by the latency of streaming B from HBM, need.
+// (48 KB stages, 4 of them) and stores its output rows straight from registers
+// (outputs under 256 rows and split-K partials, where the contraction per tile is
+// long and the stores are a small share).  CTA pair (cta_group::2): an output tile
+// is 256 x 256, each CTA holds its 128 rows of A and half of the B tile (32 KB
+// stages); the pair's MMA reads both halves of B, so each byte of B is staged in
+// one SM only.  A pair's bf16 tile leaves through TMA stores from a per-warp
+// staging buffer of 32 rows x RLQ_STG_COLS columns (coalesced and asynchronous:
+// the epilogue moves on while the copy drains); the rest of the shared memory
+// goes to pipeline stages, whose depth keeps enough operand bytes in flight to
+// cover the L2 / HBM latency.
+#ifndef RLQ_PAIR_STAGES
+#define RLQ_PAIR_STAGES 4
+#endif
+#ifndef RLQ_STG_COLS
+#define RLQ_STG_COLS 64
+#endif
+constexpr int STG_COLS = RLQ_STG_COLS;            // bf16 columns per staged store round (64 or 128)
+constexpr int STG_WARP_BYTES = 32 * STG_COLS * 2;  // one warp's staging buffer
+static_assert(STG_COLS == 64 || STG_COLS == 128, "staged rounds of 64 or 128 columns");
+
 template <bool kPair>
 struct Cfg {
-    static constexpr int STAGES = 4;
-    static constexpr int STAGING = kPair ? STG_BYTES : 0;  // output staging (TMA stores)
+    static constexpr int STAGES = kPair ? RLQ_PAIR_STAGES : 4;
+    static constexpr int STAGING = kPair ? NUM_EPI_WARPS * STG_WARP_BYTES : 0;
     static constexpr int B_ROWS = kPair ? BN / 2 : BN;  // B rows (output columns) staged per CTA
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -105,183 +115,6 @@ struct Cfg {
 };
 
 
-// Error sites (reported by rlq_check / rlq_last_error).
-enum : uint32_t {
-    SITE_PRODUCER_EMPTY = 1,
-    SITE_MMA_TMEM_EMPTY = 2,
-    SITE_MMA_FULL = 3,
-    SITE_EPI_TMEM_FULL = 4,
-    SITE_TEARDOWN = 5,
-    SITE_DRAIN = 6,
-    SITE_SCALE_EMPTY = 7,
-    SITE_EPI_SCALE_FULL = 8,
-    SITE_DIAG = 99,
-};
-
-// ------------------------------------------------------------ PTX helpers ---
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// As mbar_try_wait, but the thread may be suspended in hardware for up to
-// SUSPEND_NS while the phase is incomplete; it resumes as soon as the phase
-// completes.  Waiting warps then cost no issue slots.
-constexpr uint32_t SUSPEND_NS = 20000;
-
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "n"(SUSPEND_NS)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void record_error(uint32_t code, uint32_t site)
-{
-    atomicCAS(&g_rlq_error_word, 0ull, ((unsigned long long)site << 32) | code);
-}
-
-// Waits for the phase of `bar` with the given parity.  Returns false, without
-// waiting further, once the CTA's abort flag is up or after limit_ns; in the
-// second case it records a timeout and raises the flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                       uint64_t limit_ns, uint32_t site)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait_sleep(bar, parity))
-            return true;
-        if ((i & 3) == 0) {
-            if (*abort_flag)
-                return false;
-            if (global_timer_ns() - t0 > limit_ns) {
-                record_error(RLQ_ERR_TIMEOUT, site);
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
-        ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
-// 4-byte global -> shared copy; src_bytes = 0 writes zero without reading.
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-
-// 16-byte global -> shared copy (both addresses 16-byte aligned); src_bytes = 0 writes zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-
-// Arrive on `bar` once this thread's earlier cp.async copies have landed.
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// TMA store of a box from shared memory, tracked by the issuing thread's bulk group.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y)
-{
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
-                 ::"l"((uint64_t)map), "r"(src), "r"(x), "r"(y)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z)
-{
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
-                 ::"l"((uint64_t)map), "r"(src), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
-// Pair forms.  The load lands in this CTA's shared memory and completes its bytes
-// on `bar`, a barrier of either CTA of the pair (a shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%3, %4}], [%2];"
-        ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
-// shared::cluster address of the variable at shared::cta address `a` in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-    return r;
-}
-
-// Arrive on a barrier of either CTA of the cluster (default .release.cta semantics:
-// the signal orders completed work, here TMEM loads finished by tcgen05.wait::ld;
-// a .release.cluster arrive measured 2.3x slower GEMMs).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar)
-{
-    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
-}
-
-__device__ __forceinline__ uint32_t cta_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 // First row, within a tile, of the rows this CTA owns.
 template <bool kPair>
 __device__ __forceinline__ int row_offset()
@@ -289,112 +122,6 @@ __device__ __forceinline__ int row_offset()
     if constexpr (kPair)
         return (int)cta_rank() * BM;
     return 0;
-}
-
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
-{
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// One tcgen05.mma: the CTA's own 128-row tile, or (kPair) the pair's 256-row tile,
-// issued by the even CTA and reading A and B from both CTAs' shared memory.
-template <bool kPair>
-__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate)
-{
-    if constexpr (kPair) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-            : "memory");
-    }
-}
-
-// Commit this thread's earlier MMAs to the barrier at shared::cta offset `bar`:
-// the own CTA's barrier, or (kPair) the barrier at that offset in both CTAs.
-template <bool kPair>
-__device__ __forceinline__ void tc_commit_t(uint32_t bar)
-{
-    if constexpr (kPair) {
-        const uint16_t mask = 0x3;
-        asm volatile(
-            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-            ::"r"(bar), "h"(mask)
-            : "memory");
-    } else {
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                     : "memory");
-    }
-}
-
-// Issues a load of 32 consecutive fp32 columns of this warp's 32 TMEM lanes
-// into r; the registers are valid only after tmem_wait32(r).
-__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-}
-
-// Waits for the outstanding TMEM loads.  The registers of r are tied to the
-// wait as in/out operands so that no use of them is scheduled before it.
-__device__ __forceinline__ void tmem_wait32(uint32_t (&r)[32])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
-                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-                 :
-                 : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row core-matrix groups 1024 bytes apart (SBO), version 1.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
-{
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// MN-major operand (the MN index contiguous), 128-byte swizzle: each atom is
-// 128 MN elements (bytes) x 8 contraction rows (1024 bytes); contraction rows
-// are 128 bytes apart, 8-row groups 1024 bytes apart (SBO), and the second
-// 128-wide MN atom of a 256-wide tile sits 16 KB further (LBO).
-__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr)
-{
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(16384 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
 // Explicit shared-memory loads: the aligned dynamic-smem base is computed through
@@ -412,6 +139,21 @@ __device__ __forceinline__ float4 lds_v4(uint32_t a)
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
     return v;
+}
+
+// The warp has read its part of a TMEM buffer (every tcgen05.ld waited for):
+// signal the MMA warp that may overwrite it, on the issuing CTA's barrier.
+template <bool kPair>
+__device__ __forceinline__ void release_tmem(uint32_t tempty, int lane)
+{
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+        if constexpr (kPair)
+            mbar_arrive_cluster(cluster_addr(tempty, 0));
+        else
+            mbar_arrive(tempty);
+    }
 }
 
 __device__ __forceinline__ float2 f2_of(uint32_t lo, uint32_t hi)
@@ -455,15 +197,18 @@ struct Params {
     const float *sb;
     int64_t sb_bstride;
     int64_t sb_cstride;
-    uint16_t *out;
+    int out_mode;     // OUT_BF16, OUT_F32_PARTIAL (split-K) or OUT_F32_ACC
+    uint16_t *out;    // OUT_BF16
     int64_t ldo;
+    float *acc_out;   // OUT_F32_ACC: acc_out[r * ld_acc + c] += the product
+    int64_t ld_acc;
     int R, C;
     int kblocks;
     int m_tiles, n_tiles, num_tiles;
     int m_fastest;
     // split-K: unit u covers tile u / splits and contraction blocks
     // [(u % splits) * kbps, min(kblocks, ... + kbps)); with splits > 1 the
-    // epilogue writes fp32 partials to the workspace ws [splits][R][C]
+    // epilogue writes fp32 partials (OUT_F32_PARTIAL) to the workspace ws [splits][R][C]
     int splits, kbps, num_units;
     float *ws;
     uint64_t timeout_ns;
@@ -499,16 +244,29 @@ __device__ __forceinline__ Unit unit_of(const Params &p, int u)
     return w;
 }
 
-template <bool kColScaleB, bool kBMajorMN, bool kPair>
+// Promotion modes.
+//   MODE_BLOCK:  sb is one scale per (contraction block, 128 output columns):
+//                FProp and DGrad, acc += P_b * (sa * sb).
+//   MODE_COLS:   sb is one scale per (contraction block, output column): WGrad,
+//                acc += P_b * (sa * sb[c]).
+//   MODE_ONCE:   sa and sb are constant along the contraction (per-token x
+//                per-channel FProp): the MMAs accumulate the whole contraction
+//                range in TMEM and the epilogue scales once, out = P * (sa * sb[c]).
+enum : int { MODE_BLOCK = 0, MODE_COLS = 1, MODE_ONCE = 2 };
+
+// Epilogue outputs.
+enum : int { OUT_BF16 = 0, OUT_F32_PARTIAL = 1, OUT_F32_ACC = 2 };
+
+template <int kMode, bool kBMajorMN, bool kPair>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_block_scaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmWs,
-                        const Params p)
+                        const __grid_constant__ CUtensorMap tmOut, const Params p)
 {
     using Cf = Cfg<kPair>;
     constexpr int STAGES = Cf::STAGES;
     constexpr int STAGE_BYTES = Cf::STAGE_BYTES;
     constexpr int NUM_BARS = Cf::NUM_BARS;
+    constexpr bool kOnce = kMode == MODE_ONCE;
     // A CTA pair (cluster of 2) shares one 256-row tile: CTA `rank` owns rows
     // rank * 128 .. rank * 128 + 127 of it; the even CTA issues the pair's MMAs.
     // (The rank is re-read where it is used rather than kept in a register.)
@@ -572,9 +330,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
-        prefetch_tmap(&tmOut);
-        if (p.splits > 1)
-            prefetch_tmap(&tmWs);
+        if (kPair && p.out_mode == OUT_BF16)
+            prefetch_tmap(&tmOut);
     }
     tc_fence_before();
     __syncthreads();
@@ -654,24 +411,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------- MMA issuers ---
-        // Warp 1 issues the even contraction blocks (TMEM buffer 0), warp 3 the odd
-        // ones (buffer 1): one thread's issue latency overlaps the other's MMAs.
-        // (A pair's MMAs are issued by the even CTA only.)
+        // Per-block promotion: warp 1 issues the even contraction blocks (TMEM
+        // buffer 0), warp 3 the odd ones (buffer 1), so that one thread's issue
+        // latency overlaps the other's MMAs.  Scale-once: warp 1 issues every block
+        // of a unit into the unit's buffer (units alternate between the buffers),
+        // accumulating across the contraction.  (A pair's MMAs are issued by the
+        // even CTA only.)
         const int parity = warp == 1 ? 0 : 1;
-        if (lane == 0 && (!kPair || cta_rank() == 0)) {
-            int it = 0;
+        if (lane == 0 && (!kPair || cta_rank() == 0) && (!kOnce || warp == 1)) {
+            int it = 0, uc = 0;
             bool ok = true;
-            for (int u = unit0; ok && u < p.num_units; u += unit_step) {
+            for (int u = unit0; ok && u < p.num_units; u += unit_step, ++uc) {
                 const Unit w = unit_of(p, u);
+                if (kOnce) {
+                    const uint32_t bph = (uint32_t)(uc >> 1) & 1u;
+                    if (!mbar_wait(tempty_bar(uc & 1), bph ^ 1u, abort_flag, p.timeout_ns, SITE_MMA_TMEM_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-                    if ((it & 1) != parity)
+                    if (!kOnce && (it & 1) != parity)
                         continue;
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                    const int buf = it & 1;
-                    const uint32_t bph = (uint32_t)(it >> 1) & 1u;
-                    if (!mbar_wait(tempty_bar(buf), bph ^ 1u, abort_flag, p.timeout_ns, SITE_MMA_TMEM_EMPTY) ||
-                        !mbar_wait(full_bar(s), ph, abort_flag, p.timeout_ns, SITE_MMA_FULL)) {
+                    const int buf = kOnce ? (uc & 1) : (it & 1);
+                    if (!kOnce) {
+                        const uint32_t bph = (uint32_t)(it >> 1) & 1u;
+                        if (!mbar_wait(tempty_bar(buf), bph ^ 1u, abort_flag, p.timeout_ns, SITE_MMA_TMEM_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!mbar_wait(full_bar(s), ph, abort_flag, p.timeout_ns, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
@@ -679,31 +451,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t d = tmem_base + (uint32_t)(buf * BN);
                     const uint64_t ad = sw128_desc(a_stage(s));
                     const uint64_t bd = kBMajorMN ? sw128_desc_mn(b_stage(s)) : sw128_desc(b_stage(s));
+                    const bool first = !kOnce || kb == w.kb0;
 #pragma unroll
                     for (int j = 0; j < BK / UMMA_K; ++j) {
                         // K-major: +32 bytes along K (+2 in the address field); MN-major:
                         // +32 contraction rows of 128 bytes (+256)
                         const uint64_t bj = kBMajorMN ? bd + (uint64_t)(256 * j) : bd + 2 * j;
-                        tc_mma_f8<kPair>(d, ad + 2 * j, bj, kBMajorMN ? Cf::IDESC_BMN : Cf::IDESC_BK, j > 0 ? 1u : 0u);
+                        tc_mma_f8<kPair>(d, ad + 2 * j, bj, kBMajorMN ? Cf::IDESC_BMN : Cf::IDESC_BK,
+                                         (first && j == 0) ? 0u : 1u);
                     }
                     // (pair: arrives on the barrier at this offset in both CTAs)
                     tc_commit_t<kPair>(empty_bar(s));
-                    tc_commit_t<kPair>(tfull_bar(buf));
+                    if (!kOnce || kb + 1 == w.kb1)
+                        tc_commit_t<kPair>(tfull_bar(buf));
                 }
             }
-            // every MMA issued above has completed once this commit arrives
+        }
+        if (lane == 0 && (!kPair || cta_rank() == 0)) {
+            // every MMA this thread issued has completed once this commit arrives
             tc_commit_t<kPair>(teardown_bar);
             volatile uint32_t never = 0;
             mbar_wait(teardown_bar, 0, &never, 20000000ull, SITE_TEARDOWN);
         }
     } else if (warp == 2) {
         // ------------------------------------------------ scale loader ---
+        // One ring slot per contraction block (scale-once: per unit, read at the
+        // unit's first block, the scales being the same for every block).
         int it = 0;
         bool ok = true;
         for (int u = unit0; ok && u < p.num_units; u += unit_step) {
             const Unit w = unit_of(p, u);
             const int mt = w.mt, nt = w.nt;
-            for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+            for (int kb = w.kb0; kb < (kOnce ? w.kb0 + 1 : w.kb1); ++kb, ++it) {
                 const int k = it % SCALE_SLOTS;
                 const uint32_t ph = (uint32_t)(it / SCALE_SLOTS) & 1u;
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(sempty_bar(k), ph ^ 1u, abort_flag, p.timeout_ns,
@@ -718,7 +497,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int r = mt * Cf::TILE_M + row_offset<kPair>() + lane + 32 * j;
                     cp_async4(slot + 4u * (lane + 32 * j), r < p.R ? sa_row + r : sa_row, r < p.R ? 4u : 0u);
                 }
-                if (kColScaleB) {
+                if (kMode != MODE_BLOCK) {
                     const float *sb_row = p.sb + (int64_t)kb * p.sb_bstride;
                     // 256 column scales as 64 aligned 16-byte pieces (rows of sb are 16-byte
                     // aligned, C % 128 == 0: a piece is wholly inside or outside the tensor)
@@ -744,9 +523,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int h = (warp - FIRST_EPI_WARP) >> 2;  // column half of the tile
         const int row = q * 32 + lane;               // tile row = TMEM lane
 
-        int it = 0;
+        int it = 0, uc = 0;
         bool ok = true;
-        for (int u = unit0; ok && u < p.num_units; u += unit_step) {
+        for (int u = unit0; ok && u < p.num_units; u += unit_step, ++uc) {
             const Unit wu = unit_of(p, u);
             const int mt = wu.mt, nt = wu.nt;
             const int col0 = nt * BN + h * 128;
@@ -755,9 +534,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 64; ++j)
                 acc[j] = make_float2(0.0f, 0.0f);
-            for (int kb = wu.kb0; kb < wu.kb1; ++kb, ++it) {
-                const int buf = it & 1;
-                const uint32_t bph = (uint32_t)(it >> 1) & 1u;
+            for (int kb = wu.kb0; kb < (kOnce ? wu.kb0 + 1 : wu.kb1); ++kb, ++it) {
+                const int buf = kOnce ? (uc & 1) : (it & 1);
+                const uint32_t bph = kOnce ? ((uint32_t)(uc >> 1) & 1u) : ((uint32_t)(it >> 1) & 1u);
                 const int k = it % SCALE_SLOTS;
                 // every lane acquires the scales and the partial itself; the
                 // decision is warp-uniform because tcgen05.ld is .sync.aligned
@@ -773,7 +552,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float sa = lds_f32(slot + 4u * row);
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
                 uint32_t ra[32], rb[32];
-                if (!kColScaleB) {
+                if (kMode == MODE_BLOCK) {
                     const float scl = sa * lds_f32(slot + 4u * (BM + h));
                     const float2 scl2 = make_float2(scl, scl);
                     tmem_ld32_async(taddr, ra);
@@ -788,7 +567,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     promote_chunk(&acc[32], ra, scl2);
                     tmem_wait32(rb);
                     promote_chunk(&acc[48], rb, scl2);
+                    release_tmem<kPair>(tempty_bar(buf), lane);
                 } else {
+                    // MODE_COLS: acc += P * (sa * sb[c]); MODE_ONCE: the same product
+                    // into a zero accumulator, once per unit
                     const uint32_t sbs = slot + 4u * (BM + h * 128);
                     const float2 sa2v = make_float2(sa, sa);
                     tmem_ld32_async(taddr, ra);
@@ -802,98 +584,86 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld32_async(taddr + 96, rb);
                     promote_chunk_cols(&acc[32], ra, sa2v, sbs + 256);
                     tmem_wait32(rb);
+                    // column-scaled: released before the last chunk's FMAs (registers only);
+                    // a same-box A/B measured this 1% faster for WGrad but 8% slower for the
+                    // block-scaled mode above, which releases after them
+                    release_tmem<kPair>(tempty_bar(buf), lane);
                     promote_chunk_cols(&acc[48], rb, sa2v, sbs + 384);
                 }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    if constexpr (kPair)
-                        mbar_arrive_cluster(cluster_addr(tempty_bar(buf), 0));  // the issuing CTA's barrier
-                    else
-                        mbar_arrive(tempty_bar(buf));
-                    mbar_arrive(sempty_bar(k));
-                }
+                if (lane == 0)
+                    mbar_arrive(sempty_bar(k));  // the scales are read
             }
-            if (!kPair) {
-                // single CTA: this thread's row, 128 columns, stored directly (512 or
-                // 256 contiguous bytes per thread); rows beyond R are skipped
-                const int grow = mt * BM + row;
-                if (ok && half_ok && grow < p.R) {
-                    if (p.splits > 1) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)wu.split * p.R + grow) * p.C + col0);
+            if (kPair && p.out_mode == OUT_BF16) {
+                // this warp's 32 rows x 128 columns in rounds of STG_COLS columns: each
+                // round is staged as 32 rows of STG_COLS * 2 bytes (16-byte chunks
+                // XOR-swizzled by row % 8, the tensor map's 128-byte swizzle; a 64-column
+                // round is one 128-byte box row) and leaves by TMA stores; rows beyond R
+                // are clipped by the tensor map
+                const uint32_t stg = smem_u32(staging) + (uint32_t)((warp - FIRST_EPI_WARP) * STG_WARP_BYTES);
+                const int y = mt * Cf::TILE_M + row_offset<kPair>() + q * 32;
 #pragma unroll
-                        for (int v = 0; v < 32; ++v)
-                            dst[v] = make_float4(acc[2 * v].x, acc[2 * v].y, acc[2 * v + 1].x, acc[2 * v + 1].y);
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (int64_t)grow * p.ldo + col0);
-#pragma unroll
-                        for (int v = 0; v < 16; ++v)
-                            dst[v] = make_uint4(bf16x2_rn(acc[4 * v]), bf16x2_rn(acc[4 * v + 1]),
-                                                bf16x2_rn(acc[4 * v + 2]), bf16x2_rn(acc[4 * v + 3]));
-                    }
-                }
-            } else if (ok && p.splits > 1) {
-                // fp32 partial of this contraction range into plane `split` of the
-                // workspace [splits][R][C] (reduced by k_splitk_reduce): two rounds
-                // of two 32x32 boxes (rows of 128 bytes, swizzled as below)
-                const uint32_t stg = smem_u32(staging) + (uint32_t)((warp - FIRST_EPI_WARP) * 2 * 32 * 128);
-#pragma unroll
-                for (int rd = 0; rd < 2; ++rd) {
+                for (int rd = 0; rd < 128 / STG_COLS; ++rd) {
                     if (lane == 0)
-                        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // buffer read out
                     __syncwarp();
 #pragma unroll
-                    for (int v = 0; v < 16; ++v) {
+                    for (int v = 0; v < STG_COLS / 8; ++v) {
+                        const int j = rd * (STG_COLS / 2) + 4 * v;  // acc pairs of columns 8v .. 8v + 7
                         const uint32_t addr = stg + (uint32_t)((v >> 3) * 32 * 128 + lane * 128 +
-                                                               ((((v & 7) ^ (lane & 7))) << 4));
-                        const int j = rd * 32 + 2 * v;  // columns 2j .. 2j+3 of this half
-                        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(acc[j].x), "f"(acc[j].y)
-                                     : "memory");
-                        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr + 8), "f"(acc[j + 1].x),
-                                     "f"(acc[j + 1].y)
-                                     : "memory");
+                                                               (((v & 7) ^ (lane & 7)) << 4));
+                        if (ok)
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                         "r"(bf16x2_rn(acc[j])), "r"(bf16x2_rn(acc[j + 1])),
+                                         "r"(bf16x2_rn(acc[j + 2])), "r"(bf16x2_rn(acc[j + 3]))
+                                         : "memory");
                     }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> TMA reads
                     __syncwarp();
-                    if (lane == 0 && half_ok) {
-                        const int y = mt * Cf::TILE_M + row_offset<kPair>() + q * 32;
-                        tma_store_3d(&tmWs, stg, col0 + rd * 64, y, wu.split);
-                        tma_store_3d(&tmWs, stg + 32 * 128, col0 + rd * 64 + 32, y, wu.split);
+                    if (lane == 0 && ok && half_ok) {
+                        tma_store_2d(&tmOut, stg, col0 + rd * STG_COLS, y);
+                        if (STG_COLS == 128)
+                            tma_store_2d(&tmOut, stg + 32 * 128, col0 + rd * STG_COLS + 64, y);
                         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                     }
                 }
-            } else if (ok) {
-                // this warp's 32 rows x 128 columns: two 32x64 boxes, rows of
-                // 128 bytes with the 16-byte chunks XOR-swizzled by (row % 8)
-                const uint32_t stg = smem_u32(staging) + (uint32_t)((warp - FIRST_EPI_WARP) * 2 * 32 * 128);
-                if (lane == 0)
-                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // previous tile's boxes read
-                __syncwarp();
+                continue;
+            }
+            // This thread's row, 128 columns, stored directly (512 or 256 contiguous
+            // bytes per thread); rows beyond R are skipped.
+            const int grow = mt * Cf::TILE_M + row_offset<kPair>() + row;
+            if (ok && half_ok && grow < p.R) {
+                if (p.out_mode == OUT_F32_PARTIAL) {
+                    // fp32 partial of this contraction range, plane `split` of [splits][R][C]
+                    float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)wu.split * p.R + grow) * p.C + col0);
 #pragma unroll
-                for (int v = 0; v < 16; ++v) {
-                    const uint32_t addr = stg + (uint32_t)((v >> 3) * 32 * 128 + lane * 128 +
-                                                           ((((v & 7) ^ (lane & 7))) << 4));
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                                 "r"(bf16x2_rn(acc[4 * v])), "r"(bf16x2_rn(acc[4 * v + 1])),
-                                 "r"(bf16x2_rn(acc[4 * v + 2])), "r"(bf16x2_rn(acc[4 * v + 3]))
-                                 : "memory");
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> TMA reads
-                __syncwarp();
-                if (lane == 0 && half_ok) {
-                    // rows beyond R are clipped by the tensor map
-                    const int y = mt * Cf::TILE_M + row_offset<kPair>() + q * 32;
-                    tma_store_2d(&tmOut, stg, col0, y);
-                    tma_store_2d(&tmOut, stg + 32 * 128, col0 + 64, y);
-                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    for (int v = 0; v < 32; ++v)
+                        dst[v] = make_float4(acc[2 * v].x, acc[2 * v].y, acc[2 * v + 1].x, acc[2 * v + 1].y);
+                } else if (p.out_mode == OUT_F32_ACC) {
+                    // acc_out[r, c] += the product, in fp32 (each element owned by this thread)
+                    float4 *dst = reinterpret_cast<float4 *>(p.acc_out + (int64_t)grow * p.ld_acc + col0);
+#pragma unroll
+                    for (int v = 0; v < 32; ++v) {
+                        float4 o = dst[v];
+                        o.x += acc[2 * v].x;
+                        o.y += acc[2 * v].y;
+                        o.z += acc[2 * v + 1].x;
+                        o.w += acc[2 * v + 1].y;
+                        dst[v] = o;
+                    }
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (int64_t)grow * p.ldo + col0);
+#pragma unroll
+                    for (int v = 0; v < 16; ++v)
+                        dst[v] = make_uint4(bf16x2_rn(acc[4 * v]), bf16x2_rn(acc[4 * v + 1]),
+                                            bf16x2_rn(acc[4 * v + 2]), bf16x2_rn(acc[4 * v + 3]));
                 }
             }
         }
-        if (lane == 0)
-            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // stores complete before exit
-        __syncwarp();
     }
 
+    if (kPair && warp >= FIRST_EPI_WARP && lane == 0)
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // stores complete before exit
     tc_fence_before();
     __syncthreads();
     if constexpr (kPair) {
@@ -1030,24 +800,6 @@ rlq_status encode_out_map(CUtensorMap *map, uint16_t *base, int64_t cols, int64_
     return RLQ_OK;
 }
 
-// fp32 split-K workspace [splits][rows][cols], dense; box 32 columns x 32 rows x 1, 128-byte swizzle.
-rlq_status encode_ws_map(CUtensorMap *map, float *base, int64_t cols, int64_t rows, int splits)
-{
-    auto enc = get_encode_fn();
-    if (!enc)
-        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)splits};
-    const cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)(cols * rows * 4)};
-    const cuuint32_t box[3] = {32, 32, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for the split-K workspace", (int)r);
-    return RLQ_OK;
-}
-
 // 2-D E4M3 tensor [rows][inner] with row pitch `ld` bytes; box 128 x box_rows.
 rlq_status encode_map(CUtensorMap *map, const uint8_t *base, int64_t inner, int64_t rows, int64_t ld, int box_rows)
 {
@@ -1069,8 +821,8 @@ rlq_status encode_map(CUtensorMap *map, const uint8_t *base, int64_t inner, int6
 
 struct DevInfo {
     int sms = 0;
-    bool attr_set[8] = {};
-    int max_clusters[8] = {};  // co-resident CTA pairs of each paired variant (0: not yet known, -1: none)
+    bool attr_set[16] = {};
+    int max_clusters[16] = {};  // co-resident CTA pairs of each paired variant (0: not yet known, -1: none)
 };
 
 DevInfo &dev_info(int dev)
@@ -1141,7 +893,7 @@ bool pair_mode_enabled()
     return on;
 }
 
-template <bool kCol, bool kBMN, bool kPair>
+template <int kMode, bool kBMN, bool kPair>
 rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool withhold_first_load = false)
 {
     using Cf = Cfg<kPair>;
@@ -1154,16 +906,13 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
     rs = kBMN ? encode_map(&tmB, a.B, a.C, a.L, a.ldb, BK) : encode_map(&tmB, a.B, a.L, a.C, a.ldb, Cf::B_ROWS);
     if (rs != RLQ_OK)
         return rs;
-    rs = encode_out_map(&tmO, a.out, a.C, a.R, a.ldo);
-    if (rs != RLQ_OK)
-        return rs;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return cuda_status(e, "cudaGetDevice");
     DevInfo &di = dev_info(dev);
-    const int variant = (kCol ? 1 : 0) + (kBMN ? 2 : 0) + (kPair ? 4 : 0);
-    auto kernel = k_gemm_block_scaled<kCol, kBMN, kPair>;
+    const int variant = kMode * 4 + (kBMN ? 2 : 0) + (kPair ? 1 : 0);
+    auto kernel = k_gemm_block_scaled<kMode, kBMN, kPair>;
     if (!di.attr_set[variant]) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
         if (e != cudaSuccess)
@@ -1191,7 +940,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
             di.max_clusters[variant] = n < 1 ? -1 : n;  // -1: no pair fits, use single CTAs
         }
         if (di.max_clusters[variant] < 0)
-            return launch_impl<kCol, kBMN, false>(a, splits, st, withhold_first_load);
+            return launch_impl<kMode, kBMN, false>(a, splits, st, withhold_first_load);
     }
     Params p;
     p.sa = a.sa;
@@ -1201,6 +950,8 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
     p.sb_cstride = a.sb_cstride;
     p.out = a.out;
     p.ldo = a.ldo;
+    p.acc_out = a.acc;
+    p.ld_acc = a.ld_acc;
     p.R = (int)a.R;
     p.C = (int)a.C;
     p.kblocks = (int)((a.L + BK - 1) / BK);
@@ -1215,11 +966,13 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
     p.splits = (p.kblocks + p.kbps - 1) / p.kbps;
     p.num_units = p.num_tiles * p.splits;
     p.ws = p.splits > 1 ? a.ws : nullptr;
-    CUtensorMap tmW = tmO;  // not read with one split
-    if (p.splits > 1) {
-        rs = encode_ws_map(&tmW, a.ws, a.C, a.R, p.splits);
+    p.out_mode = p.splits > 1 ? OUT_F32_PARTIAL : (a.acc ? OUT_F32_ACC : OUT_BF16);
+    if (kPair && p.out_mode == OUT_BF16) {
+        rs = encode_out_map(&tmO, a.out, a.C, a.R, a.ldo);
         if (rs != RLQ_OK)
             return rs;
+    } else {
+        tmO = tmA;  // not read
     }
     if (kPair) {
         const int pairs = p.num_units < di.max_clusters[variant] ? p.num_units : di.max_clusters[variant];
@@ -1227,7 +980,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
     } else {
         cfg.gridDim = dim3(p.num_units < di.sms ? p.num_units : di.sms, 1, 1);
     }
-    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmO, tmW, p);
+    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmO, p);
     if (e == cudaSuccess)
         e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1)
@@ -1241,6 +994,12 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
     else
         k_splitk_reduce<<<(int)rgrid, 256, 0, st>>>(a.ws, p.splits, p.R, p.C, a.out, a.ldo);
     return cuda_status(cudaGetLastError(), "split-K reduction launch");
+}
+
+template <int kMode, bool kBMN>
+rlq_status launch_mode(const GemmArgs &a, int splits, cudaStream_t st, bool pair, bool stall)
+{
+    return pair ? launch_impl<kMode, kBMN, true>(a, splits, st) : launch_impl<kMode, kBMN, false>(a, splits, st, stall);
 }
 
 // One-shot diagnostic armed by arm_gemm_stall() for the calling thread.
@@ -1263,7 +1022,9 @@ rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st)
     if (a.R == 0 || a.C == 0)
         return RLQ_OK;
     if (a.L == 0) {
-        // empty contraction: the sum is zero
+        // empty contraction: the sum is zero (nothing to add in accumulate mode)
+        if (a.acc)
+            return RLQ_OK;
         return cuda_status(cudaMemset2DAsync(a.out, (size_t)a.ldo * 2, 0, (size_t)a.C * 2, (size_t)a.R, st),
                            "cudaMemset2DAsync (empty contraction)");
     }
@@ -1274,27 +1035,19 @@ rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st)
         if (rs != RLQ_OK)
             return rs;
     }
-    if (a.acc) {
-        // the fp32 result comes from the split-K partials: at least two splits
-        // (the caller checked that two planes fit and that L spans two blocks)
-        if (a.ws == nullptr || a.ws_bytes < 2 * a.R * a.C * 4 || a.L <= BK)
-            return fail(RLQ_ERR_INVALID_ARG, "accumulate mode needs two workspace planes and L > 128");
-        if (splits < 2)
-            splits = 2;
-    }
     // the armed stall diagnostic applies to this launch only, on single CTAs
     const bool stall = t_stall_armed;
     t_stall_armed = false;
     // CTA pairs for tiles of 256 output rows; one CTA per 128 rows when the output
     // has fewer rows or the contraction is split
     const bool pair = splits == 1 && a.R >= 2 * BM && pair_mode_enabled() && !stall;
+    if (a.scale_once)
+        return launch_mode<MODE_ONCE, false>(a, splits, st, pair, stall);
     if (a.per_col_sb)
-        return pair ? launch_impl<true, false, true>(a, splits, st)
-                    : launch_impl<true, false, false>(a, splits, st, stall);
+        return launch_mode<MODE_COLS, false>(a, splits, st, pair, stall);
     if (a.b_mn_major)
-        return pair ? launch_impl<false, true, true>(a, splits, st)
-                    : launch_impl<false, true, false>(a, splits, st, stall);
-    return pair ? launch_impl<false, false, true>(a, splits, st) : launch_impl<false, false, false>(a, splits, st, stall);
+        return launch_mode<MODE_BLOCK, true>(a, splits, st, pair, stall);
+    return launch_mode<MODE_BLOCK, false>(a, splits, st, pair, stall);
 }
 
 void arm_gemm_stall() { t_stall_armed = true; }
@@ -1316,26 +1069,23 @@ rlq_status check_device_errors(cudaStream_t st)
     cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess)
         return cuda_status(e, "cudaStreamSynchronize");
-    unsigned long long word = 0;
-    e = cudaMemcpyFromSymbolAsync(&word, g_rlq_error_word, sizeof word, 0, cudaMemcpyDeviceToHost, st);
+    // every translation unit with bounded-wait kernels keeps its own error word
+    unsigned long long words[2] = {0, 0};
+    e = take_error_word(st, &words[0]);
     if (e == cudaSuccess)
-        e = cudaStreamSynchronize(st);
+        e = take_nvfp4_error_word(st, &words[1]);
     if (e != cudaSuccess)
-        return cuda_status(e, "reading the device error word");
+        return cuda_status(e, "reading and clearing the device error words");
+    const unsigned long long word = words[0] ? words[0] : words[1];
     if (word == 0)
         return RLQ_OK;
-    const unsigned long long zero = 0;
-    e = cudaMemcpyToSymbolAsync(g_rlq_error_word, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess)
-        e = cudaStreamSynchronize(st);
-    if (e != cudaSuccess)
-        return cuda_status(e, "clearing the device error word");
     const uint32_t code = (uint32_t)word, site = (uint32_t)(word >> 32);
     static const char *names[] = {"?", "TMA producer (stage free)", "MMA issuer (TMEM buffer free)",
                                   "MMA issuer (stage loaded)", "epilogue (partial ready)", "teardown", "drain",
-                                  "scale loader (slot free)", "epilogue (scales ready)"};
-    const char *where = site == SITE_DIAG ? "diagnostic wait" : (site < 9 ? names[site] : "?");
-    return fail((rlq_status)code, "device-side wait ran out at site %u (%s)", site, where);
+                                  "scale loader (slot free)", "epilogue (scales ready)", "FP4 converter (stage free)"};
+    const char *where = site == SITE_DIAG ? "diagnostic wait" : (site < 10 ? names[site] : "?");
+    return fail((rlq_status)code, "device-side wait ran out at site %u (%s)%s", site, where,
+                words[1] && !words[0] ? " in the NVFP4 GEMM" : "");
 }
 
 rlq_status launch_diag_wait(int64_t timeout_us, cudaStream_t st)

@@ -1,0 +1,520 @@
+// NVFP4 weight-only GEMM on 5th-generation tensor cores (sm_103a).
+//
+// QeRL news article: the rollout runs the policy with NVFP4 weights (4-bit E2M1
+// values, an FP8 E4M3 scale per block of 16 elements and an FP32 tensor scale)
+// in FP4 x BF16 kernels: the activations stay bf16.  This kernel computes
+//
+//   Y[m, n] = bf16_RN( st * sum_k X[m, k] * (e2m1(q[n, k]) * e4m3(sb[n, k / 16])) )
+//
+// with X bf16 [M, K], q the packed E2M1 codes [N, K/2], sb the block-scale codes
+// [N, K/16] and st the fp32 tensor scale, as rlq_quant_nvfp4 writes them.  An
+// E2M1 value times an E4M3 value has at most 6 significant bits and lies in
+// [2^-10, 2688] (or is 0), so it is exact in bf16: the weight tile is expanded to
+// bf16 in shared memory and the contraction runs on tcgen05.mma kind::f16 (bf16 x
+// bf16 -> fp32), accumulated in TMEM over the whole K; st is applied once in the
+// epilogue.
+//
+// Roles (one persistent CTA per SM, 768 threads):
+//   * warp 0 (one thread): TMA producer.  Per 64-element contraction stage the
+//     128 x 64 bf16 X tile (128-byte swizzle) into a 3-stage ring; per 256-element
+//     chunk the 256 rows x 128 bytes of packed codes (128-byte swizzle) and 256 x 16
+//     bytes of block scales into a 2-slot raw ring.
+//   * warp 1 (one thread): MMA issuer (4 x M=128, N=256, K=16 per stage into one
+//     of two TMEM accumulators, 256 fp32 columns each; tiles alternate); warp 1
+//     owns the 512 TMEM columns.
+//   * warps 4-19 (512 threads, two per weight row, 32 elements each per stage):
+//     converters.  Eight codes become eight bf16 values: magnitudes through two
+//     byte tables (prmt), signs replicated from each nibble's top bit (prmt sign
+//     mode), then one bf16x2 multiply by the block's scale per pair (exact); the
+//     values are stored as 16-byte chunks in the layout of the MMA's shared-memory
+//     descriptor (128-byte swizzle).
+//   * warps 20-23 (128 threads, one TMEM lane each): epilogue, tcgen05.ld in 32-
+//     column chunks, times st, rounded to bf16 and stored row by row.
+// Every mbarrier wait is bounded as in the FP8 GEMM: a wait that runs out records
+// an error word (this translation unit's) and raises the CTA's abort flag; the
+// CTA drains its TMA copies, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "rlq_internal.h"
+#include "rlq_tc.cuh"
+
+namespace rlq {
+namespace {
+
+constexpr int NV_BM = 128;                  // X rows per tile (TMEM lanes)
+constexpr int NV_BN = 256;                  // weight rows (output columns) per tile (MMA N)
+constexpr int NV_BK = 64;                   // contraction elements per stage (128 bytes of bf16)
+constexpr int NV_CHUNK = 4 * NV_BK;         // contraction elements per raw chunk (128 bytes of codes)
+constexpr int NV_STAGES = 3;
+constexpr int NV_RAW_SLOTS = 2;
+constexpr int NV_A_BYTES = NV_BM * NV_BK * 2;          // 16 KB
+constexpr int NV_B_BYTES = NV_BN * NV_BK * 2;          // 32 KB
+constexpr int NV_CODE_BYTES = NV_BN * (NV_CHUNK / 2);  // 32 KB
+constexpr int NV_SCALE_BYTES = NV_BN * (NV_CHUNK / 16);  // 4 KB
+constexpr int NV_THREADS = 768;
+constexpr int NV_CONV_WARP0 = 4;
+constexpr int NV_CONV_WARPS = 16;            // two threads per weight row, 32 elements each per stage
+constexpr int NV_EPI_WARP0 = 20;             // four warps, one per TMEM lane quarter (warp % 4)
+constexpr int NV_EPI_WARPS = 4;
+constexpr int NV_TMEM_COLS = 512;
+constexpr int NV_PREFETCH_CHUNKS = 3;        // weight chunks prefetched into L2 ahead of the ring
+constexpr int NV_UMMA_K = 16;
+// barriers: a_full, b_full, stage_empty per stage; raw_full, raw_empty per raw
+// slot; tfull, tempty per accumulator; teardown
+constexpr int NV_NUM_BARS = 3 * NV_STAGES + 2 * NV_RAW_SLOTS + 4 + 1;
+constexpr int NV_OFF_A = 0;
+constexpr int NV_OFF_B = NV_OFF_A + NV_STAGES * NV_A_BYTES;
+constexpr int NV_OFF_CODES = NV_OFF_B + NV_STAGES * NV_B_BYTES;
+constexpr int NV_OFF_SCALES = NV_OFF_CODES + NV_RAW_SLOTS * NV_CODE_BYTES;
+constexpr int NV_OFF_BARS = NV_OFF_SCALES + NV_RAW_SLOTS * NV_SCALE_BYTES;
+constexpr int NV_SMEM = 1024 /* alignment slack */ + NV_OFF_BARS + NV_NUM_BARS * 8 + 16;
+static_assert(NV_SMEM <= 232448, "shared memory budget");
+// tcgen05.mma kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B
+// bf16 (format 1 in bits 7-9 and 10-12), both K-major, N >> 3 in bits 17-22,
+// M >> 4 in bits 24-28.
+constexpr uint32_t NV_IDESC =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NV_BN >> 3) << 17) | ((uint32_t)(NV_BM >> 4) << 24);
+
+struct NvParams {
+    const float *st;  // tensor scale (device)
+    uint16_t *y;
+    int64_t ldy;
+    int M, N, K;
+    int kstages;      // ceil(K / 64)
+    int m_tiles, num_tiles;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void nv_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(NV_IDESC), "r"(accumulate)
+        : "memory");
+}
+
+// Prefetch a tensor-map box into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"((uint64_t)map), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// bf16 bit pattern of a (non-negative, finite) E4M3 block-scale code: exact, since
+// E4M3 has 3 mantissa bits and a range inside bf16's.
+__device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t e)
+{
+    const uint32_t ex = (e >> 3) & 15u, m = e & 7u;
+    const float v = ex == 0 ? (float)m * 0x1p-9f : __uint_as_float(((ex + 120u) << 23) | (m << 20));
+    return __float_as_uint(v) >> 16;
+}
+
+// Eight E2M1 codes (one 32-bit word, element 0 in the lowest nibble) times one
+// bf16 scale (in both halves of s2): four bf16x2 words, element 0 lowest.
+// Magnitude bytes of 0, 0.5, 1, 1.5, 2, 3, 4, 6 in bf16: high bytes 00 3F 3F 3F 40
+// 40 40 40, low bytes 00 00 80 C0 00 40 80 C0.  Signs: element 2k's sign is bit 7
+// of byte k of (w << 4), element 2k+1's bit 7 of byte k of w; a prmt selector with
+// bit 3 set replicates the selected byte's bit 7, so one prmt gives the sign bytes
+// of four elements, which are merged into their high bytes before the interleave.
+__device__ __forceinline__ uint4 e2m1x8_to_bf16(uint32_t w, uint32_t s2)
+{
+    constexpr uint32_t HI0 = 0x3F3F3F00u, HI1 = 0x40404040u;
+    constexpr uint32_t LO0 = 0xC0800000u, LO1 = 0xC0804000u;
+    const uint32_t m = w & 0x77777777u;  // magnitudes: prmt selectors in plain (not sign) mode
+    const uint32_t m2 = m >> 16;
+    const uint32_t we = w << 4;
+    const uint32_t s03 = prmt(we, w, 0xD9C8u);  // signs of elements 0, 1, 2, 3 as 00 / FF bytes
+    const uint32_t s47 = prmt(we, w, 0xFBEAu);  // elements 4 .. 7
+    const uint32_t h03 = prmt(HI0, HI1, m) | (s03 & 0x80808080u);
+    const uint32_t h47 = prmt(HI0, HI1, m2) | (s47 & 0x80808080u);
+    const uint32_t l03 = prmt(LO0, LO1, m), l47 = prmt(LO0, LO1, m2);
+    uint4 out;
+    out.x = mul_bf16x2(prmt(l03, h03, 0x5140u), s2);  // elements 0, 1
+    out.y = mul_bf16x2(prmt(l03, h03, 0x7362u), s2);  // elements 2, 3
+    out.z = mul_bf16x2(prmt(l47, h47, 0x5140u), s2);
+    out.w = mul_bf16x2(prmt(l47, h47, 0x7362u), s2);
+    return out;
+}
+
+__global__ void __launch_bounds__(NV_THREADS, 1)
+    k_gemm_nvfp4w(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmQ,
+                  const __grid_constant__ CUtensorMap tmS, const NvParams p)
+{
+    extern __shared__ uint8_t nv_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(nv_smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NV_OFF_BARS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NV_NUM_BARS);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t s0 = smem_u32(smem);
+    auto a_stage = [&](int s) { return s0 + (uint32_t)(NV_OFF_A + s * NV_A_BYTES); };
+    auto b_stage = [&](int s) { return s0 + (uint32_t)(NV_OFF_B + s * NV_B_BYTES); };
+    auto codes_slot = [&](int r) { return s0 + (uint32_t)(NV_OFF_CODES + r * NV_CODE_BYTES); };
+    auto scales_slot = [&](int r) { return s0 + (uint32_t)(NV_OFF_SCALES + r * NV_SCALE_BYTES); };
+    auto a_full = [&](int s) { return smem_u32(&bars[s]); };
+    auto b_full = [&](int s) { return smem_u32(&bars[NV_STAGES + s]); };
+    auto st_empty = [&](int s) { return smem_u32(&bars[2 * NV_STAGES + s]); };
+    auto raw_full = [&](int r) { return smem_u32(&bars[3 * NV_STAGES + r]); };
+    auto raw_empty = [&](int r) { return smem_u32(&bars[3 * NV_STAGES + NV_RAW_SLOTS + r]); };
+    auto tfull = [&](int b) { return smem_u32(&bars[3 * NV_STAGES + 2 * NV_RAW_SLOTS + b]); };
+    auto tempty = [&](int b) { return smem_u32(&bars[3 * NV_STAGES + 2 * NV_RAW_SLOTS + 2 + b]); };
+    const uint32_t teardown = smem_u32(&bars[3 * NV_STAGES + 2 * NV_RAW_SLOTS + 4]);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NV_STAGES; ++s) {
+            mbar_init(a_full(s), 1);
+            mbar_init(b_full(s), NV_CONV_WARPS);
+            mbar_init(st_empty(s), 1);
+        }
+        for (int r = 0; r < NV_RAW_SLOTS; ++r) {
+            mbar_init(raw_full(r), 1);
+            mbar_init(raw_empty(r), NV_CONV_WARPS);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull(b), 1);
+            mbar_init(tempty(b), NV_EPI_WARPS);
+        }
+        mbar_init(teardown, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(NV_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmS);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ---
+        if (lane == 0) {
+            int it = 0, rc = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                const int mt = t % p.m_tiles, nt = t / p.m_tiles;
+                for (int ks = 0; ks < p.kstages; ++ks, ++it) {
+                    if ((ks & 3) == 0) {
+                        const int r = rc % NV_RAW_SLOTS;
+                        if (!mbar_wait(raw_empty(r), ((uint32_t)(rc / NV_RAW_SLOTS) & 1u) ^ 1u, abort_flag,
+                                       p.timeout_ns, SITE_PRODUCER_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(raw_full(r), NV_CODE_BYTES + NV_SCALE_BYTES);
+                        tma_load_2d(codes_slot(r), &tmQ, raw_full(r), (ks >> 2) * (NV_CHUNK / 2), nt * NV_BN);
+                        tma_load_2d(scales_slot(r), &tmS, raw_full(r), (ks >> 2) * (NV_CHUNK / 16), nt * NV_BN);
+                        // start the weight stream a few chunks ahead into L2 (this tile's
+                        // chunks only; the two ring slots alone hold too few bytes in flight
+                        // to cover HBM latency)
+                        const int ahead = (ks >> 2) + NV_PREFETCH_CHUNKS;
+                        if (ahead * NV_CHUNK < p.K) {
+                            tma_prefetch_l2(&tmQ, ahead * (NV_CHUNK / 2), nt * NV_BN);
+                            tma_prefetch_l2(&tmS, ahead * (NV_CHUNK / 16), nt * NV_BN);
+                        }
+                        ++rc;
+                    }
+                    const int s = it % NV_STAGES;
+                    if (!mbar_wait(st_empty(s), ((uint32_t)(it / NV_STAGES) & 1u) ^ 1u, abort_flag, p.timeout_ns,
+                                   SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(a_full(s), NV_A_BYTES);
+                    tma_load_2d(a_stage(s), &tmX, a_full(s), ks * NV_BK, mt * NV_BM);
+                }
+            }
+            // Once the MMA warp made its final commit, a normal run has consumed every
+            // copy; a CTA that aborted waits (bounded) for the copies still in flight.
+            volatile uint32_t never = 0;
+            mbar_wait(teardown, 0, &never, p.timeout_ns, SITE_TEARDOWN);
+            if (!ok || *abort_flag) {
+                for (int j = it > NV_STAGES ? it - NV_STAGES : 0; j < it; ++j)
+                    mbar_wait(a_full(j % NV_STAGES), (uint32_t)(j / NV_STAGES) & 1u, &never, 20000000ull, SITE_DRAIN);
+                for (int j = rc > NV_RAW_SLOTS ? rc - NV_RAW_SLOTS : 0; j < rc; ++j)
+                    mbar_wait(raw_full(j % NV_RAW_SLOTS), (uint32_t)(j / NV_RAW_SLOTS) & 1u, &never, 20000000ull,
+                              SITE_DRAIN);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer ---
+        if (lane == 0) {
+            int it = 0, tc = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++tc) {
+                const int buf = tc & 1;
+                if (!mbar_wait(tempty(buf), ((uint32_t)(tc >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns,
+                               SITE_MMA_TMEM_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t d = tmem_base + (uint32_t)(buf * NV_BN);
+                for (int ks = 0; ks < p.kstages; ++ks, ++it) {
+                    const int s = it % NV_STAGES;
+                    const uint32_t ph = (uint32_t)(it / NV_STAGES) & 1u;
+                    if (!mbar_wait(a_full(s), ph, abort_flag, p.timeout_ns, SITE_MMA_FULL) ||
+                        !mbar_wait(b_full(s), ph, abort_flag, p.timeout_ns, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sw128_desc(a_stage(s)), bd = sw128_desc(b_stage(s));
+#pragma unroll
+                    for (int j = 0; j < NV_BK / NV_UMMA_K; ++j)  // +32 bytes along K per MMA
+                        nv_mma(d, ad + 2 * j, bd + 2 * j, (ks > 0 || j > 0) ? 1u : 0u);
+                    tc_commit(st_empty(s));
+                    if (ks + 1 == p.kstages)
+                        tc_commit(tfull(buf));
+                }
+            }
+            // every MMA issued above has completed once this commit arrives
+            tc_commit(teardown);
+            volatile uint32_t never = 0;
+            mbar_wait(teardown, 0, &never, 20000000ull, SITE_TEARDOWN);
+        }
+    } else if (warp >= NV_CONV_WARP0 && warp < NV_CONV_WARP0 + NV_CONV_WARPS) {
+        // ------------------------------------------------- converters ---
+        const int ct = threadIdx.x - NV_CONV_WARP0 * 32;  // 0..511
+        const int row = ct >> 1;                           // weight row within the tile, 0..255
+        const int half = ct & 1;                           // elements 32*half .. 32*half+31 of a stage
+        const uint32_t sw = (uint32_t)(row & 7);
+        int it = 0, rc = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int ks = 0; ks < p.kstages; ++ks, ++it) {
+                const int r = rc % NV_RAW_SLOTS;
+                if ((ks & 3) == 0 &&
+                    !__all_sync(0xFFFFFFFFu, mbar_wait(raw_full(r), (uint32_t)(rc / NV_RAW_SLOTS) & 1u, abort_flag,
+                                                       p.timeout_ns, SITE_CONVERTER_EMPTY))) {
+                    ok = false;
+                    break;
+                }
+                const int s = it % NV_STAGES;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(st_empty(s), ((uint32_t)(it / NV_STAGES) & 1u) ^ 1u,
+                                                       abort_flag, p.timeout_ns, SITE_CONVERTER_EMPTY))) {
+                    ok = false;
+                    break;
+                }
+                // this thread's 32 codes of the stage: 16-byte chunk 2q + half of the row's
+                // 128-byte (swizzled) line in the raw slot, q = ks % 4; scale bytes 2 half,
+                // 2 half + 1 of the row's four for the stage
+                const int qk = ks & 3;
+                uint4 c;
+                {
+                    const uint32_t a = codes_slot(r) + (uint32_t)(row * 128) +
+                                       ((((uint32_t)(2 * qk + half)) ^ sw) << 4);
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(c.x), "=r"(c.y), "=r"(c.z), "=r"(c.w)
+                                 : "r"(a));
+                }
+                uint32_t sc;
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(scales_slot(r) + (uint32_t)(row * 16 + qk * 4)));
+                sc >>= 16 * half;
+                const uint32_t sb0 = e4m3_to_bf16_bits(sc & 0xFFu), sb1 = e4m3_to_bf16_bits((sc >> 8) & 0xFFu);
+                const uint32_t s0 = sb0 | (sb0 << 16), s1 = sb1 | (sb1 << 16);
+                const uint32_t brow = b_stage(s) + (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
+                const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {  // elements 8j .. 8j+7 of this half, block scale j / 2
+                    const uint4 v = e2m1x8_to_bf16(w4[j], j < 2 ? s0 : s1);
+                    const uint32_t chunk = (uint32_t)(4 * half + j);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(brow + ((chunk ^ sw) << 4)),
+                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                 : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> MMA reads
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(b_full(s));
+                if (qk == 3 || ks + 1 == p.kstages) {  // the raw chunk is read out
+                    if (lane == 0)
+                        mbar_arrive(raw_empty(r));
+                    ++rc;
+                }
+            }
+        }
+    } else if (warp >= NV_EPI_WARP0) {
+        // --------------------------------------------------- epilogue ---
+        const int q = warp & 3;  // TMEM lane quarter of this warp
+        const int row = q * 32 + lane;
+        const float st = *p.st;
+        const float2 st2 = make_float2(st, st);
+        int tc = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tc) {
+            const int mt = t % p.m_tiles, nt = t / p.m_tiles;
+            const int buf = tc & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull(buf), (uint32_t)(tc >> 1) & 1u, abort_flag, p.timeout_ns,
+                                                   SITE_EPI_TMEM_FULL)))
+                break;
+            tc_fence_after();
+            const int grow = mt * NV_BM + row;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NV_BN);
+            uint32_t r[32];
+#pragma unroll 1
+            for (int cc = 0; cc < NV_BN / 32; ++cc) {
+                tmem_ld32_async(taddr + (uint32_t)(cc * 32), r);
+                tmem_wait32(r);
+                if (cc == NV_BN / 32 - 1) {  // the accumulator is read out
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(tempty(buf));
+                }
+                const int col = nt * NV_BN + cc * 32;
+                if (grow < p.M && col < p.N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)grow * p.ldy + col);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float2 a = __fmul2_rn(make_float2(__uint_as_float(r[8 * v + 2 * u]),
+                                                                    __uint_as_float(r[8 * v + 2 * u + 1])),
+                                                        st2);
+                            uint32_t d;
+                            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(a.y), "f"(a.x));
+                            o[u] = d;
+                        }
+                        dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(NV_TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host ---
+
+PFN_cuTensorMapEncodeTiled_v12000 nv_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+rlq_status nv_map(CUtensorMap *map, CUtensorMapDataType dt, const void *base, int64_t inner, int64_t rows,
+                  int64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz, const char *what)
+{
+    auto enc = nv_encode_fn();
+    if (!enc)
+        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for the %s", (int)r, what);
+    return RLQ_OK;
+}
+
+uint64_t nv_wait_limit_ns()
+{
+    static uint64_t ns = [] {
+        const char *e = std::getenv("RLQ_WAIT_TIMEOUT_MS");
+        long long ms = e ? std::atoll(e) : 1000;
+        if (ms < 1)
+            ms = 1;
+        if (ms > 600000)
+            ms = 600000;
+        return (uint64_t)ms * 1000000ull;
+    }();
+    return ns;
+}
+
+}  // namespace
+
+rlq_status launch_gemm_nvfp4w(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq, const uint8_t *wsb,
+                              int64_t ldwsb, const float *st, uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                              cudaStream_t stream)
+{
+    CUtensorMap tmX, tmQ, tmS;
+    rlq_status rs = nv_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, NV_BK, NV_BM,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "bf16 activations");
+    if (rs != RLQ_OK)
+        return rs;
+    rs = nv_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, K / 2, N, ldwq, NV_CHUNK / 2, NV_BN,
+                CU_TENSOR_MAP_SWIZZLE_128B, "packed E2M1 weight codes");
+    if (rs != RLQ_OK)
+        return rs;
+    rs = nv_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, wsb, K / 16, N, ldwsb, NV_CHUNK / 16, NV_BN,
+                CU_TENSOR_MAP_SWIZZLE_NONE, "E4M3 block scales");
+    if (rs != RLQ_OK)
+        return rs;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return cuda_status(e, "device query");
+    static bool attr[64] = {};
+    if (!attr[dev & 63]) {
+        e = cudaFuncSetAttribute(k_gemm_nvfp4w, cudaFuncAttributeMaxDynamicSharedMemorySize, NV_SMEM);
+        if (e != cudaSuccess)
+            return cuda_status(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        attr[dev & 63] = true;
+    }
+    NvParams p;
+    p.st = st;
+    p.y = y;
+    p.ldy = ldy;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.kstages = (int)((K + NV_BK - 1) / NV_BK);
+    p.m_tiles = (int)((M + NV_BM - 1) / NV_BM);
+    p.num_tiles = p.m_tiles * (int)((N + NV_BN - 1) / NV_BN);
+    p.timeout_ns = nv_wait_limit_ns();
+    const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+    k_gemm_nvfp4w<<<grid, NV_THREADS, NV_SMEM, stream>>>(tmX, tmQ, tmS, p);
+    return cuda_status(cudaGetLastError(), "NVFP4 GEMM launch");
+}
+
+cudaError_t take_nvfp4_error_word(cudaStream_t st, unsigned long long *word) { return take_error_word(st, word); }
+
+}  // namespace rlq

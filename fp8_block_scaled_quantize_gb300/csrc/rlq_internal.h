@@ -62,18 +62,30 @@ struct GemmArgs {
     int64_t sb_cstride;
     bool per_col_sb;
     bool b_mn_major;
+    // sa(b, r) and sb(b, c) equal for every contraction block b (per-token x
+    // per-channel scales, sb column-scaled): the contraction is accumulated in
+    // the tensor cores and scaled once
+    bool scale_once;
     uint16_t *out;
     int64_t ldo;
     int64_t R, C, L;
     // split-K workspace (16-byte aligned fp32), or NULL for the single-pass GEMM
     float *ws;
     int64_t ws_bytes;
-    // accumulate mode: acc[r * ld_acc + c] += the fp32 result (out is not written);
-    // needs ws with room for two planes and at least two contraction blocks
+    // accumulate mode: acc[r * ld_acc + c] += the fp32 result (out is not written),
+    // from the GEMM's epilogue, or from the split-K partials where the plan splits
     float *acc;
     int64_t ld_acc;
 };
 rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st);
+
+// ---- NVFP4 weight-only GEMM (rlq_gemm_nvfp4.cu); arguments already validated ----
+// Y[M, N] = bf16(st * X W^T), X bf16 [M, K] (pitch ldx elements), W from packed
+// E2M1 codes wq [N, K/2] (pitch ldwq bytes) and E4M3 block scales wsb [N, K/16]
+// (pitch ldwsb bytes), st one fp32 in device memory.  K % 64 == 0, K > 0.
+rlq_status launch_gemm_nvfp4w(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq, const uint8_t *wsb,
+                              int64_t ldwsb, const float *st, uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                              cudaStream_t stream);
 
 // Number of contraction splits the split-K GEMM uses for an [R x C] output
 // with contraction length L on the current device, and the workspace bytes
@@ -81,8 +93,10 @@ rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st);
 // workspace (-1: no limit).
 rlq_status plan_splitk(int64_t R, int64_t C, int64_t L, int64_t ws_cap, int *splits, int64_t *ws_bytes);
 
-// Reads and clears the device error word of the current device (after syncing st).
+// Reads and clears the device error words of the current device (after syncing st).
 rlq_status check_device_errors(cudaStream_t st);
+// The NVFP4 GEMM's translation unit's error word, read and cleared (0: none).
+cudaError_t take_nvfp4_error_word(cudaStream_t st, unsigned long long *word);
 rlq_status launch_diag_wait(int64_t timeout_us, cudaStream_t st);
 
 // Arms, for the calling thread, a one-shot stall of the next block-scaled GEMM

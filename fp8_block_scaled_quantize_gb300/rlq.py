@@ -41,6 +41,7 @@ _SIGS = {
     "rlq_uaq_fold": [_P, _I, _I, _I, _P, _P, _I, _I, _P],
     "rlq_gemm_wgrad_accumulate": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_quant_nvfp4": [_P, _I, _I, _I, _P, _I, _P, _I, _P, _P],
+    "rlq_gemm_nvfp4_weight_only": [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _P],
     "rlq_aqn_sigma": [ctypes.c_float, ctypes.c_float, _I, _I, ctypes.POINTER(ctypes.c_float)],
     "rlq_aqn_perturb": [_P, _I, _P, ctypes.c_float, _P],
     "rlq_check": [_P],
@@ -185,6 +186,10 @@ def rlq_gemm_wgrad_accumulate(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc
 
 def rlq_quant_nvfp4(w, N, K, ldw, q, ldq, sb, ldsb, st, stream):
     return _call("rlq_quant_nvfp4", w, N, K, ldw, q, ldq, sb, ldsb, st, stream)
+
+
+def rlq_gemm_nvfp4_weight_only(x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, stream):
+    return _call("rlq_gemm_nvfp4_weight_only", x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, stream)
 
 
 def rlq_aqn_sigma(sigma_start, sigma_end, t, T) -> float:
@@ -416,18 +421,16 @@ def gemm_wgrad(dyqT, dysc, xqT, xsc, out=None, stream=None, split_k: bool = Fals
 
 def gemm_wgrad_accumulate_(dw_acc: torch.Tensor, dyqT, dysc, xqT, xsc, workspace=None, stream=None):
     """dw_acc [N, K] fp32 += dY^T X (the WGrad product, kept in fp32).  The
-    workspace (uint8 device tensor) defaults to the larger of two fp32 planes and
-    the library's split-K plan."""
+    workspace (uint8 device tensor) defaults to the library's split-K plan (none
+    when the plan is one pass: the GEMM's epilogue then adds into dw_acc)."""
     if dw_acc.dtype != torch.float32:
         raise TypeError("dw_acc must be float32")
     N, M = dyqT.shape
     K = xqT.shape[0]
-    if workspace is None:
-        nbytes = max(2 * N * K * 4, rlq_gemm_splitk_workspace_bytes(GEMM_WGRAD, M, N, K))
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dw_acc.device)
+    ptr, nbytes = _workspace(GEMM_WGRAD, M, N, K, workspace, dw_acc.device)
     rlq_gemm_wgrad_accumulate(dyqT.data_ptr(), _ld(dyqT), dysc.data_ptr(), _ld(dysc), xqT.data_ptr(), _ld(xqT),
-                              xsc.data_ptr(), _ld(xsc), dw_acc.data_ptr(), _ld(dw_acc), M, N, K,
-                              workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+                              xsc.data_ptr(), _ld(xsc), dw_acc.data_ptr(), _ld(dw_acc), M, N, K, ptr, nbytes,
+                              _stream(stream))
     return dw_acc
 
 
@@ -449,13 +452,27 @@ def quant_nvfp4(w: torch.Tensor, stream=None):
         raise TypeError("w must be bfloat16")
     N, K = w.shape
     dev = w.device
-    kq = _round_up(max(K // 2, 1), 8)
+    # pitches rounded to 16 bytes: the layout gemm_nvfp4_weight_only reads by TMA
+    kq = _round_up(max(K // 2, 1), 16)
+    ks = _round_up(max(K // 16, 1), 16)
     q = torch.empty((N, kq), dtype=torch.uint8, device=dev)[:, :K // 2]
-    sb = torch.empty((N, max(K // 16, 1)), dtype=torch.uint8, device=dev)[:, :K // 16]
+    sb = torch.empty((N, ks), dtype=torch.uint8, device=dev)[:, :K // 16]
     st = torch.empty((1,), dtype=torch.float32, device=dev)
-    rlq_quant_nvfp4(w.data_ptr(), N, K, _ld(w), q.data_ptr(), kq, sb.data_ptr(), max(K // 16, 1), st.data_ptr(),
-                    _stream(stream))
+    rlq_quant_nvfp4(w.data_ptr(), N, K, _ld(w), q.data_ptr(), kq, sb.data_ptr(), ks, st.data_ptr(), _stream(stream))
     return q, sb, st
+
+
+def gemm_nvfp4_weight_only(x: torch.Tensor, q, sb, st, out=None, stream=None):
+    """Y [M, N] bf16 = X W^T with bf16 X [M, K] and NVFP4 weights (the outputs of
+    ``quant_nvfp4``: q [N, K/2] packed E2M1, sb [N, K/16] E4M3, st [1] f32)."""
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    M, K = x.shape
+    N = q.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    rlq_gemm_nvfp4_weight_only(x.data_ptr(), _ld(x), q.data_ptr(), q.stride(0), sb.data_ptr(), sb.stride(0),
+                               st.data_ptr(), y.data_ptr(), _ld(y), M, N, K, _stream(stream))
+    return y
 
 
 def aqn_perturb_(gamma: torch.Tensor, z: torch.Tensor, sigma: float, stream=None):

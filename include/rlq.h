@@ -215,7 +215,9 @@ rlq_status rlq_gemm_wgrad(const uint8_t *dyqT, int64_t lddyqT, const float *dysc
  *
  * which with replicated scales (xs_rep[kb, m] = sx[m], ws_rep[kb, n] = sw[n])
  * equals sx[m] sw[n] sum_k x[m,k] w[n,k] up to the order of the fp32 sums.
- * The column-scaled kernel of rlq_gemm_wgrad runs it.
+ * The GEMM relies on that: it accumulates the whole contraction (or, split-K,
+ * each split's range) in fp32 in the tensor cores and multiplies the sum once by
+ * fl32(xs_rep[kb0, m] * ws_rep[kb0, n]), kb0 the first block of the range.
  *
  *   xq  E4M3 [M, K], pitch ldxq;  xs_rep f32, xs_rep[kb * ldxs + m], ldxs >= M
  *   wq  E4M3 [N, K], pitch ldwq;  ws_rep f32, ws_rep[kb * ldws + n], ldws >= N,
@@ -249,19 +251,20 @@ rlq_status rlq_gemm_fprop_per_channel_splitk(const uint8_t *xq, int64_t ldxq, co
  *
  *   dw_acc[n, k] += sum_mb dysc[mb, n] * xsc[mb, k] * sum_{m in mb} dy[m,n] x[m,k]
  *
- * with the operands of rlq_gemm_wgrad.  The product is formed as in the split-K
- * WGrad (each split's sum in fp32, the splits added in split order) and then added
- * to dw_acc in fp32; nothing is rounded to bf16.
+ * with the operands of rlq_gemm_wgrad.  The product is formed as in
+ * rlq_gemm_wgrad (fp32 promotion of each 128-token block) and the GEMM's
+ * epilogue adds it to dw_acc in fp32; nothing is rounded to bf16.  Where the
+ * library's split-K plan splits the contraction (outputs of few tiles) and the
+ * workspace holds the plan, each split's fp32 sum goes to the workspace and a
+ * reduction adds the splits, in split order, to dw_acc.
  *
  *   dw_acc     f32 [N, K], pitch ld_acc >= K, 16-byte aligned rows (pointer
  *              16-byte aligned, ld_acc % 4 == 0); read and written
- *   workspace  device scratch, 16-byte aligned, at least 2 * N * K * 4 bytes
- *              (more lets the library use its split-K plan); contents on entry
- *              do not matter; not to be used by anything else until the call
- *              has completed on `stream`
- * M == 0 adds nothing.  M must exceed 128 (the fp32 result is assembled from at
- * least two contraction splits), else RLQ_ERR_UNSUPPORTED.  N % 128 == 0,
- * K % 128 == 0.
+ *   workspace  optional device scratch (NULL, or 16-byte aligned) for the split-K
+ *              plan, sized as for rlq_gemm_wgrad_splitk; contents on entry do not
+ *              matter; not to be used by anything else until the call has
+ *              completed on `stream`
+ * M == 0 adds nothing.  N % 128 == 0, K % 128 == 0.
  */
 rlq_status rlq_gemm_wgrad_accumulate(const uint8_t *dyqT, int64_t lddyqT, const float *dysc, int64_t lddysc,
                                      const uint8_t *xqT, int64_t ldxqT, const float *xsc, int64_t ldxsc,
@@ -291,6 +294,32 @@ rlq_status rlq_gemm_wgrad_accumulate(const uint8_t *dyqT, int64_t lddyqT, const 
  */
 rlq_status rlq_quant_nvfp4(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
                            uint8_t *sb, int64_t ldsb, float *st, rlq_stream_t stream);
+
+/*
+ * NVFP4 weight-only GEMM: BF16 activations times NVFP4 weights, the FP4 x BF16
+ * rollout GEMM of the QeRL news article (NVFP4 with two-level scaling, FP8 E4M3
+ * block scales and an FP32 tensor scale, run by FP4 x BF16 kernels).
+ *
+ *   Y[m, n] = bf16_RN( st * sum_k x[m, k] * e2m1(q[n, k]) * e4m3(sb[n, k / 16]) )
+ *
+ * with the operands rlq_quant_nvfp4 writes.  Each weight value e2m1 * e4m3 is exact
+ * in bf16 (at most 6 significant bits, within [2^-10, 2688] or 0); the products with
+ * x and their sum over K are accumulated in fp32 by the tensor cores, then multiplied
+ * once by st and rounded to bf16.  The activations are not quantized.
+ *
+ *   x    bf16 [M, K], pitch ldx >= K (elements, a multiple of 8), 16-byte aligned
+ *   wq   packed E2M1 codes [N, K/2] as rlq_quant_nvfp4 writes them (low nibble =
+ *        even element), pitch ldwq >= K/2 bytes, a multiple of 16, 16-byte aligned
+ *   wsb  E4M3 block-scale codes [N, K/16], pitch ldwsb >= K/16 bytes, a multiple of
+ *        16, 16-byte aligned
+ *   wst  the fp32 tensor scale, one value in device memory
+ *   y    bf16 [M, N], pitch ldy >= N (output, overwritten)
+ * N % 128 == 0 and K % 64 == 0, else RLQ_ERR_UNSUPPORTED.  M any value >= 0.
+ * Errors as for the other GEMMs (bounded device waits report at rlq_check).
+ */
+rlq_status rlq_gemm_nvfp4_weight_only(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq,
+                                      const uint8_t *wsb, int64_t ldwsb, const float *wst, uint16_t *y,
+                                      int64_t ldy, int64_t M, int64_t N, int64_t K, rlq_stream_t stream);
 
 /*
  * AQN, adaptive quantization noise (QeRL news article: channel-wise Gaussian

@@ -200,9 +200,8 @@ def test_aqn_validation_and_host_schedule():
 def test_wgrad_accumulate_validation():
     g = rlq.rlq_gemm_wgrad_accumulate
     ok = (FAKE, 256, FAKE, 128, FAKE, 256, FAKE, 128, FAKE, 128, 256, 128, 128, FAKE, 2 * 128 * 128 * 4, None)
-    assert _status(g, *ok[:10], 128, *ok[11:]) == 2                 # M = 128: one token block
-    assert _status(g, *ok[:14], 2 * 128 * 128 * 4 - 16, None) == 1  # workspace below two planes
-    assert _status(g, *ok[:13], None, 1 << 20, None) == 1           # no workspace
+    assert _status(g, *ok[:13], FAKE + 8, 1 << 20, None) == 3       # workspace not 16-byte aligned
+    assert _status(g, *ok[:14], -1, None) == 1                      # negative workspace size
     assert _status(g, *ok[:8], FAKE + 4, *ok[9:]) == 3              # dw_acc not 16-byte aligned
     assert _status(g, *ok[:9], 126, *ok[10:]) == 1                  # ld_acc < K
     assert _status(g, *ok[:10], 0, *ok[11:]) == 0                   # M = 0: nothing to add

@@ -1,0 +1,161 @@
+"""GPU parity of the NVFP4 weight-only GEMM (QeRL news article: the rollout's
+FP4 x BF16 GEMM with NVFP4 weights) through the C ABI, against the oracle's fp64
+gemm_nvfp4_weight_only over the oracle's own codes.
+
+* Tolerance of the other GEMM tests: relative Frobenius <= 2e-3 and per element
+  |err| <= 1e-2 * (|ref| + 1) on the bf16 output.
+* Exact pin: integer activations, block scales that are powers of two and a tensor
+  scale of 1 give fp32 sums that are exact: the GPU output must equal the exact
+  result rounded to bf16, bit for bit.
+* The weights come from the GPU quantizer, whose codes are first asserted equal to
+  the oracle's; then the workloads' shapes (8B decode, Qwen2.5-7B layers, 32B at
+  decode sizes), ragged M, a pitched layout and the empty contraction.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_block_scaled_quantize_gb300 import inputs as I
+from fp8_block_scaled_quantize_gb300 import rlq
+from gpu_util import assert_gemm_close, idx, normal_bits, np_, strata, to_dev, u16
+
+pytestmark = pytest.mark.gpu
+
+
+def _unpack(qp: np.ndarray) -> np.ndarray:
+    lo, hi = qp & 0xF, qp >> 4
+    return np.stack([lo, hi], axis=-1).reshape(qp.shape[0], -1)
+
+
+def _pack(q: np.ndarray) -> np.ndarray:
+    return (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+
+
+def _padded(a: np.ndarray) -> torch.Tensor:
+    """A device view of `a` whose rows start 16 bytes apart (the pitch rule for
+    codes and block scales)."""
+    rows, cols = a.shape
+    buf = torch.zeros((rows, (cols + 15) // 16 * 16), dtype=torch.uint8, device="cuda")
+    buf[:, :cols] = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return buf[:, :cols]
+
+
+def _quantized_weight(w_bits):
+    """GPU NVFP4 quantization, asserted equal to the oracle's; returns both."""
+    q, sb, st = rlq.quant_nvfp4(to_dev(w_bits))
+    rlq.check()
+    oq, osb, ost = oracle.quant_nvfp4(w_bits)
+    assert np_(st)[0] == np.float32(ost)
+    assert np.array_equal(np_(sb), osb)
+    assert np.array_equal(_unpack(np_(q)), oq)
+    return (q, sb, st), (oq, osb, ost)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (5, 256, 128), (128, 256, 256), (200, 384, 320),
+                                   (300, 640, 1024), (129, 128, 2048)])
+def test_parity_small_shapes(M, N, K):
+    x = normal_bits(90, (M, K), 1.0, "x")
+    w = normal_bits(90, (N, K), 0.02, "w")
+    (q, sb, st), (oq, osb, ost) = _quantized_weight(w)
+    y = rlq.gemm_nvfp4_weight_only(to_dev(x), q, sb, st)
+    rlq.check()
+    assert_gemm_close(y, oracle.gemm_nvfp4_weight_only(x, oq, osb, ost), f"NVFP4 GEMM {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 128, 64), (130, 256, 512), (64, 512, 1280)])
+def test_integer_case_bit_exact(M, N, K):
+    """x integers in [-4, 4], E2M1 codes at random, block scales 1/2, 1 and 2 (E4M3
+    codes 0x30, 0x38, 0x40), st = 1: every product is a multiple of 1/4 of at most
+    48 in magnitude and every partial sum a multiple of 1/4 below 2^17, so the fp32
+    sum is exact whatever its order; the GPU's bf16 output must then be the exact
+    result rounded to bf16, bit for bit."""
+    rng = np.random.default_rng(M + N + K)
+    x = I.to_bf16_bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
+    q = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    sb = rng.choice(np.array([0x30, 0x38, 0x40], np.uint8), size=(N, K // 16))
+    ref = oracle.gemm_nvfp4_weight_only(x, q, sb, 1.0)
+    assert np.all(ref * 4 == np.round(ref * 4)) and np.all(np.abs(ref) < 2 ** 17)
+    qp = _padded(_pack(q))
+    sbd = _padded(sb)
+    st = torch.ones(1, dtype=torch.float32, device="cuda")
+    y = rlq.gemm_nvfp4_weight_only(to_dev(x), qp, sbd, st)
+    rlq.check()
+    assert np.array_equal(u16(y), I.to_bf16_bits(ref.astype(np.float32)))
+
+
+def test_decode_upproj_8b_full_size():
+    d = I.decode_upproj_8b()
+    (q, sb, st), (oq, osb, ost) = _quantized_weight(d["w"])
+    y = rlq.gemm_nvfp4_weight_only(to_dev(d["x"]), q, sb, st)
+    rlq.check()
+    rng = np.random.default_rng(91)
+    cols = strata(14336, 64, rng)
+    ref = oracle.gemm_nvfp4_weight_only(d["x"], oq, osb, ost, cols=cols)
+    assert_gemm_close(y[:, idx(cols)], ref, "NVFP4 GEMM, 8B decode up-projection")
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+@pytest.mark.parametrize("M", [64, 512])
+def test_qwen7b_layers(which, M):
+    d = I.qwen7b_layer(M, which)
+    (q, sb, st), (oq, osb, ost) = _quantized_weight(d["w"])
+    y = rlq.gemm_nvfp4_weight_only(to_dev(d["x"]), q, sb, st)
+    rlq.check()
+    N = d["w"].shape[0]
+    rng = np.random.default_rng(M + N)
+    rows = np.arange(M) if M <= 64 else strata(M, 16, rng)
+    cols = strata(N, 32, rng)
+    ref = oracle.gemm_nvfp4_weight_only(d["x"], oq, osb, ost, rows=rows, cols=cols)
+    assert_gemm_close(y[idx(rows)][:, idx(cols)], ref, f"NVFP4 GEMM qwen7b {which} M={M}")
+
+
+@pytest.mark.parametrize("orient", ["up", "down"])
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_sweep_32b_decode(orient, M):
+    d = I.sweep_32b(M, orient, with_dy=False)
+    (q, sb, st), (oq, osb, ost) = _quantized_weight(d["w"])
+    y = rlq.gemm_nvfp4_weight_only(to_dev(d["x"]), q, sb, st)
+    rlq.check()
+    N = d["w"].shape[0]
+    cols = strata(N, 64, np.random.default_rng(M))
+    ref = oracle.gemm_nvfp4_weight_only(d["x"], oq, osb, ost, cols=cols)
+    assert_gemm_close(y[:, idx(cols)], ref, f"NVFP4 GEMM 32B {orient} M={M}")
+
+
+def test_pitched_operands_and_guard_bands():
+    M, N, K = 70, 256, 512
+    x = normal_bits(92, (M, K), 1.0, "x")
+    w = normal_bits(92, (N, K), 0.02, "w")
+    oq, osb, ost = oracle.quant_nvfp4(w)
+    dev = "cuda"
+    xb = torch.zeros((M, K + 24), dtype=torch.bfloat16, device=dev)
+    xb[:, :K] = to_dev(x)
+    qb = torch.zeros((N, K // 2 + 48), dtype=torch.uint8, device=dev)
+    qb[:, :K // 2] = torch.from_numpy(_pack(oq)).cuda()
+    sbb = torch.zeros((N, K // 16 + 16), dtype=torch.uint8, device=dev)
+    sbb[:, :K // 16] = torch.from_numpy(osb).cuda()
+    st = torch.tensor([ost], dtype=torch.float32, device=dev)
+    yb = torch.full((M, N + 40), 3.0, dtype=torch.bfloat16, device=dev)
+    rlq.rlq_gemm_nvfp4_weight_only(xb.data_ptr(), K + 24, qb.data_ptr(), K // 2 + 48, sbb.data_ptr(), K // 16 + 16,
+                                   st.data_ptr(), yb.data_ptr(), N + 40, M, N, K,
+                                   torch.cuda.current_stream().cuda_stream)
+    rlq.check()
+    assert_gemm_close(yb[:, :N], oracle.gemm_nvfp4_weight_only(x, oq, osb, ost), "pitched NVFP4 GEMM")
+    assert torch.all(yb[:, N:] == 3.0)
+
+
+def test_empty_contraction_and_validation():
+    dev = "cuda"
+    y = torch.full((4, 128), 5.0, dtype=torch.bfloat16, device=dev)
+    st = torch.ones(1, dtype=torch.float32, device=dev)
+    rlq.rlq_gemm_nvfp4_weight_only(None, 0, None, 0, None, 0, st.data_ptr(), y.data_ptr(), 128, 4, 128, 0,
+                                   torch.cuda.current_stream().cuda_stream)
+    rlq.check()
+    assert torch.all(y == 0)
+    x = torch.zeros((4, 96), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(rlq.RlqError) as e:  # K % 64
+        rlq.rlq_gemm_nvfp4_weight_only(x.data_ptr(), 96, x.data_ptr(), 48, x.data_ptr(), 16, st.data_ptr(),
+                                       y.data_ptr(), 128, 4, 128, 96, 0)
+    assert e.value.status == 2
+    rlq.check()

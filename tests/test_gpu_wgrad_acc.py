@@ -54,6 +54,36 @@ def test_two_micro_batches_sum():
     _assert_fp32_close(acc, _ref(*a) + _ref(*b), "two micro-batches")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 256, 128), (100, 512, 256), (128, 256, 384), (4096, 2048, 1024)])
+def test_accumulate_from_the_epilogue_without_workspace(M, N, K):
+    """No workspace: the GEMM's epilogue adds each tile's fp32 result into the
+    gradient (single CTAs and CTA pairs, one token block or many)."""
+    qdyT, sdyc, qxT, sxc = _operands(68, M, N, K)
+    rng = np.random.default_rng(69)
+    acc0 = (rng.standard_normal((N, K)) * 1e-2).astype(np.float32)
+    acc = torch.from_numpy(acc0.copy()).cuda()
+    rlq.rlq_gemm_wgrad_accumulate(qdyT.data_ptr(), qdyT.stride(0), sdyc.data_ptr(), sdyc.stride(0), qxT.data_ptr(),
+                                  qxT.stride(0), sxc.data_ptr(), sxc.stride(0), acc.data_ptr(), K, M, N, K, None, 0,
+                                  torch.cuda.current_stream().cuda_stream)
+    rlq.check()
+    ref = _ref(qdyT, sdyc, qxT, sxc)
+    _assert_fp32_close(acc - torch.from_numpy(acc0).cuda(), ref, f"increment {M}x{N}x{K}")
+
+
+def test_epilogue_accumulate_from_zero_rounds_to_the_single_pass_wgrad():
+    """From zero and without a workspace, the fp32 result rounded to bf16 equals the
+    single-pass WGrad's output bit for bit (same promotion order)."""
+    M, N, K = 1024, 512, 768
+    qdyT, sdyc, qxT, sxc = _operands(70, M, N, K)
+    acc = torch.zeros((N, K), dtype=torch.float32, device="cuda")
+    rlq.rlq_gemm_wgrad_accumulate(qdyT.data_ptr(), qdyT.stride(0), sdyc.data_ptr(), sdyc.stride(0), qxT.data_ptr(),
+                                  qxT.stride(0), sxc.data_ptr(), sxc.stride(0), acc.data_ptr(), K, M, N, K, None, 0,
+                                  torch.cuda.current_stream().cuda_stream)
+    dw = rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc)
+    rlq.check()
+    assert torch.equal(acc.to(torch.bfloat16), dw)
+
+
 def test_accumulate_from_zero_rounds_to_the_split_k_wgrad():
     """From a zero gradient with the split-K plan's workspace, the fp32 result rounded
     to bf16 is the split-K WGrad's output bit for bit (same splits, same order)."""
