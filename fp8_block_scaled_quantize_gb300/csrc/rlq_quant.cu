@@ -753,16 +753,40 @@ __global__ void __launch_bounds__(256) k_quant_per_row(const uint16_t *__restric
 //   element     q  = E2M1_RNsat(fl32(x / fl32(decode(sb) * st))), +-0 when that is 0.
 // Three launches: the tensor amax (packed maxima, one atomic max per warp, the
 // bits of a non-negative float ordering as unsigned integers), the block pass
-// (one thread per block), and one thread that turns the amax into st.
+// (one thread per block: IEEE quotients, E2M1 codes by the hardware conversion
+// two at a time), and one thread that turns the amax into st.
 
-// E2M1 code of r: RN-even onto 0, 0.5, 1, 1.5, 2, 3, 4, 6 with saturation; each
-// threshold is a midpoint, strict where the tie goes down to the even code.
-__device__ __forceinline__ uint32_t e2m1_code(float r)
+// E2M1 codes of two values (RN-even onto 0, 0.5, 1, 1.5, 2, 3, 4, 6, saturating at
+// +-6, sign of zero kept), `lo` in bits 0..3 and `hi` in bits 4..7: the hardware
+// conversion, one instruction per pair.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
 {
-    const float a = fabsf(r);
-    const uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-                       (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
-    return c | (signbit(r) ? 8u : 0u);
+    uint32_t d;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(d)
+        : "f"(hi), "f"(lo));
+    return d;
+}
+
+// A quotient that gives the E2M1 code of the IEEE quotient fl32(x / S), for S a
+// normal fp32 value above 2^-100 and r = RN(1 / S).  q0 = RN(x * r) is within 2
+// ulps of x / S (one rounding of the product plus |x| times the reciprocal's half
+// ulp), and fl32(x / S) within half an ulp, so the two can fall on different sides
+// of a rounding point of the E2M1 code only if q0 lies within 3 ulps of one.  Those
+// points are the midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5 and 5 (codes saturate at
+// 6, so nothing above 5 decides anything): each has at most 3 significant bits, i.e.
+// its low 21 mantissa bits are 0 and its biased exponent lies in 125..129.  Every
+// q0 whose magnitude has an exponent in 124..129 and low 21 mantissa bits within 4
+// of a multiple of 2^21 takes the IEEE division instead (exact E2M1 values such as
+// 1.0 take it too, harmlessly); all other quotients keep q0.
+__device__ __forceinline__ float nv_quot(float x, float S, float r)
+{
+    const float q0 = __fmul_rn(x, r);
+    const uint32_t u = __float_as_uint(q0) & 0x7FFFFFFFu;
+    const uint32_t ex = u >> 23;
+    if (ex >= 124u && ex <= 129u && ((u + 4u) & 0x1FFFFFu) <= 8u)
+        return __fdiv_rn(x, S);
+    return q0;
 }
 
 // Exact fp32 value of a finite E4M3 code.
@@ -815,10 +839,19 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const uint16_t *__restrict_
         sb[n * ldsb + kb] = (uint8_t)e;
         const float S = __fmul_rn(e4m3_value(e), st);
         uint32_t word[2] = {0u, 0u};
+        if (S == 0.0f) {  // a block below the format's range: +-0 codes, sign kept
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const uint32_t c = S == 0.0f ? (signbit(f[j]) ? 8u : 0u) : e2m1_code(__fdiv_rn(f[j], S));
-            word[j >> 3] |= c << (4 * (j & 7));
+            for (int j = 0; j < 16; ++j)
+                word[j >> 3] |= (signbit(f[j]) ? 8u : 0u) << (4 * (j & 7));
+        } else if (S < 0x1p-100f) {  // 1 / S may overflow: IEEE quotients throughout
+#pragma unroll
+            for (int j = 0; j < 16; j += 2)
+                word[j >> 3] |= e2m1x2(__fdiv_rn(f[j], S), __fdiv_rn(f[j + 1], S)) << (4 * (j & 7));
+        } else {
+            const float r = __frcp_rn(S);
+#pragma unroll
+            for (int j = 0; j < 16; j += 2)
+                word[j >> 3] |= e2m1x2(nv_quot(f[j], S, r), nv_quot(f[j + 1], S, r)) << (4 * (j & 7));
         }
         *reinterpret_cast<uint2 *>(q + n * ldq + kb * 8) = make_uint2(word[0], word[1]);
     }

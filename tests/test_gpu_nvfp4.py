@@ -68,3 +68,26 @@ def test_nvfp4_pitched():
     rlq.check()
     _check(w, qb[:, :K // 2], sbb[:, :K // 16], st)
     assert torch.all(qb[:, K // 2:] == 0xA5) and torch.all(sbb[:, K // 16:] == 0x5A)
+
+
+def test_nvfp4_midpoint_quotients_under_non_power_of_two_block_scales():
+    """Blocks whose scale decodes to 1.125, 1.25, 1.5 or 1.75 (amax 6.75, 7.5, 9,
+    10.5 with a tensor scale of 1) holding x = m * S for every E2M1 midpoint m:
+    x / S is exactly a midpoint (a tie, to the even code), while x * RN(1 / S) lands
+    an ulp away from it; the codes must still equal the oracle's, which divides."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    blocks = []
+    for S in (1.125, 1.25, 1.5, 1.75):
+        v = np.zeros(16, np.float32)
+        v[0] = 6.0 * S                    # block amax: its scale code decodes to S exactly
+        v[1:8] = mids * S
+        v[8:15] = -mids * S
+        v[15] = 0.375 * S                 # below the first midpoint
+        blocks.append(v)
+    row = np.concatenate(blocks + [np.zeros(16 * 4, np.float32)])
+    row[-1] = 2688.0                      # tensor amax 6 * 448: tensor scale exactly 1
+    w = I.to_bf16_bits(np.tile(row, (4, 1)))
+    assert np.array_equal(oracle.bf16_to_f32(w)[0], row)  # every value exact in bf16
+    q, sb, st = rlq.quant_nvfp4(to_dev(w))
+    rlq.check()
+    _check(w, q, sb, st)
