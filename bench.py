@@ -346,10 +346,31 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def kernel_source_hash(path: str, fn: str) -> str | None:
+    """sha256 (16 hex digits) of the source text that defines kernel `fn`: the file
+    from its start to the closing brace of `fn`'s body, so the helpers above it count
+    and code added after it does not."""
+    import hashlib
+    import re
+    text = open(path, encoding="utf-8").read()
+    m = re.search(r"__global__[^;{]*?\b" + re.escape(fn) + r"\s*\(", text, flags=re.S)
+    if not m:
+        return None
+    i = text.find("{", m.end())
+    depth = 0
+    for j in range(i, len(text)):
+        if text[j] == "{":
+            depth += 1
+        elif text[j] == "}":
+            depth -= 1
+            if depth == 0:
+                return hashlib.sha256(text[:j + 1].encode()).hexdigest()[:16]
+    return None
+
+
 def _load_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when there is none or the kernel source changed since it was captured."""
-    import hashlib
+    when there is none or the kernel's source changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -359,11 +380,10 @@ def _load_traffic(kernel: str):
     if not isinstance(v, dict):
         return None
     src = os.path.join(ROOT, v.get("source", ""))
-    if not os.path.exists(src):
+    if not os.path.exists(src) or not v.get("kernel_fn"):
         return None
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    return v.get("dram_bytes_per_launch") if sha == v.get("source_sha256_16") else None
+    sha = kernel_source_hash(src, v["kernel_fn"])
+    return v.get("dram_bytes_per_launch") if sha is not None and sha == v.get("source_sha256_16") else None
 
 
 def run_e2e(st: Step, host, args, dist, world, flop_step):
@@ -746,7 +766,8 @@ CASE_DOC = """Run one kernel of the path on one shape --case-reps times (after 2
 calls), for profiler captures of a small case: gemm_fprop, gemm_dgrad,
 gemm_dgrad_mn (untransposed weight codes), gemm_wgrad (optionally --split-k), gemm_wgrad_accumulate,
 gemm_fprop_per_channel, gemm_nvfp4, quant_rows, quant_dual,
-rmsnorm_quant, rmsnorm_quant_dual, quant_weight, uaq_fold.  Prints the
+rmsnorm_quant, rmsnorm_quant_dual, quant_weight (with the transposed copy),
+quant_weight_nt (without), uaq_fold.  Prints the
 median CUDA-event time; no JSON line."""
 
 
@@ -805,6 +826,8 @@ def run_case(args):
         fn = lambda: rlq.quant_act_1x128(x, colwise=True)
     elif name == "quant_weight":
         fn = lambda: rlq.quant_weight_128x128(w, transposed=True)
+    elif name == "quant_weight_nt":  # without the transposed copy (the bench step's form)
+        fn = lambda: rlq.quant_weight_128x128(w)
     elif name == "uaq_fold":
         s = torch.full((K,), 1.5, dtype=torch.float32, device=dev)
         fn = lambda: rlq.uaq_fold_(w, s, x)
