@@ -122,6 +122,11 @@ class ClockSampler:
                  "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            # nvidia-smi takes a moment to print its first sample: start the timed
+            # region only once sampling is running (at most 3 s of waiting).
+            t_end = time.time() + 3.0
+            while not self.lines and time.time() < t_end and self.proc.poll() is None:
+                time.sleep(0.01)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -601,16 +606,23 @@ def run_sweep(args):
         q4, sb4, st4 = rlq.quant_nvfp4(w)
         y4 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         nbytes = 2 * M * K + N * K // 2 + N * K // 16 + 2 * M * N
-        ms = _time_ms(lambda: rlq.gemm_nvfp4_weight_only(x, q4, sb4, st4, out=y4), flush)
         flop = 2.0 * M * N * K
-        r = {"sweep": True, "config": cfg, "kernel": "gemm_nvfp4_weight_only", "ms": round(ms, 4),
-             "tflops": round(flop / (ms * 1e-3) / 1e12, 1), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
-        t_roof = max(flop / (peaks["bf16_burst"] * 1e12), nbytes / (bw * 1e9)) * 1e3
-        r["bound"] = "tensor (bf16)" if flop / (peaks["bf16_burst"] * 1e12) >= nbytes / (bw * 1e9) else "hbm"
-        r["frac_roofline"] = round(t_roof / ms, 3)
-        rows.append(r)
-        print(json.dumps(r), flush=True)
-        del q4, sb4, st4, y4
+        ws = _splitk_ws(rlq.GEMM_NVFP4_WEIGHT_ONLY, M, N, K)
+        variants = [("gemm_nvfp4_weight_only", lambda: rlq.gemm_nvfp4_weight_only(x, q4, sb4, st4, out=y4))]
+        if ws is not None:
+            variants.append(("gemm_nvfp4_weight_only_splitk",
+                             lambda: rlq.gemm_nvfp4_weight_only(x, q4, sb4, st4, out=y4, split_k=True,
+                                                                workspace=ws)))
+        for name, fn in variants:
+            ms = _time_ms(fn, flush)
+            r = {"sweep": True, "config": cfg, "kernel": name, "ms": round(ms, 4),
+                 "tflops": round(flop / (ms * 1e-3) / 1e12, 1), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+            t_roof = max(flop / (peaks["bf16_burst"] * 1e12), nbytes / (bw * 1e9)) * 1e3
+            r["bound"] = "tensor (bf16)" if flop / (peaks["bf16_burst"] * 1e12) >= nbytes / (bw * 1e9) else "hbm"
+            r["frac_roofline"] = round(t_roof / ms, 3)
+            rows.append(r)
+            print(json.dumps(r), flush=True)
+        del q4, sb4, st4, y4, ws
 
     def linear(cfg, x, w, dy=None, s=None, full=False, per_channel=False, norm=False, nvfp4=False):
         """Time the quantizers, fold and GEMMs of one linear layer (with
@@ -791,7 +803,7 @@ def run_case(args):
     elif name == "gemm_nvfp4":
         q4, sb4, st4 = rlq.quant_nvfp4(w)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        fn = lambda: rlq.gemm_nvfp4_weight_only(x, q4, sb4, st4, out=y)
+        fn = lambda: rlq.gemm_nvfp4_weight_only(x, q4, sb4, st4, out=y, split_k=args.split_k)
     elif name == "gemm_fprop_per_channel":
         qx, _, sx = rlq.quant_per_row(x)
         qw, _, sw = rlq.quant_per_row(w)

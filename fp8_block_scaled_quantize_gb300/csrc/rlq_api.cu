@@ -423,6 +423,10 @@ rlq_status rlq_gemm_splitk_workspace_bytes(rlq_gemm_kind kind, int64_t M, int64_
     case RLQ_GEMM_WGRAD:
         R = N, C = K, L = M;
         break;
+    case RLQ_GEMM_NVFP4_WEIGHT_ONLY: {
+        int splits = 1;
+        return plan_nvfp4_splitk(M, N, K, -1, &splits, bytes);
+    }
     default:
         return fail(RLQ_ERR_INVALID_ARG, "unknown GEMM kind %d", (int)kind);
     }
@@ -531,9 +535,13 @@ rlq_status rlq_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, const fl
     return cuda_status(launch_uaq_fold(w, N, K, ldw, s, prev, R, ldp, cs(stream)), "UAQ fold launch");
 }
 
-rlq_status rlq_gemm_nvfp4_weight_only(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq,
-                                     const uint8_t *wsb, int64_t ldwsb, const float *wst, uint16_t *y, int64_t ldy,
-                                     int64_t M, int64_t N, int64_t K, rlq_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+rlq_status gemm_nvfp4(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq, const uint8_t *wsb, int64_t ldwsb,
+                      const float *wst, uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K, void *workspace,
+                      int64_t workspace_bytes, rlq_stream_t stream)
 {
     RLQ_REQUIRE(M >= 0 && N >= 0 && K >= 0, RLQ_ERR_INVALID_ARG, "negative size");
     RLQ_REQUIRE(N % G == 0 && K % 64 == 0, RLQ_ERR_UNSUPPORTED,
@@ -550,7 +558,28 @@ rlq_status rlq_gemm_nvfp4_weight_only(const uint16_t *x, int64_t ldx, const uint
     RLQ_TRY(check_codes("wsb", wsb, ldwsb, K / 16));
     RLQ_REQUIRE(wst, RLQ_ERR_INVALID_ARG, "wst is NULL");
     RLQ_REQUIRE(al(wst, 4), RLQ_ERR_MISALIGNED, "wst is not 4-byte aligned");
-    return launch_gemm_nvfp4w(x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, cs(stream));
+    return launch_gemm_nvfp4w(x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, workspace, workspace_bytes,
+                              cs(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+rlq_status rlq_gemm_nvfp4_weight_only(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq,
+                                     const uint8_t *wsb, int64_t ldwsb, const float *wst, uint16_t *y, int64_t ldy,
+                                     int64_t M, int64_t N, int64_t K, rlq_stream_t stream)
+{
+    return gemm_nvfp4(x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, nullptr, 0, stream);
+}
+
+rlq_status rlq_gemm_nvfp4_weight_only_splitk(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq,
+                                            const uint8_t *wsb, int64_t ldwsb, const float *wst, uint16_t *y,
+                                            int64_t ldy, int64_t M, int64_t N, int64_t K, void *workspace,
+                                            int64_t workspace_bytes, rlq_stream_t stream)
+{
+    RLQ_TRY(check_workspace(workspace, workspace_bytes));
+    return gemm_nvfp4(x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, workspace, workspace_bytes, stream);
 }
 
 rlq_status rlq_aqn_sigma(float sigma_start, float sigma_end, int64_t t, int64_t T, float *sigma)

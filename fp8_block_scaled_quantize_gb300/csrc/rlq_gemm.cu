@@ -1064,6 +1064,17 @@ rlq_status plan_splitk(int64_t R, int64_t C, int64_t L, int64_t ws_cap, int *spl
     return RLQ_OK;
 }
 
+rlq_status launch_splitk_reduce(const float *ws, int splits, int64_t R, int64_t C, uint16_t *out, int64_t ldo, int sms,
+                                cudaStream_t st)
+{
+    const int64_t total = R * (C / 8);
+    int64_t rgrid = (total + 255) / 256;
+    if (rgrid > (int64_t)sms * 8)
+        rgrid = (int64_t)sms * 8;
+    k_splitk_reduce<<<(int)rgrid, 256, 0, st>>>(ws, splits, (int)R, (int)C, out, ldo);
+    return cuda_status(cudaGetLastError(), "split-K reduction launch");
+}
+
 rlq_status check_device_errors(cudaStream_t st)
 {
     cudaError_t e = cudaStreamSynchronize(st);

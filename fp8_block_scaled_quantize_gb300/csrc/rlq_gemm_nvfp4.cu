@@ -30,6 +30,10 @@
 //     descriptor (128-byte swizzle).
 //   * warps 20-23 (128 threads, one TMEM lane each): epilogue, tcgen05.ld in 32-
 //     column chunks, times st, rounded to bf16 and stored row by row.
+// Work units: (tile, split) pairs.  With splits > 1 each unit sums a contiguous
+// range of contraction stages (a whole number of raw chunks) and the epilogue
+// writes st times its fp32 sum to plane `split` of the caller's workspace; the
+// split-K reduction then adds the planes in split order and rounds to bf16.
 // Every mbarrier wait is bounded as in the FP8 GEMM: a wait that runs out records
 // an error word (this translation unit's) and raises the CTA's abort flag; the
 // CTA drains its TMA copies, frees TMEM and exits.
@@ -83,11 +87,32 @@ struct NvParams {
     const float *st;  // tensor scale (device)
     uint16_t *y;
     int64_t ldy;
+    float *ws;        // split partials [splits][M][N] fp32 (splits > 1 only)
     int M, N, K;
-    int kstages;      // ceil(K / 64)
+    int kstages;      // K / 64
     int m_tiles, num_tiles;
+    int splits;       // contraction splits per tile (1: no split)
+    int kps;          // stages per split, a multiple of 4 (one raw chunk = 4 stages)
+    int num_units;    // num_tiles * splits
     uint64_t timeout_ns;
 };
+
+// Unit u -> tile (mt, nt) and its stage range [ks0, ks1).
+struct NvUnit {
+    int mt, nt, split, ks0, ks1;
+};
+
+__device__ __forceinline__ NvUnit nv_unit(const NvParams &p, int u)
+{
+    NvUnit w;
+    const int t = u / p.splits;
+    w.split = u - t * p.splits;
+    w.mt = t % p.m_tiles;
+    w.nt = t / p.m_tiles;
+    w.ks0 = w.split * p.kps;
+    w.ks1 = w.ks0 + p.kps < p.kstages ? w.ks0 + p.kps : p.kstages;
+    return w;
+}
 
 __device__ __forceinline__ void nv_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate)
 {
@@ -220,9 +245,10 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
         if (lane == 0) {
             int it = 0, rc = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                const int mt = t % p.m_tiles, nt = t / p.m_tiles;
-                for (int ks = 0; ks < p.kstages; ++ks, ++it) {
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const NvUnit w = nv_unit(p, u);
+                const int mt = w.mt, nt = w.nt;
+                for (int ks = w.ks0; ks < w.ks1; ++ks, ++it) {
                     if ((ks & 3) == 0) {
                         const int r = rc % NV_RAW_SLOTS;
                         if (!mbar_wait(raw_empty(r), ((uint32_t)(rc / NV_RAW_SLOTS) & 1u) ^ 1u, abort_flag,
@@ -233,11 +259,11 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
                         mbar_arrive_expect_tx(raw_full(r), NV_CODE_BYTES + NV_SCALE_BYTES);
                         tma_load_2d(codes_slot(r), &tmQ, raw_full(r), (ks >> 2) * (NV_CHUNK / 2), nt * NV_BN);
                         tma_load_2d(scales_slot(r), &tmS, raw_full(r), (ks >> 2) * (NV_CHUNK / 16), nt * NV_BN);
-                        // start the weight stream a few chunks ahead into L2 (this tile's
+                        // start the weight stream a few chunks ahead into L2 (this unit's
                         // chunks only; the two ring slots alone hold too few bytes in flight
                         // to cover HBM latency)
                         const int ahead = (ks >> 2) + NV_PREFETCH_CHUNKS;
-                        if (ahead * NV_CHUNK < p.K) {
+                        if (4 * ahead < w.ks1) {
                             tma_prefetch_l2(&tmQ, ahead * (NV_CHUNK / 2), nt * NV_BN);
                             tma_prefetch_l2(&tmS, ahead * (NV_CHUNK / 16), nt * NV_BN);
                         }
@@ -270,7 +296,8 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
         if (lane == 0) {
             int it = 0, tc = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++tc) {
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++tc) {
+                const NvUnit w = nv_unit(p, u);
                 const int buf = tc & 1;
                 if (!mbar_wait(tempty(buf), ((uint32_t)(tc >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns,
                                SITE_MMA_TMEM_EMPTY)) {
@@ -278,7 +305,7 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
                     break;
                 }
                 const uint32_t d = tmem_base + (uint32_t)(buf * NV_BN);
-                for (int ks = 0; ks < p.kstages; ++ks, ++it) {
+                for (int ks = w.ks0; ks < w.ks1; ++ks, ++it) {
                     const int s = it % NV_STAGES;
                     const uint32_t ph = (uint32_t)(it / NV_STAGES) & 1u;
                     if (!mbar_wait(a_full(s), ph, abort_flag, p.timeout_ns, SITE_MMA_FULL) ||
@@ -290,9 +317,9 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
                     const uint64_t ad = sw128_desc(a_stage(s)), bd = sw128_desc(b_stage(s));
 #pragma unroll
                     for (int j = 0; j < NV_BK / NV_UMMA_K; ++j)  // +32 bytes along K per MMA
-                        nv_mma(d, ad + 2 * j, bd + 2 * j, (ks > 0 || j > 0) ? 1u : 0u);
+                        nv_mma(d, ad + 2 * j, bd + 2 * j, (ks > w.ks0 || j > 0) ? 1u : 0u);
                     tc_commit(st_empty(s));
-                    if (ks + 1 == p.kstages)
+                    if (ks + 1 == w.ks1)
                         tc_commit(tfull(buf));
                 }
             }
@@ -309,8 +336,9 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
         const uint32_t sw = (uint32_t)(row & 7);
         int it = 0, rc = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-            for (int ks = 0; ks < p.kstages; ++ks, ++it) {
+        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const NvUnit w = nv_unit(p, u);
+            for (int ks = w.ks0; ks < w.ks1; ++ks, ++it) {
                 const int r = rc % NV_RAW_SLOTS;
                 if ((ks & 3) == 0 &&
                     !__all_sync(0xFFFFFFFFu, mbar_wait(raw_full(r), (uint32_t)(rc / NV_RAW_SLOTS) & 1u, abort_flag,
@@ -355,7 +383,7 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(b_full(s));
-                if (qk == 3 || ks + 1 == p.kstages) {  // the raw chunk is read out
+                if (qk == 3 || ks + 1 == w.ks1) {  // the raw chunk is read out
                     if (lane == 0)
                         mbar_arrive(raw_empty(r));
                     ++rc;
@@ -369,8 +397,9 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
         const float st = *p.st;
         const float2 st2 = make_float2(st, st);
         int tc = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tc) {
-            const int mt = t % p.m_tiles, nt = t / p.m_tiles;
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
+            const NvUnit w = nv_unit(p, u);
+            const int mt = w.mt, nt = w.nt;
             const int buf = tc & 1;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull(buf), (uint32_t)(tc >> 1) & 1u, abort_flag, p.timeout_ns,
                                                    SITE_EPI_TMEM_FULL)))
@@ -390,7 +419,19 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
                         mbar_arrive(tempty(buf));
                 }
                 const int col = nt * NV_BN + cc * 32;
-                if (grow < p.M && col < p.N) {
+                if (p.splits > 1) {
+                    if (grow < p.M && col < p.N) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)w.split * p.M + grow) * p.N + col);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const float2 a = __fmul2_rn(
+                                make_float2(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1])), st2);
+                            const float2 b = __fmul2_rn(
+                                make_float2(__uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])), st2);
+                            dst[v] = make_float4(a.x, a.y, b.x, b.y);
+                        }
+                    }
+                } else if (grow < p.M && col < p.N) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)grow * p.ldy + col);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -467,11 +508,71 @@ uint64_t nv_wait_limit_ns()
     return ns;
 }
 
+// Split plan for an [M, N] output with K / 64 contraction stages on `sms` SMs.
+// A unit costs about NV_UNIT_US to start plus NV_STAGE_US per stage (the
+// converter ring's pace on one SM); units run in waves of `sms`; more than one
+// split adds the reduction (launch plus the partials' traffic).  The plan takes
+// the cheapest split count up to 16 whose partials fit ws_cap bytes (-1: no
+// limit), with every split a whole number of raw chunks and none empty.
+constexpr double NV_UNIT_US = 2.0, NV_STAGE_US = 0.65, NV_REDUCE_US = 2.0, NV_REDUCE_BYTES_PER_US = 4.0e6;
+
+void nv_plan(int64_t M, int64_t N, int64_t K, int sms, int64_t ws_cap, int *splits_out, int *kps_out)
+{
+    const int64_t kstages = K / NV_BK;
+    const int64_t tiles = ((M + NV_BM - 1) / NV_BM) * ((N + NV_BN - 1) / NV_BN);
+    int best_s = 1;
+    int64_t best_kps = kstages;
+    double best = 1e300;
+    for (int s = 1; s <= 16; ++s) {
+        int64_t kps = (kstages + s - 1) / s;
+        kps = (kps + 3) / 4 * 4;
+        if (s > 1 && (kstages + kps - 1) / kps != s)
+            continue;  // this count leaves a split empty: a smaller count covers it
+        if (s > 1 && ws_cap >= 0 && (int64_t)s * M * N * 4 > ws_cap)
+            break;
+        const int64_t units = tiles * s;
+        const int64_t waves = (units + sms - 1) / sms;
+        double cost = (double)waves * (NV_UNIT_US + (double)(s == 1 ? kstages : kps) * NV_STAGE_US);
+        if (s > 1)
+            cost += NV_REDUCE_US + (double)(s + 1) * (double)M * (double)N * 4.0 / NV_REDUCE_BYTES_PER_US;
+        if (cost < best) {
+            best = cost;
+            best_s = s;
+            best_kps = s == 1 ? kstages : kps;
+        }
+    }
+    *splits_out = best_s;
+    *kps_out = (int)best_kps;
+}
+
+rlq_status nv_sms(int *sms)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    return e == cudaSuccess ? RLQ_OK : cuda_status(e, "device query");
+}
+
 }  // namespace
+
+rlq_status plan_nvfp4_splitk(int64_t M, int64_t N, int64_t K, int64_t ws_cap, int *splits, int64_t *ws_bytes)
+{
+    int sms = 0, kps = 0;
+    const rlq_status rs = nv_sms(&sms);
+    if (rs != RLQ_OK)
+        return rs;
+    int s = 1;
+    if (M > 0 && N > 0 && K > 0)
+        nv_plan(M, N, K, sms, ws_cap, &s, &kps);
+    *splits = s;
+    *ws_bytes = s > 1 ? (int64_t)s * M * N * 4 : 0;
+    return RLQ_OK;
+}
 
 rlq_status launch_gemm_nvfp4w(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq, const uint8_t *wsb,
                               int64_t ldwsb, const float *st, uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
-                              cudaStream_t stream)
+                              void *workspace, int64_t workspace_bytes, cudaStream_t stream)
 {
     CUtensorMap tmX, tmQ, tmS;
     rlq_status rs = nv_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, NV_BK, NV_BM,
@@ -503,16 +604,25 @@ rlq_status launch_gemm_nvfp4w(const uint16_t *x, int64_t ldx, const uint8_t *wq,
     p.st = st;
     p.y = y;
     p.ldy = ldy;
+    p.ws = static_cast<float *>(workspace);
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
-    p.kstages = (int)((K + NV_BK - 1) / NV_BK);
+    p.kstages = (int)(K / NV_BK);
     p.m_tiles = (int)((M + NV_BM - 1) / NV_BM);
     p.num_tiles = p.m_tiles * (int)((N + NV_BN - 1) / NV_BN);
+    p.splits = 1;
+    p.kps = p.kstages;
+    if (workspace)
+        nv_plan(M, N, K, sms, workspace_bytes, &p.splits, &p.kps);
+    p.num_units = p.num_tiles * p.splits;
     p.timeout_ns = nv_wait_limit_ns();
-    const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+    const int grid = p.num_units < sms ? p.num_units : sms;
     k_gemm_nvfp4w<<<grid, NV_THREADS, NV_SMEM, stream>>>(tmX, tmQ, tmS, p);
-    return cuda_status(cudaGetLastError(), "NVFP4 GEMM launch");
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.splits == 1)
+        return cuda_status(e, "NVFP4 GEMM launch");
+    return launch_splitk_reduce(p.ws, p.splits, M, N, y, ldy, sms, stream);
 }
 
 cudaError_t take_nvfp4_error_word(cudaStream_t st, unsigned long long *word) { return take_error_word(st, word); }

@@ -83,9 +83,19 @@ rlq_status launch_gemm(const GemmArgs &a, cudaStream_t st);
 // Y[M, N] = bf16(st * X W^T), X bf16 [M, K] (pitch ldx elements), W from packed
 // E2M1 codes wq [N, K/2] (pitch ldwq bytes) and E4M3 block scales wsb [N, K/16]
 // (pitch ldwsb bytes), st one fp32 in device memory.  K % 64 == 0, K > 0.
+// workspace (16-byte aligned, or NULL for one pass) holds the split plan's fp32
+// partials; the plan is lowered until they fit workspace_bytes.
 rlq_status launch_gemm_nvfp4w(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq, const uint8_t *wsb,
                               int64_t ldwsb, const float *st, uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
-                              cudaStream_t stream);
+                              void *workspace, int64_t workspace_bytes, cudaStream_t stream);
+// Split count and workspace bytes (splits * M * N * 4, or 0 for one pass) of the
+// NVFP4 GEMM's split plan on the current device; ws_cap limits the workspace
+// (-1: no limit).
+rlq_status plan_nvfp4_splitk(int64_t M, int64_t N, int64_t K, int64_t ws_cap, int *splits, int64_t *ws_bytes);
+// out[r, c] = bf16_RN(sum over s < splits, in order, of ws[(s * R + r) * C + c]),
+// C % 8 == 0, on `sms` SMs' worth of blocks at most.
+rlq_status launch_splitk_reduce(const float *ws, int splits, int64_t R, int64_t C, uint16_t *out, int64_t ldo, int sms,
+                                cudaStream_t st);
 
 // Number of contraction splits the split-K GEMM uses for an [R x C] output
 // with contraction length L on the current device, and the workspace bytes

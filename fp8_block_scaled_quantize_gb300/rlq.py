@@ -42,6 +42,7 @@ _SIGS = {
     "rlq_gemm_wgrad_accumulate": [_P, _I, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_quant_nvfp4": [_P, _I, _I, _I, _P, _I, _P, _I, _P, _P],
     "rlq_gemm_nvfp4_weight_only": [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _P],
+    "rlq_gemm_nvfp4_weight_only_splitk": [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _P, _I, _P],
     "rlq_aqn_sigma": [ctypes.c_float, ctypes.c_float, _I, _I, ctypes.POINTER(ctypes.c_float)],
     "rlq_aqn_perturb": [_P, _I, _P, ctypes.c_float, _P],
     "rlq_check": [_P],
@@ -126,7 +127,7 @@ def rlq_gemm_wgrad(dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw,
     return _call("rlq_gemm_wgrad", dyqT, lddyqT, dysc, lddysc, xqT, ldxqT, xsc, ldxsc, dw, lddw, M, N, K, stream)
 
 
-GEMM_FPROP, GEMM_DGRAD, GEMM_WGRAD = 0, 1, 2
+GEMM_FPROP, GEMM_DGRAD, GEMM_WGRAD, GEMM_NVFP4_WEIGHT_ONLY = 0, 1, 2, 3
 
 
 def rlq_gemm_splitk_workspace_bytes(kind, M, N, K) -> int:
@@ -190,6 +191,12 @@ def rlq_quant_nvfp4(w, N, K, ldw, q, ldq, sb, ldsb, st, stream):
 
 def rlq_gemm_nvfp4_weight_only(x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, stream):
     return _call("rlq_gemm_nvfp4_weight_only", x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, stream)
+
+
+def rlq_gemm_nvfp4_weight_only_splitk(x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, workspace,
+                                      workspace_bytes, stream):
+    return _call("rlq_gemm_nvfp4_weight_only_splitk", x, ldx, wq, ldwq, wsb, ldwsb, wst, y, ldy, M, N, K, workspace,
+                 workspace_bytes, stream)
 
 
 def rlq_aqn_sigma(sigma_start, sigma_end, t, T) -> float:
@@ -462,16 +469,25 @@ def quant_nvfp4(w: torch.Tensor, stream=None):
     return q, sb, st
 
 
-def gemm_nvfp4_weight_only(x: torch.Tensor, q, sb, st, out=None, stream=None):
+def gemm_nvfp4_weight_only(x: torch.Tensor, q, sb, st, out=None, stream=None, split_k: bool = False,
+                           workspace=None):
     """Y [M, N] bf16 = X W^T with bf16 X [M, K] and NVFP4 weights (the outputs of
-    ``quant_nvfp4``: q [N, K/2] packed E2M1, sb [N, K/16] E4M3, st [1] f32)."""
+    ``quant_nvfp4``: q [N, K/2] packed E2M1, sb [N, K/16] E4M3, st [1] f32).
+
+    ``split_k`` runs the split-K form with ``workspace`` (a uint8 device tensor)
+    or a workspace allocated here for the library's plan."""
     if x.dtype != torch.bfloat16:
         raise TypeError("x must be bfloat16")
     M, K = x.shape
     N = q.shape[0]
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    rlq_gemm_nvfp4_weight_only(x.data_ptr(), _ld(x), q.data_ptr(), q.stride(0), sb.data_ptr(), sb.stride(0),
-                               st.data_ptr(), y.data_ptr(), _ld(y), M, N, K, _stream(stream))
+    args = (x.data_ptr(), _ld(x), q.data_ptr(), q.stride(0), sb.data_ptr(), sb.stride(0), st.data_ptr(),
+            y.data_ptr(), _ld(y), M, N, K)
+    if split_k:
+        rlq_gemm_nvfp4_weight_only_splitk(*args, *_workspace(GEMM_NVFP4_WEIGHT_ONLY, M, N, K, workspace, x.device),
+                                          _stream(stream))
+    else:
+        rlq_gemm_nvfp4_weight_only(*args, _stream(stream))
     return y
 
 

@@ -322,6 +322,30 @@ rlq_status rlq_gemm_nvfp4_weight_only(const uint16_t *x, int64_t ldx, const uint
                                       int64_t ldy, int64_t M, int64_t N, int64_t K, rlq_stream_t stream);
 
 /*
+ * Split-K form of the NVFP4 weight-only GEMM, for decode-sized M, where the
+ * output has fewer 128 x 256 tiles than the GPU has SMs (a layer with few
+ * output channels and a long contraction leaves most SMs idle otherwise).  A
+ * scheduling choice of this library; the pages prescribe no tiling.  Each
+ * split sums a contiguous range of K (a multiple of 256 elements) in fp32 on
+ * the tensor cores, multiplies its sum by st, and the split results are added
+ * in split order in fp32 and rounded to bf16 once:
+ *
+ *   Y[m, n] = bf16_RN( sum over splits s, in order, of fl32(st * S_s[m, n]) )
+ *
+ * Deterministic (no atomics); it may differ from the single-pass call in the
+ * last bits of the fp32 sum.  workspace and workspace_bytes as for the FP8
+ * split-K calls (caller-owned, 16-byte aligned or NULL for one pass; the plan
+ * is lowered until splits * M * N * 4 bytes fit); the unconstrained plan's
+ * size comes from rlq_gemm_splitk_workspace_bytes(RLQ_GEMM_NVFP4_WEIGHT_ONLY,
+ * M, N, K).  Other arguments, shapes and errors as for
+ * rlq_gemm_nvfp4_weight_only.
+ */
+rlq_status rlq_gemm_nvfp4_weight_only_splitk(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq,
+                                            const uint8_t *wsb, int64_t ldwsb, const float *wst, uint16_t *y,
+                                            int64_t ldy, int64_t M, int64_t N, int64_t K, void *workspace,
+                                            int64_t workspace_bytes, rlq_stream_t stream);
+
+/*
  * AQN, adaptive quantization noise (QeRL news article: channel-wise Gaussian
  * perturbations mapped into the LayerNorm scale parameters, decaying on an
  * exponential schedule).  The pages give no formula; the one used here:
@@ -368,7 +392,12 @@ rlq_status rlq_aqn_perturb(uint16_t *gamma, int64_t K, const float *z, float sig
  * unconstrained plan uses on the current device for that GEMM and shape
  * (0 when the plan is one pass).
  */
-typedef enum { RLQ_GEMM_FPROP = 0, RLQ_GEMM_DGRAD = 1, RLQ_GEMM_WGRAD = 2 } rlq_gemm_kind;
+typedef enum {
+    RLQ_GEMM_FPROP = 0,
+    RLQ_GEMM_DGRAD = 1,
+    RLQ_GEMM_WGRAD = 2,
+    RLQ_GEMM_NVFP4_WEIGHT_ONLY = 3 /* rlq_gemm_nvfp4_weight_only_splitk; M, N, K as in that call */
+} rlq_gemm_kind;
 
 rlq_status rlq_gemm_splitk_workspace_bytes(rlq_gemm_kind kind, int64_t M, int64_t N, int64_t K,
                                            int64_t *bytes);

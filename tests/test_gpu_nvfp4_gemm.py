@@ -159,3 +159,102 @@ def test_empty_contraction_and_validation():
                                        y.data_ptr(), 128, 4, 128, 96, 0)
     assert e.value.status == 2
     rlq.check()
+
+
+def _ws(M, N, K):
+    nb = rlq.rlq_gemm_splitk_workspace_bytes(rlq.GEMM_NVFP4_WEIGHT_ONLY, M, N, K)
+    return nb, (torch.empty(nb, dtype=torch.uint8, device="cuda") if nb else None)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 4096), (16, 256, 8192), (130, 384, 2048), (1, 128, 4288),
+                                   (7, 640, 3392)])
+def test_splitk_parity(M, N, K):
+    """Shapes whose output has far fewer tiles than the GPU has SMs: the plan
+    splits K (asserted), including splits whose last range is not a whole raw
+    chunk (K / 64 = 67 and 53 stages)."""
+    nb, ws = _ws(M, N, K)
+    assert nb > 0 and nb % (4 * M * N) == 0, nb
+    x = normal_bits(93, (M, K), 1.0, "x")
+    w = normal_bits(93, (N, K), 0.02, "w")
+    (q, sb, st), (oq, osb, ost) = _quantized_weight(w)
+    y = rlq.gemm_nvfp4_weight_only(to_dev(x), q, sb, st, split_k=True, workspace=ws)
+    y1 = rlq.gemm_nvfp4_weight_only(to_dev(x), q, sb, st)
+    rlq.check()
+    ref = oracle.gemm_nvfp4_weight_only(x, oq, osb, ost)
+    assert_gemm_close(y, ref, f"split-K NVFP4 GEMM {M}x{N}x{K} ({nb // (4 * M * N)} splits)")
+    assert_gemm_close(y1, ref, f"NVFP4 GEMM {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 128, 4288), (64, 256, 8192)])
+def test_splitk_integer_case_bit_exact(M, N, K):
+    """The exact integer case of test_integer_case_bit_exact under a split plan:
+    every split sum and their total are exact, so the split and single-pass
+    outputs both equal the exact result rounded to bf16."""
+    nb, ws = _ws(M, N, K)
+    assert nb > 0
+    rng = np.random.default_rng(M * 7 + K)
+    x = I.to_bf16_bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
+    q = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    sb = rng.choice(np.array([0x30, 0x38, 0x40], np.uint8), size=(N, K // 16))
+    ref = oracle.gemm_nvfp4_weight_only(x, q, sb, 1.0)
+    assert np.all(ref * 4 == np.round(ref * 4)) and np.all(np.abs(ref) < 2 ** 17)
+    qp, sbd = _padded(_pack(q)), _padded(sb)
+    st = torch.ones(1, dtype=torch.float32, device="cuda")
+    y = rlq.gemm_nvfp4_weight_only(to_dev(x), qp, sbd, st, split_k=True, workspace=ws)
+    y1 = rlq.gemm_nvfp4_weight_only(to_dev(x), qp, sbd, st)
+    rlq.check()
+    exact = I.to_bf16_bits(ref.astype(np.float32))
+    assert np.array_equal(u16(y), exact)
+    assert np.array_equal(u16(y1), exact)
+
+
+@pytest.mark.parametrize("case", ["32b_down_m1", "32b_down_m16", "qwen7b_down_m64"])
+def test_splitk_down_projections(case):
+    """The down projections at decode sizes (few output tiles, long contraction:
+    the case the split plan is for)."""
+    if case.startswith("32b"):
+        M = int(case.split("_m")[1])
+        d = I.sweep_32b(M, "down", with_dy=False)
+    else:
+        M = 64
+        d = I.qwen7b_layer(M, "down")
+    N, K = d["w"].shape
+    nb, ws = _ws(M, N, K)
+    assert nb > 0
+    (q, sb, st), (oq, osb, ost) = _quantized_weight(d["w"])
+    y = rlq.gemm_nvfp4_weight_only(to_dev(d["x"]), q, sb, st, split_k=True, workspace=ws)
+    rlq.check()
+    cols = strata(N, 64, np.random.default_rng(5))
+    ref = oracle.gemm_nvfp4_weight_only(d["x"], oq, osb, ost, cols=cols)
+    assert_gemm_close(y[:, idx(cols)], ref, f"split-K NVFP4 GEMM {case} ({nb // (4 * M * N)} splits)")
+
+
+def test_splitk_workspace_limits():
+    """A workspace smaller than the plan's lowers the split count (still within
+    tolerance); none runs the single pass, bit-equal to the plain call; a
+    misaligned workspace is rejected before any launch."""
+    M, N, K = 16, 256, 8192
+    nb, ws = _ws(M, N, K)
+    splits = nb // (4 * M * N)
+    assert splits >= 3
+    x = normal_bits(94, (M, K), 1.0, "x")
+    w = normal_bits(94, (N, K), 0.02, "w")
+    (q, sb, st), (oq, osb, ost) = _quantized_weight(w)
+    xd = to_dev(x)
+    ref = oracle.gemm_nvfp4_weight_only(x, oq, osb, ost)
+    small = torch.empty(2 * 4 * M * N, dtype=torch.uint8, device="cuda")
+    y2 = rlq.gemm_nvfp4_weight_only(xd, q, sb, st, split_k=True, workspace=small)
+    y1 = rlq.gemm_nvfp4_weight_only(xd, q, sb, st)
+    y0 = torch.empty_like(y1)
+    rlq.rlq_gemm_nvfp4_weight_only_splitk(xd.data_ptr(), K, q.data_ptr(), q.stride(0), sb.data_ptr(), sb.stride(0),
+                                          st.data_ptr(), y0.data_ptr(), N, M, N, K, None, 0,
+                                          torch.cuda.current_stream().cuda_stream)
+    rlq.check()
+    assert_gemm_close(y2, ref, "split-K NVFP4 GEMM with a 2-split workspace")
+    assert torch.equal(y0, y1)
+    with pytest.raises(rlq.RlqError) as e:
+        rlq.rlq_gemm_nvfp4_weight_only_splitk(xd.data_ptr(), K, q.data_ptr(), q.stride(0), sb.data_ptr(),
+                                              sb.stride(0), st.data_ptr(), y0.data_ptr(), N, M, N, K,
+                                              ws.data_ptr() + 4, nb - 16, torch.cuda.current_stream().cuda_stream)
+    assert e.value.status == 3
+    rlq.check()
