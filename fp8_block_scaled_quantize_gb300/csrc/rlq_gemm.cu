@@ -55,8 +55,7 @@ namespace rlq {
 namespace {
 
 constexpr int BM = 128;                    // tile rows (TMEM lanes)
-constexpr int BN = 256;                    // tile columns (MMA N) of the wide tiles
-constexpr int BN_NARROW = 160;             // tile columns of the narrow tiles (three TMEM buffers)
+constexpr int BN = 256;                    // tile columns (MMA N)
 constexpr int BK = 128;                    // contraction block = scale granularity = 128 bytes of E4M3
 constexpr int UMMA_K = 32;                 // K of one kind::f8f6f4 MMA
 constexpr int A_BYTES = BM * BK;           // 16 KB
@@ -69,7 +68,7 @@ constexpr int FIRST_EPI_WARP = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int REGS_PRODUCER = 40;
 constexpr int REGS_EPILOGUE = 232;
-constexpr int TMEM_COLS = 512;             // all of TMEM: 2 x 256 or 3 x 160 partial buffers
+constexpr int TMEM_COLS = 2 * BN;          // two partial buffers
 constexpr int SCALE_SLOTS = 8;             // scale ring depth (contraction blocks)
 constexpr int SLOT_FLOATS = BM + BN;       // 128 row scales + up to 256 column scales
 constexpr int RING_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
@@ -95,32 +94,15 @@ constexpr int STG_COLS = RLQ_STG_COLS;            // bf16 columns per staged sto
 constexpr int STG_WARP_BYTES = 32 * STG_COLS * 2;  // one warp's staging buffer
 static_assert(STG_COLS == 64 || STG_COLS == 128, "staged rounds of 64 or 128 columns");
 
-#ifndef RLQ_NARROW_STAGES
-#define RLQ_NARROW_STAGES 6
-#endif
-#ifndef RLQ_NARROW_EARLY_RELEASE
-#define RLQ_NARROW_EARLY_RELEASE 1
-#endif
-
-// kBN = 256: wide tiles, two TMEM buffers.  kBN = 160 (CTA pairs, K-major B only):
-// narrow tiles, three TMEM buffers, so that a buffer's epilogue and release have
-// two blocks of MMAs to hide behind instead of one; each epilogue thread holds 80
-// columns and reads a block's partial with one wait.
-template <bool kPair, int kBN = BN>
+template <bool kPair>
 struct Cfg {
-    static_assert(kBN == BN || (kBN == BN_NARROW && kPair), "narrow tiles run on CTA pairs");
-    static constexpr int NBUF = TMEM_COLS / kBN;        // TMEM partial buffers
-    static constexpr int EPI_COLS = kBN / 2;            // columns per epilogue thread
-    static constexpr int STAGES = kBN == BN_NARROW ? RLQ_NARROW_STAGES : (kPair ? RLQ_PAIR_STAGES : 4);
-    // narrow tiles: one warp stages its 32 rows x 80 columns (160-byte rows, no swizzle)
-    static constexpr int STG_BYTES_WARP = kBN == BN_NARROW ? 32 * EPI_COLS * 2 : STG_WARP_BYTES;
-    static constexpr int STAGING = kPair ? NUM_EPI_WARPS * STG_BYTES_WARP : 0;
-    static constexpr int B_ROWS = kPair ? kBN / 2 : kBN;  // B rows (output columns) staged per CTA
+    static constexpr int STAGES = kPair ? RLQ_PAIR_STAGES : 4;
+    static constexpr int STAGING = kPair ? NUM_EPI_WARPS * STG_WARP_BYTES : 0;
+    static constexpr int B_ROWS = kPair ? BN / 2 : BN;  // B rows (output columns) staged per CTA
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static_assert(STAGE_BYTES % 1024 == 0, "stages stay aligned to the 128-byte swizzle atom");
     static constexpr int TILE_M = kPair ? 2 * BM : BM;  // output rows per tile
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 1 + 2 * SCALE_SLOTS;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 2 * SCALE_SLOTS;
     static constexpr int SMEM_BYTES =
         1024 /* alignment slack */ + STAGES * STAGE_BYTES + STAGING + RING_BYTES + NUM_BARS * 8 + 16;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -128,7 +110,7 @@ struct Cfg {
     // B E4M3 (format 0 in bits 7-9 / 10-12), A K-major (bit 15 = 0), B K-major (bit
     // 16 = 0) or MN-major (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28
     // (M = 256 for a CTA pair).
-    static constexpr uint32_t IDESC_BK = (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(TILE_M >> 4) << 24);
+    static constexpr uint32_t IDESC_BK = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(TILE_M >> 4) << 24);
     static constexpr uint32_t IDESC_BMN = IDESC_BK | (1u << 16);
 };
 
@@ -194,28 +176,6 @@ __device__ __forceinline__ void promote_chunk_cols(float2 *acc, const uint32_t (
 {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float4 sb4 = lds_v4(sbs + 16u * j);
-        const float2 s01 = __fmul2_rn(sa2, make_float2(sb4.x, sb4.y));
-        const float2 s23 = __fmul2_rn(sa2, make_float2(sb4.z, sb4.w));
-        acc[2 * j] = __ffma2_rn(f2_of(r[4 * j], r[4 * j + 1]), s01, acc[2 * j]);
-        acc[2 * j + 1] = __ffma2_rn(f2_of(r[4 * j + 2], r[4 * j + 3]), s23, acc[2 * j + 1]);
-    }
-}
-
-// acc[0 .. N/2-1] += r[0 .. N-1] * scale (N columns, two per packed FMA).
-template <int N>
-__device__ __forceinline__ void promote_n(float2 *acc, const uint32_t *r, float2 scl)
-{
-#pragma unroll
-    for (int j = 0; j < N / 2; ++j)
-        acc[j] = __ffma2_rn(f2_of(r[2 * j], r[2 * j + 1]), scl, acc[j]);
-}
-
-// promote_chunk_cols for 16 columns.
-__device__ __forceinline__ void promote_chunk_cols16(float2 *acc, const uint32_t (&r)[16], float2 sa2, uint32_t sbs)
-{
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
         const float4 sb4 = lds_v4(sbs + 16u * j);
         const float2 s01 = __fmul2_rn(sa2, make_float2(sb4.x, sb4.y));
         const float2 s23 = __fmul2_rn(sa2, make_float2(sb4.z, sb4.w));
@@ -297,22 +257,16 @@ enum : int { MODE_BLOCK = 0, MODE_COLS = 1, MODE_ONCE = 2 };
 // Epilogue outputs.
 enum : int { OUT_BF16 = 0, OUT_F32_PARTIAL = 1, OUT_F32_ACC = 2 };
 
-template <int kMode, bool kBMajorMN, bool kPair, int kBN = BN>
+template <int kMode, bool kBMajorMN, bool kPair>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_block_scaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const Params p)
 {
-    using Cf = Cfg<kPair, kBN>;
+    using Cf = Cfg<kPair>;
     constexpr int STAGES = Cf::STAGES;
     constexpr int STAGE_BYTES = Cf::STAGE_BYTES;
     constexpr int NUM_BARS = Cf::NUM_BARS;
-    constexpr int NBUF = Cf::NBUF;
     constexpr bool kOnce = kMode == MODE_ONCE;
-    constexpr bool kNarrow = kBN == BN_NARROW;
-    static_assert(!kNarrow || (!kBMajorMN && kMode != MODE_ONCE), "narrow tiles: K-major B, per-block scales");
-    // TMEM buffer of the n-th block (or unit) and the parity of its use
-    auto buf_of = [](int n) { return (int)((uint32_t)n % (uint32_t)NBUF); };
-    auto use_of = [](int n) { return ((uint32_t)n / (uint32_t)NBUF) & 1u; };
     // A CTA pair (cluster of 2) shares one 256-row tile: CTA `rank` owns rows
     // rank * 128 .. rank * 128 + 127 of it; the even CTA issues the pair's MMAs.
     // (The rank is re-read where it is used rather than kept in a register.)
@@ -333,17 +287,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
     auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
     auto tfull_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + b]); };
-    auto tempty_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + NBUF + b]); };
-    const uint32_t teardown_bar = smem_u32(&bars[2 * STAGES + 2 * NBUF]);
-    auto sfull_bar = [&](int k) { return smem_u32(&bars[2 * STAGES + 2 * NBUF + 1 + k]); };
-    auto sempty_bar = [&](int k) { return smem_u32(&bars[2 * STAGES + 2 * NBUF + 1 + SCALE_SLOTS + k]); };
+    auto tempty_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + 2 + b]); };
+    const uint32_t teardown_bar = smem_u32(&bars[2 * STAGES + 4]);
+    auto sfull_bar = [&](int k) { return smem_u32(&bars[2 * STAGES + 5 + k]); };
+    auto sempty_bar = [&](int k) { return smem_u32(&bars[2 * STAGES + 5 + SCALE_SLOTS + k]); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);  // the stage is free once its MMAs completed
         }
-        for (int b = 0; b < NBUF; ++b) {
+        for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
             // a pair's buffer is free once the epilogue warps of both CTAs released it
             mbar_init(tempty_bar(b), kPair ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
@@ -411,9 +365,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             mbar_arrive_expect_tx(full_bar(s), 2 * STAGE_BYTES);
                         tma_load_2d_pair(a_stage(s), &tmA, fb, kb * BK, mt * Cf::TILE_M + row_offset<kPair>());
                         if (kBMajorMN)  // this CTA's 128 output columns: one 128 x 128 box
-                            tma_load_2d_pair(b_stage(s), &tmB, fb, nt * kBN + row_offset<kPair>(), kb * BK);
-                        else  // this CTA's half of the tile's B rows
-                            tma_load_2d_pair(b_stage(s), &tmB, fb, kb * BK, nt * kBN + (int)cta_rank() * Cf::B_ROWS);
+                            tma_load_2d_pair(b_stage(s), &tmB, fb, nt * BN + row_offset<kPair>(), kb * BK);
+                        else
+                            tma_load_2d_pair(b_stage(s), &tmB, fb, kb * BK, nt * BN + row_offset<kPair>());
                     } else {
                         if (p.withhold_first_load && it == 0)
                             continue;  // nothing arrives on this stage's barrier
@@ -421,10 +375,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_2d(a_stage(s), &tmA, full_bar(s), kb * BK, mt * BM);
                         if (kBMajorMN) {
                             // B stored [contraction][output]: two 128-column boxes of 128 rows
-                            tma_load_2d(b_stage(s), &tmB, full_bar(s), nt * kBN, kb * BK);
-                            tma_load_2d(b_stage(s) + Cf::B_BYTES / 2, &tmB, full_bar(s), nt * kBN + 128, kb * BK);
+                            tma_load_2d(b_stage(s), &tmB, full_bar(s), nt * BN, kb * BK);
+                            tma_load_2d(b_stage(s) + Cf::B_BYTES / 2, &tmB, full_bar(s), nt * BN + 128, kb * BK);
                         } else {
-                            tma_load_2d(b_stage(s), &tmB, full_bar(s), kb * BK, nt * kBN);
+                            tma_load_2d(b_stage(s), &tmB, full_bar(s), kb * BK, nt * BN);
                         }
                     }
                 }
@@ -470,8 +424,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int u = unit0; ok && u < p.num_units; u += unit_step, ++uc) {
                 const Unit w = unit_of(p, u);
                 if (kOnce) {
-                    const uint32_t bph = use_of(uc);
-                    if (!mbar_wait(tempty_bar(buf_of(uc)), bph ^ 1u, abort_flag, p.timeout_ns, SITE_MMA_TMEM_EMPTY)) {
+                    const uint32_t bph = (uint32_t)(uc >> 1) & 1u;
+                    if (!mbar_wait(tempty_bar(uc & 1), bph ^ 1u, abort_flag, p.timeout_ns, SITE_MMA_TMEM_EMPTY)) {
                         ok = false;
                         break;
                     }
@@ -481,9 +435,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         continue;
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                    const int buf = kOnce ? buf_of(uc) : buf_of(it);
+                    const int buf = kOnce ? (uc & 1) : (it & 1);
                     if (!kOnce) {
-                        const uint32_t bph = use_of(it);
+                        const uint32_t bph = (uint32_t)(it >> 1) & 1u;
                         if (!mbar_wait(tempty_bar(buf), bph ^ 1u, abort_flag, p.timeout_ns, SITE_MMA_TMEM_EMPTY)) {
                             ok = false;
                             break;
@@ -494,7 +448,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d = tmem_base + (uint32_t)(buf * kBN);
+                    const uint32_t d = tmem_base + (uint32_t)(buf * BN);
                     const uint64_t ad = sw128_desc(a_stage(s));
                     const uint64_t bd = kBMajorMN ? sw128_desc_mn(b_stage(s)) : sw128_desc(b_stage(s));
                     const bool first = !kOnce || kb == w.kb0;
@@ -545,19 +499,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (kMode != MODE_BLOCK) {
                     const float *sb_row = p.sb + (int64_t)kb * p.sb_bstride;
-                    // the tile's kBN column scales as kBN / 4 aligned 16-byte pieces (rows of
-                    // sb are 16-byte aligned, C % 128 == 0: a piece is wholly inside or
-                    // outside the tensor)
+                    // 256 column scales as 64 aligned 16-byte pieces (rows of sb are 16-byte
+                    // aligned, C % 128 == 0: a piece is wholly inside or outside the tensor)
 #pragma unroll
-                    for (int j = 0; j < (kBN + 127) / 128; ++j) {
-                        const int piece = lane + 32 * j;
-                        const int c = nt * kBN + 4 * piece;
-                        if (piece < kBN / 4)
-                            cp_async16(slot + 4u * (BM + 4 * piece), c < p.C ? sb_row + c : sb_row, c < p.C ? 16u : 0u);
+                    for (int j = 0; j < BN / 128; ++j) {
+                        const int c = nt * BN + 4 * (lane + 32 * j);
+                        cp_async16(slot + 4u * (BM + 4 * (lane + 32 * j)), c < p.C ? sb_row + c : sb_row,
+                                   c < p.C ? 16u : 0u);
                     }
-                } else if (lane < 2) {
-                    // the (at most two) 128-column scale blocks the tile's columns fall in
-                    const int c = (((nt * kBN) >> 7) + lane) * 128;
+                } else if (lane < BN / 128) {
+                    const int c = nt * BN + lane * 128;
                     const float *src = p.sb + (int64_t)kb * p.sb_bstride + (int64_t)(c >> 7) * p.sb_cstride;
                     cp_async4(slot + 4u * (BM + lane), c < p.C ? src : p.sb, c < p.C ? 4u : 0u);
                 }
@@ -574,162 +525,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         int it = 0, uc = 0;
         bool ok = true;
-        if constexpr (kNarrow) {
-        // Narrow tiles: a thread holds its row's 80 columns of the tile; each block's
-        // partial is read with three tcgen05.ld (32 + 32 + 16 columns) and one wait.
-        constexpr int NC = Cf::EPI_COLS;
-        for (int u = unit0; ok && u < p.num_units; u += unit_step) {
-            const Unit wu = unit_of(p, u);
-            const int mt = wu.mt, nt = wu.nt;
-            const int col0 = nt * kBN + h * NC;
-            const int sblk0 = (nt * kBN) >> 7;  // the tile's first 128-column scale block
-            float2 acc[NC / 2];
-#pragma unroll
-            for (int j = 0; j < NC / 2; ++j)
-                acc[j] = make_float2(0.0f, 0.0f);
-            for (int kb = wu.kb0; kb < wu.kb1; ++kb, ++it) {
-                const int buf = buf_of(it);
-                const uint32_t bph = use_of(it);
-                const int k = it % SCALE_SLOTS;
-                const bool w = mbar_wait(sfull_bar(k), (uint32_t)(it / SCALE_SLOTS) & 1u, abort_flag, p.timeout_ns,
-                                         SITE_EPI_SCALE_FULL) &&
-                               mbar_wait(tfull_bar(buf), bph, abort_flag, p.timeout_ns, SITE_EPI_TMEM_FULL);
-                if (!__all_sync(0xFFFFFFFFu, w)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t slot = smem_u32(ring) + (uint32_t)(k * SLOT_FLOATS * 4);
-                const float sa = lds_f32(slot + 4u * row);
-                // Every load starts at a TMEM column that is a multiple of its width:
-                // half 0 reads columns 0-31, 32-63, 64-79 of the buffer (x32, x32, x16),
-                // half 1 reads 80-95, 96-127, 128-159 (x16, x32, x32); buffers start at
-                // columns 0, 160 and 320.
-                const uint32_t tbuf = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN);
-                uint32_t ra[32], rb[32], rc[16];
-                if (h == 0) {
-                    tmem_ld32_async(tbuf, ra);
-                    tmem_ld32_async(tbuf + 32, rb);
-                    tmem_ld16_async(tbuf + 64, rc);
-                } else {
-                    tmem_ld16_async(tbuf + 80, rc);
-                    tmem_ld32_async(tbuf + 96, ra);
-                    tmem_ld32_async(tbuf + 128, rb);
-                }
-                tmem_wait32(ra);
-                tmem_tie32(rb);
-                tmem_tie16(rc);
-#if RLQ_NARROW_EARLY_RELEASE
-                release_tmem<kPair>(tempty_bar(buf), lane);  // the partial is in registers
-#endif
-                // this thread's 80 columns: half 0 = ra | rb | rc, half 1 = rc | ra | rb
-                if (kMode == MODE_BLOCK) {
-                    // 16-column chunks never straddle a 128-column scale block (col0 % 16 == 0)
-                    const float s0 = sa * lds_f32(slot + 4u * BM), s1 = sa * lds_f32(slot + 4u * (BM + 1));
-                    auto scl = [&](int acc_index) {  // scale of the 16-column chunk at acc[acc_index]
-                        const float v = ((col0 + 2 * acc_index) >> 7) == sblk0 ? s0 : s1;
-                        return make_float2(v, v);
-                    };
-                    if (h == 0) {
-                        promote_n<16>(&acc[0], &ra[0], scl(0));
-                        promote_n<16>(&acc[8], &ra[16], scl(8));
-                        promote_n<16>(&acc[16], &rb[0], scl(16));
-                        promote_n<16>(&acc[24], &rb[16], scl(24));
-                        promote_n<16>(&acc[32], &rc[0], scl(32));
-                    } else {
-                        promote_n<16>(&acc[0], &rc[0], scl(0));
-                        promote_n<16>(&acc[8], &ra[0], scl(8));
-                        promote_n<16>(&acc[16], &ra[16], scl(16));
-                        promote_n<16>(&acc[24], &rb[0], scl(24));
-                        promote_n<16>(&acc[32], &rb[16], scl(32));
-                    }
-                } else {
-                    const uint32_t sbs = slot + 4u * (BM + h * NC);
-                    const float2 sa2v = make_float2(sa, sa);
-                    if (h == 0) {
-                        promote_chunk_cols(&acc[0], ra, sa2v, sbs);
-                        promote_chunk_cols(&acc[16], rb, sa2v, sbs + 128);
-                        promote_chunk_cols16(&acc[32], rc, sa2v, sbs + 256);
-                    } else {
-                        promote_chunk_cols16(&acc[0], rc, sa2v, sbs);
-                        promote_chunk_cols(&acc[8], ra, sa2v, sbs + 64);
-                        promote_chunk_cols(&acc[24], rb, sa2v, sbs + 192);
-                    }
-                }
-#if !RLQ_NARROW_EARLY_RELEASE
-                release_tmem<kPair>(tempty_bar(buf), lane);
-#endif
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(sempty_bar(k));  // the scales are read
-            }
-            if (p.out_mode == OUT_BF16) {
-                // this warp's 32 rows x 80 columns staged as 32 rows of 160 bytes and
-                // stored by one TMA box (no swizzle); rows beyond R and columns beyond
-                // C are clipped by the tensor map
-                const uint32_t stg = smem_u32(staging) + (uint32_t)((warp - FIRST_EPI_WARP) * Cf::STG_BYTES_WARP);
-                const int y = mt * Cf::TILE_M + row_offset<kPair>() + q * 32;
-                if (lane == 0)
-                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // buffer read out
-                __syncwarp();
-                if (ok) {
-#pragma unroll
-                    for (int v = 0; v < NC / 8; ++v)
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + (uint32_t)(lane * NC * 2 + v * 16)),
-                                     "r"(bf16x2_rn(acc[4 * v])), "r"(bf16x2_rn(acc[4 * v + 1])),
-                                     "r"(bf16x2_rn(acc[4 * v + 2])), "r"(bf16x2_rn(acc[4 * v + 3]))
-                                     : "memory");
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> TMA reads
-                __syncwarp();
-                if (lane == 0 && ok && col0 < p.C) {
-                    tma_store_2d(&tmOut, stg, col0, y);
-                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                }
-                continue;
-            }
-            // fp32 outputs: this thread's row, 16-column chunks inside C
-            const int grow = mt * Cf::TILE_M + row_offset<kPair>() + row;
-            if (ok && grow < p.R) {
-#pragma unroll
-                for (int c = 0; c < NC / 16; ++c) {
-                    if (col0 + 16 * c >= p.C)
-                        break;
-                    if (p.out_mode == OUT_F32_ACC) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.acc_out + (int64_t)grow * p.ld_acc + col0 + 16 * c);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            float4 o = dst[v];
-                            o.x += acc[8 * c + 2 * v].x;
-                            o.y += acc[8 * c + 2 * v].y;
-                            o.z += acc[8 * c + 2 * v + 1].x;
-                            o.w += acc[8 * c + 2 * v + 1].y;
-                            dst[v] = o;
-                        }
-                    } else {
-                        float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)wu.split * p.R + grow) * p.C + col0 +
-                                                                 16 * c);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_float4(acc[8 * c + 2 * v].x, acc[8 * c + 2 * v].y, acc[8 * c + 2 * v + 1].x,
-                                                 acc[8 * c + 2 * v + 1].y);
-                    }
-                }
-            }
-        }
-        } else {
         for (int u = unit0; ok && u < p.num_units; u += unit_step, ++uc) {
             const Unit wu = unit_of(p, u);
             const int mt = wu.mt, nt = wu.nt;
-            const int col0 = nt * kBN + h * 128;
+            const int col0 = nt * BN + h * 128;
             const bool half_ok = col0 < p.C;
             float2 acc[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j)
                 acc[j] = make_float2(0.0f, 0.0f);
             for (int kb = wu.kb0; kb < (kOnce ? wu.kb0 + 1 : wu.kb1); ++kb, ++it) {
-                const int buf = kOnce ? buf_of(uc) : buf_of(it);
-                const uint32_t bph = kOnce ? use_of(uc) : use_of(it);
+                const int buf = kOnce ? (uc & 1) : (it & 1);
+                const uint32_t bph = kOnce ? ((uint32_t)(uc >> 1) & 1u) : ((uint32_t)(it >> 1) & 1u);
                 const int k = it % SCALE_SLOTS;
                 // every lane acquires the scales and the partial itself; the
                 // decision is warp-uniform because tcgen05.ld is .sync.aligned
@@ -743,7 +550,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 const uint32_t slot = smem_u32(ring) + (uint32_t)(k * SLOT_FLOATS * 4);
                 const float sa = lds_f32(slot + 4u * row);
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + h * 128);
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
                 uint32_t ra[32], rb[32];
                 if (kMode == MODE_BLOCK) {
                     const float scl = sa * lds_f32(slot + 4u * (BM + h));
@@ -852,7 +659,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                             bf16x2_rn(acc[4 * v + 2]), bf16x2_rn(acc[4 * v + 3]));
                 }
             }
-        }
         }
     }
 
@@ -975,19 +781,18 @@ uint64_t wait_limit_ns()
     return ns;
 }
 
-// bf16 output [rows][cols], pitch ld elements; box 64 columns x 32 rows with the
-// 128-byte swizzle (wide tiles), or 80 columns x 32 rows without (narrow tiles).
-rlq_status encode_out_map(CUtensorMap *map, uint16_t *base, int64_t cols, int64_t rows, int64_t ld, bool narrow)
+// bf16 output [rows][cols], pitch ld elements; box 64 columns x 32 rows, 128-byte swizzle.
+rlq_status encode_out_map(CUtensorMap *map, uint16_t *base, int64_t cols, int64_t rows, int64_t ld)
 {
     auto enc = get_encode_fn();
     if (!enc)
         return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    const cuuint32_t box[2] = {narrow ? (cuuint32_t)(BN_NARROW / 2) : 64u, 32};
+    const cuuint32_t box[2] = {64, 32};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, narrow ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for the [%lld x %lld] output",
@@ -1016,8 +821,8 @@ rlq_status encode_map(CUtensorMap *map, const uint8_t *base, int64_t inner, int6
 
 struct DevInfo {
     int sms = 0;
-    bool attr_set[32] = {};
-    int max_clusters[32] = {};  // co-resident CTA pairs of each paired variant (0: not yet known, -1: none)
+    bool attr_set[16] = {};
+    int max_clusters[16] = {};  // co-resident CTA pairs of each paired variant (0: not yet known, -1: none)
 };
 
 DevInfo &dev_info(int dev)
@@ -1088,21 +893,10 @@ bool pair_mode_enabled()
     return on;
 }
 
-// Narrow (160-column, three-buffer) tiles for CTA pairs with K-major B, unless
-// RLQ_GEMM_NARROW=0 is set in the environment.
-bool narrow_tiles_enabled()
-{
-    static const bool on = [] {
-        const char *e = std::getenv("RLQ_GEMM_NARROW");
-        return !(e && e[0] == '0');
-    }();
-    return on;
-}
-
-template <int kMode, bool kBMN, bool kPair, int kBN = BN>
+template <int kMode, bool kBMN, bool kPair>
 rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool withhold_first_load = false)
 {
-    using Cf = Cfg<kPair, kBN>;
+    using Cf = Cfg<kPair>;
     CUtensorMap tmA, tmB, tmO;
     rlq_status rs = encode_map(&tmA, a.A, a.L, a.R, a.lda, BM);
     if (rs != RLQ_OK)
@@ -1117,8 +911,8 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
     if (e != cudaSuccess)
         return cuda_status(e, "cudaGetDevice");
     DevInfo &di = dev_info(dev);
-    const int variant = kMode * 4 + (kBMN ? 2 : 0) + (kPair ? 1 : 0) + (kBN == BN_NARROW ? 16 : 0);
-    auto kernel = k_gemm_block_scaled<kMode, kBMN, kPair, kBN>;
+    const int variant = kMode * 4 + (kBMN ? 2 : 0) + (kPair ? 1 : 0);
+    auto kernel = k_gemm_block_scaled<kMode, kBMN, kPair>;
     if (!di.attr_set[variant]) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
         if (e != cudaSuccess)
@@ -1146,7 +940,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
             di.max_clusters[variant] = n < 1 ? -1 : n;  // -1: no pair fits, use single CTAs
         }
         if (di.max_clusters[variant] < 0)
-            return launch_impl<kMode, kBMN, false, BN>(a, splits, st, withhold_first_load);
+            return launch_impl<kMode, kBMN, false>(a, splits, st, withhold_first_load);
     }
     Params p;
     p.sa = a.sa;
@@ -1162,7 +956,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
     p.C = (int)a.C;
     p.kblocks = (int)((a.L + BK - 1) / BK);
     p.m_tiles = (int)((a.R + Cf::TILE_M - 1) / Cf::TILE_M);
-    p.n_tiles = (int)((a.C + kBN - 1) / kBN);
+    p.n_tiles = (int)((a.C + BN - 1) / BN);
     p.num_tiles = p.m_tiles * p.n_tiles;
     // keep the smaller operand resident in L2: sweep the tiles along it
     p.m_fastest = (a.R * a.L <= a.C * a.L) ? 1 : 0;
@@ -1174,7 +968,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
     p.ws = p.splits > 1 ? a.ws : nullptr;
     p.out_mode = p.splits > 1 ? OUT_F32_PARTIAL : (a.acc ? OUT_F32_ACC : OUT_BF16);
     if (kPair && p.out_mode == OUT_BF16) {
-        rs = encode_out_map(&tmO, a.out, a.C, a.R, a.ldo, kBN == BN_NARROW);
+        rs = encode_out_map(&tmO, a.out, a.C, a.R, a.ldo);
         if (rs != RLQ_OK)
             return rs;
     } else {
@@ -1205,13 +999,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
 template <int kMode, bool kBMN>
 rlq_status launch_mode(const GemmArgs &a, int splits, cudaStream_t st, bool pair, bool stall)
 {
-    if (!pair)
-        return launch_impl<kMode, kBMN, false>(a, splits, st, stall);
-    if constexpr (!kBMN && kMode != MODE_ONCE) {
-        if (narrow_tiles_enabled())
-            return launch_impl<kMode, kBMN, true, BN_NARROW>(a, splits, st);
-    }
-    return launch_impl<kMode, kBMN, true>(a, splits, st);
+    return pair ? launch_impl<kMode, kBMN, true>(a, splits, st) : launch_impl<kMode, kBMN, false>(a, splits, st, stall);
 }
 
 // One-shot diagnostic armed by arm_gemm_stall() for the calling thread.
