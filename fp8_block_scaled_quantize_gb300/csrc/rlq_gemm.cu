@@ -90,10 +90,6 @@ constexpr int RING_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
 #ifndef RLQ_STG_COLS
 #define RLQ_STG_COLS 64
 #endif
-// Half-width MMA streams for K-major B (1) or one full-width MMA per K step (0).
-#ifndef RLQ_SPLIT_N
-#define RLQ_SPLIT_N 1
-#endif
 constexpr int STG_COLS = RLQ_STG_COLS;            // bf16 columns per staged store round (64 or 128)
 constexpr int STG_WARP_BYTES = 32 * STG_COLS * 2;  // one warp's staging buffer
 static_assert(STG_COLS == 64 || STG_COLS == 128, "staged rounds of 64 or 128 columns");
@@ -106,9 +102,7 @@ struct Cfg {
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TILE_M = kPair ? 2 * BM : BM;  // output rows per tile
-    // full / empty per stage; tfull / tempty per (TMEM buffer, column half); teardown;
-    // sfull / sempty per scale slot
-    static constexpr int NUM_BARS = 2 * STAGES + 8 + 1 + 2 * SCALE_SLOTS;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 2 * SCALE_SLOTS;
     static constexpr int SMEM_BYTES =
         1024 /* alignment slack */ + STAGES * STAGE_BYTES + STAGING + RING_BYTES + NUM_BARS * 8 + 16;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -118,13 +112,6 @@ struct Cfg {
     // (M = 256 for a CTA pair).
     static constexpr uint32_t IDESC_BK = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(TILE_M >> 4) << 24);
     static constexpr uint32_t IDESC_BMN = IDESC_BK | (1u << 16);
-    // Half-width MMAs (N = 128, K-major B): the tile's two column halves are computed,
-    // committed and released separately.
-    static constexpr uint32_t IDESC_HALF = (1u << 4) | ((uint32_t)((BN / 2) >> 3) << 17) | ((uint32_t)(TILE_M >> 4) << 24);
-    // B rows a CTA pair stages per box: each CTA holds rows [64 r, 64 r + 64) of each
-    // column half of the tile (r = CTA rank), so that a half-width pair MMA finds its
-    // N / 2 = 64 rows in each CTA
-    static constexpr int B_BOX_ROWS = kPair ? BN / 4 : BN;
 };
 
 
@@ -280,13 +267,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int STAGE_BYTES = Cf::STAGE_BYTES;
     constexpr int NUM_BARS = Cf::NUM_BARS;
     constexpr bool kOnce = kMode == MODE_ONCE;
-    // Split N (K-major B): per contraction block the MMA warp issues the tile's left
-    // 128 columns, commits them, then the right 128 columns; each column half of a
-    // TMEM buffer has its own full / empty barriers, and the epilogue warps of that
-    // half (h) wait for and release only it.  The two halves' epilogues run half a
-    // block apart, and a half can be refilled while the other is still being read.
-    constexpr bool kSplit = !kBMajorMN && RLQ_SPLIT_N;
-    constexpr int NHALF = kSplit ? 2 : 1;
     // A CTA pair (cluster of 2) shares one 256-row tile: CTA `rank` owns rows
     // rank * 128 .. rank * 128 + 127 of it; the even CTA issues the pair's MMAs.
     // (The rank is re-read where it is used rather than kept in a register.)
@@ -306,12 +286,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto b_stage = [&](int s) { return smem0 + (uint32_t)(s * STAGE_BYTES + A_BYTES); };
     auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
     auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
-    // TMEM buffer b, column half h (h = 0 when the halves are not split)
-    auto tfull_bar = [&](int b, int h) { return smem_u32(&bars[2 * STAGES + 2 * b + h]); };
-    auto tempty_bar = [&](int b, int h) { return smem_u32(&bars[2 * STAGES + 4 + 2 * b + h]); };
-    const uint32_t teardown_bar = smem_u32(&bars[2 * STAGES + 8]);
-    auto sfull_bar = [&](int k) { return smem_u32(&bars[2 * STAGES + 9 + k]); };
-    auto sempty_bar = [&](int k) { return smem_u32(&bars[2 * STAGES + 9 + SCALE_SLOTS + k]); };
+    auto tfull_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + b]); };
+    auto tempty_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + 2 + b]); };
+    const uint32_t teardown_bar = smem_u32(&bars[2 * STAGES + 4]);
+    auto sfull_bar = [&](int k) { return smem_u32(&bars[2 * STAGES + 5 + k]); };
+    auto sempty_bar = [&](int k) { return smem_u32(&bars[2 * STAGES + 5 + SCALE_SLOTS + k]); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -319,12 +298,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(empty_bar(s), 1);  // the stage is free once its MMAs completed
         }
         for (int b = 0; b < 2; ++b) {
-            for (int h = 0; h < NHALF; ++h) {
-                mbar_init(tfull_bar(b, h), 1);
-                // a pair's buffer (half) is free once the epilogue warps reading it in
-                // both CTAs released it
-                mbar_init(tempty_bar(b, h), (kPair ? 2 : 1) * NUM_EPI_WARPS / NHALF);
-            }
+            mbar_init(tfull_bar(b), 1);
+            // a pair's buffer is free once the epilogue warps of both CTAs released it
+            mbar_init(tempty_bar(b), kPair ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
         }
         mbar_init(teardown_bar, 2);  // one commit per MMA-issuing warp
         for (int k = 0; k < SCALE_SLOTS; ++k) {
@@ -388,16 +364,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (cta_rank() == 0)
                             mbar_arrive_expect_tx(full_bar(s), 2 * STAGE_BYTES);
                         tma_load_2d_pair(a_stage(s), &tmA, fb, kb * BK, mt * Cf::TILE_M + row_offset<kPair>());
-                        if (kBMajorMN) {  // this CTA's 128 output columns: one 128 x 128 box
+                        if (kBMajorMN)  // this CTA's 128 output columns: one 128 x 128 box
                             tma_load_2d_pair(b_stage(s), &tmB, fb, nt * BN + row_offset<kPair>(), kb * BK);
-                        } else if (kSplit) {
-                            // rows [64 r, 64 r + 64) of each column half (r = CTA rank)
-                            const int r64 = (int)cta_rank() * (BN / 4);
-                            tma_load_2d_pair(b_stage(s), &tmB, fb, kb * BK, nt * BN + r64);
-                            tma_load_2d_pair(b_stage(s) + Cf::B_BYTES / 2, &tmB, fb, kb * BK, nt * BN + BN / 2 + r64);
-                        } else {
+                        else
                             tma_load_2d_pair(b_stage(s), &tmB, fb, kb * BK, nt * BN + row_offset<kPair>());
-                        }
                     } else {
                         if (p.withhold_first_load && it == 0)
                             continue;  // nothing arrives on this stage's barrier
@@ -453,50 +423,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int u = unit0; ok && u < p.num_units; u += unit_step, ++uc) {
                 const Unit w = unit_of(p, u);
+                if (kOnce) {
+                    const uint32_t bph = (uint32_t)(uc >> 1) & 1u;
+                    if (!mbar_wait(tempty_bar(uc & 1), bph ^ 1u, abort_flag, p.timeout_ns, SITE_MMA_TMEM_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     if (!kOnce && (it & 1) != parity)
                         continue;
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     const int buf = kOnce ? (uc & 1) : (it & 1);
-                    const uint32_t bph = kOnce ? ((uint32_t)(uc >> 1) & 1u) : ((uint32_t)(it >> 1) & 1u);
-                    const bool first = !kOnce || kb == w.kb0;    // the block's MMAs start the buffer's sum
-                    const bool last = !kOnce || kb + 1 == w.kb1;  // and the sum is complete after them
-                    bool have_data = false;
-                    for (int h = 0; h < NHALF; ++h) {
-                        if (first && !mbar_wait(tempty_bar(buf, h), bph ^ 1u, abort_flag, p.timeout_ns,
-                                                SITE_MMA_TMEM_EMPTY)) {
+                    if (!kOnce) {
+                        const uint32_t bph = (uint32_t)(it >> 1) & 1u;
+                        if (!mbar_wait(tempty_bar(buf), bph ^ 1u, abort_flag, p.timeout_ns, SITE_MMA_TMEM_EMPTY)) {
                             ok = false;
                             break;
                         }
-                        if (!have_data) {
-                            if (!mbar_wait(full_bar(s), ph, abort_flag, p.timeout_ns, SITE_MMA_FULL)) {
-                                ok = false;
-                                break;
-                            }
-                            have_data = true;
-                        }
-                        tc_fence_after();
-                        const uint32_t d = tmem_base + (uint32_t)(buf * BN + h * (BN / 2));
-                        const uint64_t ad = sw128_desc(a_stage(s));
-                        const uint64_t bd = kBMajorMN ? sw128_desc_mn(b_stage(s))
-                                                      : sw128_desc(b_stage(s) + (uint32_t)(h * (Cf::B_BYTES / 2)));
-#pragma unroll
-                        for (int j = 0; j < BK / UMMA_K; ++j) {
-                            // K-major: +32 bytes along K (+2 in the address field); MN-major:
-                            // +32 contraction rows of 128 bytes (+256)
-                            const uint64_t bj = kBMajorMN ? bd + (uint64_t)(256 * j) : bd + 2 * j;
-                            tc_mma_f8<kPair>(d, ad + 2 * j, bj,
-                                             kSplit ? Cf::IDESC_HALF : (kBMajorMN ? Cf::IDESC_BMN : Cf::IDESC_BK),
-                                             (first && j == 0) ? 0u : 1u);
-                        }
-                        // (pair: arrives on the barrier at this offset in both CTAs)
-                        if (last)
-                            tc_commit_t<kPair>(tfull_bar(buf, h));
                     }
-                    if (!ok)
+                    if (!mbar_wait(full_bar(s), ph, abort_flag, p.timeout_ns, SITE_MMA_FULL)) {
+                        ok = false;
                         break;
-                    tc_commit_t<kPair>(empty_bar(s));  // the stage is read once both halves' MMAs are done
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+                    const uint64_t ad = sw128_desc(a_stage(s));
+                    const uint64_t bd = kBMajorMN ? sw128_desc_mn(b_stage(s)) : sw128_desc(b_stage(s));
+                    const bool first = !kOnce || kb == w.kb0;
+#pragma unroll
+                    for (int j = 0; j < BK / UMMA_K; ++j) {
+                        // K-major: +32 bytes along K (+2 in the address field); MN-major:
+                        // +32 contraction rows of 128 bytes (+256)
+                        const uint64_t bj = kBMajorMN ? bd + (uint64_t)(256 * j) : bd + 2 * j;
+                        tc_mma_f8<kPair>(d, ad + 2 * j, bj, kBMajorMN ? Cf::IDESC_BMN : Cf::IDESC_BK,
+                                         (first && j == 0) ? 0u : 1u);
+                    }
+                    // (pair: arrives on the barrier at this offset in both CTAs)
+                    tc_commit_t<kPair>(empty_bar(s));
+                    if (!kOnce || kb + 1 == w.kb1)
+                        tc_commit_t<kPair>(tfull_bar(buf));
                 }
             }
         }
@@ -575,8 +542,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // decision is warp-uniform because tcgen05.ld is .sync.aligned
                 const bool w = mbar_wait(sfull_bar(k), (uint32_t)(it / SCALE_SLOTS) & 1u, abort_flag, p.timeout_ns,
                                          SITE_EPI_SCALE_FULL) &&
-                               mbar_wait(tfull_bar(buf, kSplit ? h : 0), bph, abort_flag, p.timeout_ns,
-                                         SITE_EPI_TMEM_FULL);
+                               mbar_wait(tfull_bar(buf), bph, abort_flag, p.timeout_ns, SITE_EPI_TMEM_FULL);
                 if (!__all_sync(0xFFFFFFFFu, w)) {
                     ok = false;
                     break;
@@ -601,7 +567,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     promote_chunk(&acc[32], ra, scl2);
                     tmem_wait32(rb);
                     promote_chunk(&acc[48], rb, scl2);
-                    release_tmem<kPair>(tempty_bar(buf, kSplit ? h : 0), lane);
+                    release_tmem<kPair>(tempty_bar(buf), lane);
                 } else {
                     // MODE_COLS: acc += P * (sa * sb[c]); MODE_ONCE: the same product
                     // into a zero accumulator, once per unit
@@ -621,7 +587,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // column-scaled: released before the last chunk's FMAs (registers only);
                     // a same-box A/B measured this 1% faster for WGrad but 8% slower for the
                     // block-scaled mode above, which releases after them
-                    release_tmem<kPair>(tempty_bar(buf, kSplit ? h : 0), lane);
+                    release_tmem<kPair>(tempty_bar(buf), lane);
                     promote_chunk_cols(&acc[48], rb, sa2v, sbs + 384);
                 }
                 __syncwarp();
@@ -937,8 +903,7 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
         return rs;
     // B is [C][L] (K-major; boxes of the B rows one CTA stages) or [L][C] (MN-major,
     // boxes of 128 columns x 128 rows)
-    rs = kBMN ? encode_map(&tmB, a.B, a.C, a.L, a.ldb, BK)
-              : encode_map(&tmB, a.B, a.L, a.C, a.ldb, RLQ_SPLIT_N ? Cf::B_BOX_ROWS : Cf::B_ROWS);
+    rs = kBMN ? encode_map(&tmB, a.B, a.C, a.L, a.ldb, BK) : encode_map(&tmB, a.B, a.L, a.C, a.ldb, Cf::B_ROWS);
     if (rs != RLQ_OK)
         return rs;
     int dev = 0;
