@@ -779,7 +779,7 @@ calls), for profiler captures of a small case: gemm_fprop, gemm_dgrad,
 gemm_dgrad_mn (untransposed weight codes), gemm_wgrad (optionally --split-k), gemm_wgrad_accumulate,
 gemm_fprop_per_channel, gemm_nvfp4, quant_rows, quant_dual,
 rmsnorm_quant, rmsnorm_quant_dual, quant_weight (with the transposed copy),
-quant_weight_nt (without), uaq_fold.  Prints the
+quant_weight_nt (without), quant_nvfp4, uaq_fold.  Prints the
 median CUDA-event time; no JSON line."""
 
 
@@ -838,6 +838,8 @@ def run_case(args):
         fn = lambda: rlq.quant_act_1x128(x, colwise=True)
     elif name == "quant_weight":
         fn = lambda: rlq.quant_weight_128x128(w, transposed=True)
+    elif name == "quant_nvfp4":
+        fn = lambda: rlq.quant_nvfp4(w)
     elif name == "quant_weight_nt":  # without the transposed copy (the bench step's form)
         fn = lambda: rlq.quant_weight_128x128(w)
     elif name == "uaq_fold":

@@ -797,15 +797,32 @@ __device__ __forceinline__ float e4m3_value(uint32_t e)
     return (e & 0x80u) ? -v : v;
 }
 
+// Plain cached 16-byte load: the amax pass leaves W in L2 for the block pass.
+__device__ __forceinline__ uint4 ld_keep(const uint16_t *p)
+{
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// Tensor amax.  CTAs walk whole rows (no index division), threads 8 elements
+// apart, four loads in flight per thread.
 __global__ void __launch_bounds__(256) k_nvfp4_amax(const uint16_t *__restrict__ w, int64_t N, int64_t K, int64_t ldw,
                                                     unsigned int *__restrict__ amax_bits)
 {
-    const int64_t K8 = K / 8, total = N * K8;
+    const int K8 = (int)(K / 8);
     uint32_t pm = 0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t n = i / K8, k = (i - n * K8) * 8;
-        const uint4 v = ld_stream(w + n * ldw + k);
-        pm = bmaxabs2(pm, bmaxabs2(bmaxabs2(v.x, v.y), bmaxabs2(v.z, v.w)));
+    for (int64_t n = blockIdx.x; n < N; n += gridDim.x) {
+        const uint16_t *row = w + n * ldw;
+        for (int k8 = threadIdx.x; k8 < K8; k8 += 4 * 256) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = k8 + 256 * u < K8 ? ld_keep(row + 8 * (k8 + 256 * u)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                pm = bmaxabs2(pm, bmaxabs2(bmaxabs2(v[u].x, v[u].y), bmaxabs2(v[u].z, v[u].w)));
+        }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1)
@@ -821,10 +838,11 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const uint16_t *__restrict_
 {
     const float amax = __uint_as_float(*amax_bits);
     const float st = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);  // 6 * 448
-    const int64_t KB = K / 16, total = N * KB;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t n = i / KB, kb = i - n * KB;
-        const uint16_t *src = w + n * ldw + kb * 16;
+    const int KB = (int)(K / 16);
+    // CTAs walk whole rows, a thread per 16-element block
+    for (int64_t n = blockIdx.x; n < N; n += gridDim.x)
+    for (int kb = threadIdx.x; kb < KB; kb += 256) {
+        const uint16_t *src = w + n * ldw + (int64_t)kb * 16;
         float f[16];
         float lo8[8], hi8[8];
         unpack8(ld_stream(src), lo8);
@@ -1010,12 +1028,11 @@ cudaError_t launch_quant_nvfp4(const uint16_t *w, int64_t N, int64_t K, int64_t 
     if (e != cudaSuccess)
         return e;
     unsigned int *amax_bits = reinterpret_cast<unsigned int *>(st);
+    // one CTA per row while rows are few, else a grid-stride over rows
     const int64_t cap = (int64_t)sm_count() * 8;
-    int64_t g1 = (N * (K / 8) + 255) / 256;
-    g1 = g1 > cap ? cap : (g1 < 1 ? 1 : g1);
+    const int64_t g1 = N > cap ? cap : (N < 1 ? 1 : N);
     k_nvfp4_amax<<<(unsigned)g1, 256, 0, st_stream>>>(w, N, K, ldw, amax_bits);
-    int64_t g2 = (N * (K / 16) + 255) / 256;
-    g2 = g2 > cap * 4 ? cap * 4 : (g2 < 1 ? 1 : g2);
+    const int64_t g2 = N > cap * 4 ? cap * 4 : (N < 1 ? 1 : N);
     k_nvfp4_quant<<<(unsigned)g2, 256, 0, st_stream>>>(w, N, K, ldw, q, ldq, sb, ldsb, amax_bits);
     k_nvfp4_tensor_scale<<<1, 1, 0, st_stream>>>(st);
     return cudaGetLastError();
