@@ -223,3 +223,19 @@ def test_binding_covers_every_declared_function():
     typed_at_load = {"rlq_status_string", "rlq_last_error", "rlq_version"}
     missing = [n for n in declared_functions() if n not in rlq._SIGS and n not in typed_at_load]
     assert not missing, f"no ctypes signature for {missing}"
+
+
+def test_nvfp4_gemm_validation():
+    """Host checks of the NVFP4 weight-only GEMM and its split-K form (no launch)."""
+    g, gs = rlq.rlq_gemm_nvfp4_weight_only, rlq.rlq_gemm_nvfp4_weight_only_splitk
+    # x [4, 128] bf16, wq [128, 64] bytes (pitch 64), wsb [128, 8] (pitch 16), y [4, 128]
+    ok = (FAKE, 128, FAKE, 64, FAKE, 16, FAKE, FAKE, 128, 4, 128, 128)
+    assert _status(g, *ok[:10], 100, 128, None) == 2                         # N % 128
+    assert _status(g, *ok[:11], 96, None) == 2                               # K % 64
+    assert _status(g, *ok[:3], 72, *ok[4:], None) == 3                       # code pitch not a multiple of 16
+    assert _status(g, *ok[:6], None, *ok[7:], None) == 1                     # NULL tensor scale
+    assert _status(g, *ok[:6], FAKE + 2, *ok[7:], None) == 3                 # tensor scale not 4-byte aligned
+    assert _status(g, *ok[:9], 0, 128, 128, None) == 0                       # M = 0: nothing to do
+    assert _status(gs, *ok, FAKE + 8, 1 << 20, None) == 3                    # workspace not 16-byte aligned
+    assert _status(gs, *ok, FAKE, -1, None) == 1                             # negative workspace size
+    assert _status(gs, *ok[:10], 100, 128, FAKE, 1 << 20, None) == 2         # N % 128, with a workspace
