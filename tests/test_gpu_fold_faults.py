@@ -8,7 +8,7 @@ import torch
 import oracle
 from fp8_block_scaled_quantize_gb300 import inputs as I
 from fp8_block_scaled_quantize_gb300 import rlq
-from gpu_util import np_, to_dev, u16
+from gpu_util import normal_bits, np_, to_dev, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -36,6 +36,38 @@ def test_fold_qwen7b_per_channel_bit_exact(which):
     w_f, x_f = oracle.uaq_fold(d["w"], d["s"], d["x"])
     _, g_f = oracle.uaq_fold(np.zeros((0, d["w"].shape[1]), np.uint16), d["s"], gamma)
     assert np.array_equal(u16(wg), w_f) and np.array_equal(u16(xg), x_f) and np.array_equal(u16(gg), g_f)
+
+
+def _fold_gpu(w_bits, s):
+    wg = to_dev(w_bits)
+    rlq.uaq_fold_(wg, torch.from_numpy(s).cuda())
+    rlq.check()
+    return u16(wg)
+
+
+def test_fold_bit_exact_over_wide_ranges():
+    """W / s must equal the oracle's bf16_RN(fl32(w / s)) for every element.
+
+    Part 1: 4M random finite bf16 patterns (every exponent, both signs,
+    subnormals) against per-column scales log-uniform over 2^-126 .. 2^127 plus
+    special ones (1, 3, 7, 0.1, 1/3, 2^-100, 2^101, a subnormal scale, the
+    largest floats): quotients that overflow, underflow to subnormals or zero.
+    Part 2: N(0, 1) weights against scales in [0.5, 8], every quotient normal."""
+    rng = np.random.default_rng(77)
+    N, K = 2048, 2048
+    w = rng.integers(0, 1 << 16, size=(N, K), dtype=np.uint32).astype(np.uint16)
+    nonfinite = ((w >> 7) & 0xFF) == 0xFF
+    w[nonfinite] &= np.uint16(0x807F)  # exponent field cleared: a finite subnormal
+    s = np.exp2(rng.uniform(-126.0, 127.0, size=K)).astype(np.float32)
+    special = [1.0, 3.0, 7.0, 0.1, 1.0 / 3.0, 2.0 ** -100, 2.0 ** -100 * 0.999, 2.0 ** 101, 2.0 ** 101 * 0.999,
+               2.0 ** -126, 1e-40, 3.4e38, 2.0 ** 50]
+    s[:len(special)] = np.array(special, np.float32)
+    want, _ = oracle.uaq_fold(w, s)
+    assert np.array_equal(_fold_gpu(w, s), want)
+    w2 = normal_bits(78, (N, K), 1.0, "w")
+    s2 = rng.uniform(0.5, 8.0, size=K).astype(np.float32)
+    want2, _ = oracle.uaq_fold(w2, s2)
+    assert np.array_equal(_fold_gpu(w2, s2), want2)
 
 
 def test_fold_pitched_rows_untouched_padding():
