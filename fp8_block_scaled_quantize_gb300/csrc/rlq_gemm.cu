@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
-        if (kPair && p.out_mode == OUT_BF16)
+        if (kPair && p.out_mode != OUT_F32_PARTIAL)
             prefetch_tmap(&tmOut);
     }
     tc_fence_before();
@@ -603,6 +603,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0)
                     mbar_arrive(sempty_bar(k));  // the scales are read
             }
+            if (kPair && p.out_mode == OUT_F32_ACC) {
+                // this warp's 32 rows x 128 fp32 columns added into the caller's gradient
+                // in rounds of 32 columns: each round is staged as 32 rows of 128 bytes
+                // (16-byte chunks XOR-swizzled by row % 8, the map's 128-byte swizzle)
+                // and added at L2 by a TMA reduce; rows beyond R and columns beyond C
+                // are clipped by the tensor map
+                const uint32_t stg = smem_u32(staging) + (uint32_t)((warp - FIRST_EPI_WARP) * STG_WARP_BYTES);
+                const int y = mt * Cf::TILE_M + row_offset<kPair>() + q * 32;
+#pragma unroll
+                for (int rd = 0; rd < 4; ++rd) {
+                    if (lane == 0)
+                        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // buffer read out
+                    __syncwarp();
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const int j = 16 * rd + 2 * v;  // acc pairs of columns 32 rd + 4 v .. + 3
+                        const uint32_t addr = stg + (uint32_t)(lane * 128 + ((v ^ (lane & 7)) << 4));
+                        if (ok)
+                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(acc[j].x),
+                                         "f"(acc[j].y), "f"(acc[j + 1].x), "f"(acc[j + 1].y)
+                                         : "memory");
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> TMA reads
+                    __syncwarp();
+                    if (lane == 0 && ok && half_ok) {
+                        tma_reduce_add_2d(&tmOut, stg, col0 + 32 * rd, y);
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    }
+                }
+                continue;
+            }
             if (kPair && p.out_mode == OUT_BF16) {
                 // this warp's 32 rows x 128 columns in rounds of STG_COLS columns: each
                 // round is staged as 32 rows of STG_COLS * 2 bytes (16-byte chunks
@@ -809,6 +840,26 @@ rlq_status encode_out_map(CUtensorMap *map, uint16_t *base, int64_t cols, int64_
     return RLQ_OK;
 }
 
+// fp32 gradient [rows][cols], pitch ld elements, for TMA reduce-adds: box 32 columns
+// (128 bytes) x 32 rows, 128-byte swizzle.
+rlq_status encode_acc_map(CUtensorMap *map, float *base, int64_t cols, int64_t rows, int64_t ld)
+{
+    auto enc = get_encode_fn();
+    if (!enc)
+        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(RLQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for the [%lld x %lld] fp32 gradient",
+                    (int)r, (long long)rows, (long long)cols);
+    return RLQ_OK;
+}
+
 // 2-D E4M3 tensor [rows][inner] with row pitch `ld` bytes; box 128 x box_rows.
 rlq_status encode_map(CUtensorMap *map, const uint8_t *base, int64_t inner, int64_t rows, int64_t ld, int box_rows)
 {
@@ -976,7 +1027,11 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
     p.num_units = p.num_tiles * p.splits;
     p.ws = p.splits > 1 ? a.ws : nullptr;
     p.out_mode = p.splits > 1 ? OUT_F32_PARTIAL : (a.acc ? OUT_F32_ACC : OUT_BF16);
-    if (kPair && p.out_mode == OUT_BF16) {
+    if (kPair && p.out_mode == OUT_F32_ACC) {
+        rs = encode_acc_map(&tmO, a.acc, a.C, a.R, a.ld_acc);
+        if (rs != RLQ_OK)
+            return rs;
+    } else if (kPair && p.out_mode == OUT_BF16) {
         rs = encode_out_map(&tmO, a.out, a.C, a.R, a.ldo);
         if (rs != RLQ_OK)
             return rs;

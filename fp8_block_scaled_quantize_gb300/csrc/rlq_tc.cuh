@@ -154,6 +154,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                  : "memory");
 }
 
+// Element-wise add of a shared-memory box into global memory (fp32 per the tensor
+// map), performed at L2; completes in the bulk async group like tma_store_2d.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32_t src, int x, int y)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"((uint64_t)map), "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Pair forms.  The load lands in this CTA's shared memory and completes its bytes
 // on `bar`, a barrier of either CTA of the pair (a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y)

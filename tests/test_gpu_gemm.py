@@ -233,15 +233,19 @@ qdy, sdy, qdyT, sdyc = rlq.quant_act_1x128(to_dev(normal_bits(60, (M, N), 1e-3, 
 qw, sw, qwT = rlq.quant_weight_128x128(to_dev(normal_bits(60, (N, K), 0.02, "w")), transposed=True)
 outs = [rlq.gemm_fprop(qx, sx, qw, sw), rlq.gemm_dgrad(qdy, sdy, qwT, sw), rlq.gemm_dgrad(qdy, sdy, qw, sw, transposed=False),
         rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc)]
+acc = torch.full((N, K), 0.25, dtype=torch.float32, device="cuda")
+rlq.gemm_wgrad_accumulate_(acc, qdyT, sdyc, qxT, sxc)  # no workspace: the epilogue adds (pairs: TMA reduce-adds)
 rlq.check()
-np.savez(sys.argv[2], *[o.view(torch.int16).cpu().numpy() for o in outs])
+np.savez(sys.argv[2], *[o.view(torch.int16).cpu().numpy() for o in outs], acc.view(torch.int32).cpu().numpy())
 """
 
 
 def test_pair_and_single_cta_modes_agree_bitwise(tmp_path):
     """Tiles of 256 output rows run on CTA pairs (cta_group::2); RLQ_GEMM_PAIR=0
     forces one CTA per 128 rows.  The per-element arithmetic is the same, so the
-    two modes must give identical bits for FProp, both DGrad forms and WGrad."""
+    two modes must give identical bits for FProp, both DGrad forms, WGrad, and
+    WGrad added into an fp32 gradient (pairs add by TMA reduce at L2, single CTAs
+    by a read-modify-write: both one fp32 addition per element)."""
     import os
     import subprocess
     import sys
