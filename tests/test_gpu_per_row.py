@@ -25,8 +25,11 @@ def _check(x_bits, q, s, s_rep):
 # Few rows run one CTA per row, many rows (more than 64 per SM) one warp per row:
 # the last two shapes take the warp path on GPUs of up to 312 SMs.
 @pytest.mark.parametrize("M,K", [(1, 128), (7, 256), (300, 640), (4096, 4096), (64, 27648), (20000, 128),
-                                 (20011, 1152)])
+                                 (20011, 1152), (33, 5120), (17, 16384), (9, 16512), (3, 32768), (5, 32896),
+                                 (300, 3584), (1000, 18944), (40, 20480), (41, 24576), (42, 27648)])
 def test_per_row_parity(M, K):
+    """Rows held by one warp (K <= 4096), by one CTA (K <= 32768, 8 or 16 loads per
+    thread, ragged ends) and streamed twice (longer rows)."""
     x = normal_bits(41, (M, K), std=0.02)
     q, s, s_rep = rlq.quant_per_row(to_dev(x))
     _check(x, q, s, s_rep)
