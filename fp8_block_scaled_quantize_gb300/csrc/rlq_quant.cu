@@ -953,14 +953,35 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const uint16_t *__restrict_
     const float amax = __uint_as_float(*amax_bits);
     const float st = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);  // 6 * 448
     const int KB = (int)(K / 16);
-    // CTAs walk whole rows, a thread per 16-element block
-    for (int64_t n = blockIdx.x; n < N; n += gridDim.x)
-    for (int kb = threadIdx.x; kb < KB; kb += 256) {
-        const uint16_t *src = w + n * ldw + (int64_t)kb * 16;
+    // CTAs walk whole rows, a thread per 16-element block; the next block's 32 bytes
+    // are loaded before this one is encoded (two loads in flight per thread)
+    int64_t n = blockIdx.x;
+    int kb = threadIdx.x;
+    auto next = [&](int64_t &nn, int &kk) {
+        kk += 256;
+        if (kk >= KB) {
+            kk = threadIdx.x;
+            nn += gridDim.x;
+        }
+    };
+    uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+    if (kb < KB && n < N) {
+        c0 = ld_stream(w + n * ldw + (int64_t)kb * 16);
+        c1 = ld_stream(w + n * ldw + (int64_t)kb * 16 + 8);
+    }
+    for (; kb < KB && n < N;) {
+        int64_t nn = n;
+        int kk = kb;
+        next(nn, kk);
+        uint4 p0 = make_uint4(0, 0, 0, 0), p1 = p0;
+        if (nn < N) {
+            p0 = ld_stream(w + nn * ldw + (int64_t)kk * 16);
+            p1 = ld_stream(w + nn * ldw + (int64_t)kk * 16 + 8);
+        }
         float f[16];
         float lo8[8], hi8[8];
-        unpack8(ld_stream(src), lo8);
-        unpack8(ld_stream(src + 8), hi8);
+        unpack8(c0, lo8);
+        unpack8(c1, hi8);
         float ab = 0.0f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -986,6 +1007,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const uint16_t *__restrict_
                 word[j >> 3] |= e2m1x2(nv_quot(f[j], S, r), nv_quot(f[j + 1], S, r)) << (4 * (j & 7));
         }
         *reinterpret_cast<uint2 *>(q + n * ldq + kb * 8) = make_uint2(word[0], word[1]);
+        c0 = p0, c1 = p1, n = nn, kb = kk;
     }
 }
 
