@@ -33,8 +33,8 @@
 // (clusters of two, tcgen05.mma.cta_group::2, M = 256): each CTA stages its 128
 // rows of A and half of B, the even CTA issues the pair's MMAs and commits to
 // both CTAs' barriers, and the epilogue stages the bf16 tile in shared memory
-// for TMA stores (an fp32 gradient being accumulated: TMA reduce-adds at L2).  A
-// single CTA (fewer rows, or a split contraction) stores its rows directly.  The kernel is persistent (one CTA per SM, one pair per two)
+// for TMA stores.  A single CTA (fewer rows, or a split contraction) stores its
+// rows directly.  The kernel is persistent (one CTA per SM, one pair per two)
 // and walks (tile, contraction split) units with the smaller operand resident in
 // L2.  Every mbarrier wait is bounded: on timeout the waiting thread records an
 // error word that rlq_check() reports, raises a CTA-wide abort flag, and the CTA
