@@ -33,6 +33,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -475,23 +476,58 @@ def cpu_baseline(rows: int, cols: int, data=None):
     w = np.ascontiguousarray(d["w"][:cols])
     dy = np.ascontiguousarray(d["dy"][:rows, :cols])
     s = np.full(K, UAQ_S, np.float32)
+
+    def quantize():
+        w_f, _ = oracle.uaq_fold(w, s)
+        qw, sw, _ = oracle.quant_weight_128x128(w_f)
+        return (qw, sw) + oracle.quant_rows_1x128(x) + oracle.quant_rows_1x128(dy) + \
+            oracle.quant_cols_128x1(x) + oracle.quant_cols_128x1(dy)
+
     t0 = time.perf_counter()
-    w_f, _ = oracle.uaq_fold(w, s)
-    qw, sw, _ = oracle.quant_weight_128x128(w_f)
-    qx, sx = oracle.quant_rows_1x128(x)
-    qdy, sdy = oracle.quant_rows_1x128(dy)
-    qxT, sxc = oracle.quant_cols_128x1(x)
-    qdyT, sdyc = oracle.quant_cols_128x1(dy)
+    qw, sw, qx, sx, qdy, sdy, qxT, sxc, qdyT, sdyc = quantize()
+    t1 = time.perf_counter()
     oracle.gemm_fprop(qx, sx, qw, sw)
     oracle.gemm_dgrad(qdy, sdy, qw, sw)
     oracle.gemm_wgrad(qdyT, sdyc, qxT, sxc)
-    dt = time.perf_counter() - t0
+    t2 = time.perf_counter()
+    cores = oracle.num_threads()
+    # the quantizers and fold once more on a single core (the GEMMs' BLAS is not limited)
+    oracle.set_num_threads(1)
+    try:
+        t3 = time.perf_counter()
+        quantize()
+        t4 = time.perf_counter()
+    finally:
+        oracle.set_num_threads(cores)
+    dt = t2 - t0
     flop = 6.0 * rows * cols * K
-    return {"value": round(flop / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": round(dt, 3),
+    qbytes = (4 + 3) * cols * K + B_DUAL * (rows * K + rows * cols)  # fold + weight quant + dual X, dY
+    return {"value": round(flop / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "seconds": round(dt, 3), "cpu_model": _cpu_model(),
+            "quant_fold_seconds": round(t1 - t0, 3), "quant_fold_gbs": round(qbytes / (t1 - t0) / 1e9, 3),
+            "quant_fold_gbs_1core": round(qbytes / (t4 - t3) / 1e9, 3),
+            "gemm_seconds": round(t2 - t1, 3),
             "sample": f"sub-problem of {rows} tokens x {cols} output channels of the [{M_},{N_},{K_}] step: fold and "
                       f"128x128 quant of W[:{cols}], 1x128 + 128x1 quant of X[:{rows}] and dY[:{rows},:{cols}], "
-                      f"FProp / DGrad / WGrad restricted to it (C with OpenMP + NumPy fp64)"}
+                      f"FProp / DGrad / WGrad restricted to it (C with OpenMP + NumPy fp64; the GEMMs "
+                      f"dequantize per block inside gemm_seconds)"}
+
+
+def _cpu_model() -> str:
+    """The host CPU's name as /proc/cpuinfo gives it (model name, else implementer/part)."""
+    try:
+        txt = open("/proc/cpuinfo").read()
+    except OSError:
+        return platform.machine()
+    fields = {}
+    for line in txt.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    parts = [f"{k} {fields[k]}" for k in ("CPU implementer", "CPU part") if k in fields]
+    return f"{platform.machine()} ({', '.join(parts)})" if parts else platform.machine()
 
 
 def run_reference(args):
@@ -514,7 +550,9 @@ def run_reference(args):
             "config": {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "sample_rows": args.ref_rows,
                        "sample_cols": args.ref_cols},
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": steps[-1]["cores"], "kind": "oracle",
-                             "sample": steps[-1]["sample"]},
+                             "sample": steps[-1]["sample"], "cpu_model": steps[-1]["cpu_model"],
+                             "quant_fold_gbs": steps[-1]["quant_fold_gbs"],
+                             "quant_fold_gbs_1core": steps[-1]["quant_fold_gbs_1core"]},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

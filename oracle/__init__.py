@@ -110,6 +110,7 @@ def lib() -> ctypes.CDLL:
             L.orc_f32_to_bf16_array.argtypes = [_P, _I, _P]
             L.orc_quant_element_array.argtypes = [_P, _P, _I, _P]
             L.orc_num_threads.restype = ctypes.c_int
+            L.orc_set_num_threads.argtypes = [ctypes.c_int]
             _lib = L
     return _lib
 
@@ -121,6 +122,11 @@ def _ptr(a: np.ndarray) -> int:
 def num_threads() -> int:
     """OpenMP threads the C oracle runs on."""
     return int(lib().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """OpenMP threads for the C oracle's later calls (for timing it on fewer cores)."""
+    lib().orc_set_num_threads(int(n))
 
 
 # ------------------------------------------------------------------ E4M3 ---

@@ -434,9 +434,12 @@ void orc_quant_element_array(const float *x, const float *s, int64_t n, uint8_t 
 }
 
 int orc_num_threads(void);
+void orc_set_num_threads(int n);
 #ifdef _OPENMP
 #include <omp.h>
 int orc_num_threads(void) { return omp_get_max_threads(); }
+void orc_set_num_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
 #else
 int orc_num_threads(void) { return 1; }
+void orc_set_num_threads(int n) { (void)n; }
 #endif
