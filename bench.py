@@ -560,7 +560,7 @@ def run_reference(args):
 # ----------------------------------------------------------------- sweep ---
 
 SWEEP_DOC = """Per-configuration report (--sweep): every kernel of each workload timed on
-its own (3 warm-ups, 10 repetitions, median; L2 flushed before each repetition),
+its own (5 warm-ups, 20 repetitions, median; L2 flushed before each repetition),
 against its binding roofline.  For a GEMM that is max(FLOP / FP8 peak,
 algorithmic bytes / HBM bandwidth): at small M the weight read dominates and the
 kernel is bound by HBM, not by the tensor cores."""
@@ -584,7 +584,7 @@ def _dev_normal(gen, shape, std, outlier_frac=0.0, factor=1.0, t_frac=0.0, dev="
     return x.to(torch.bfloat16)
 
 
-def _time_ms(fn, flush, reps=10, warm=3):
+def _time_ms(fn, flush, reps=20, warm=5):
     for _ in range(warm):
         fn()
     ts = []
