@@ -184,110 +184,102 @@ __device__ __forceinline__ uint32_t bmaxabs2(uint32_t a, uint32_t b)
     return d;
 }
 
-// Two 1x128 groups held by a half-warp (8 values per lane of each): the groups'
-// maxima are reduced in one exchange (the first step hands group a to lanes 0..7
-// and group b to lanes 8..15), each lane computes one scale, and lanes 0 and 8
-// of the half hand (r, s, f) of their group to the encoding lanes.
-__device__ __forceinline__ void row_groups2(const uint4 &va, const uint4 &vb, bool valid_a, bool valid_b,
-                                            int64_t ma, int64_t kba, int64_t mb, int64_t kbb, int lane,
-                                            uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ s, int64_t lds)
+// ---------------------------------------------------------------------------
+// 1x128 row-wise, one warp per row segment.  Rows are cut into `segs` segments
+// of 256 nv elements (nv <= QR_NV) and a warp takes a whole segment, all of its
+// 16-byte loads in flight before any group is quantized.  Load i of lane l holds
+// elements 256 i + 8 l .. + 7 of the segment, so half-warp h holds group 2 i + h
+// in load i.  The QR_NV group maxima of a half-warp are reduced in one transposed
+// exchange (each step hands half of the remaining groups to the partner lane),
+// after which lane pair (2 i, 2 i + 1) of the half holds the amax of its group in
+// load i and computes that group's scale once: the maxima, the division and the
+// reciprocal cost a few instructions per segment rather than per pair of groups.
+// The encoding lanes fetch (r, s[, f]) by shuffle.  Elements at or past K read as
+// zero and write nothing.  kNorm: x is a hidden state h, normalised on the fly
+// (rmsnorm row factor rstd[m], weight gamma[k]) before it is quantized.
+constexpr int QR_NV = 8;
+
+template <bool kPrescale>
+__device__ __forceinline__ void rows_seg_codes(const uint4 (&v)[QR_NV], const Quot &own, int lane, int nv,
+                                               int64_t kleft, uint8_t *__restrict__ qp)
 {
-    const int l16 = lane & 15;
-    const uint32_t pa = bmaxabs2(bmaxabs2(va.x, va.y), bmaxabs2(va.z, va.w));
-    const uint32_t pb = bmaxabs2(bmaxabs2(vb.x, vb.y), bmaxabs2(vb.z, vb.w));
-    const bool upper = l16 & 8;
-    uint32_t p = bmaxabs2(upper ? pb : pa, __shfl_xor_sync(0xFFFFFFFFu, upper ? pa : pb, 8));
-    p = bmaxabs2(p, __shfl_xor_sync(0xFFFFFFFFu, p, 4));
-    p = bmaxabs2(p, __shfl_xor_sync(0xFFFFFFFFu, p, 2));
-    p = babs2(bmaxabs2(p, __shfl_xor_sync(0xFFFFFFFFu, p, 1)));
-    const float own_s = group_scale(bmax_final(p));
-    const Quot own = make_quot(own_s);
-    if (l16 == 0 && valid_a)
-        s[kba * lds + ma] = own_s;
-    if (l16 == 8 && valid_b)
-        s[kbb * lds + mb] = own_s;
-    const int src_a = lane & 16, src_b = src_a | 8;
-    Quot ca, cb;
-    ca.r = __shfl_sync(0xFFFFFFFFu, own.r, src_a);
-    ca.sd = __shfl_sync(0xFFFFFFFFu, own.sd, src_a);
-    ca.f = __shfl_sync(0xFFFFFFFFu, own.f, src_a);
-    cb.r = __shfl_sync(0xFFFFFFFFu, own.r, src_b);
-    cb.sd = __shfl_sync(0xFFFFFFFFu, own.sd, src_b);
-    cb.f = __shfl_sync(0xFFFFFFFFu, own.f, src_b);
-    float f[8];
-    unpack8(va, f);
-    const uint2 codes_a = encode8(f, ca);
-    unpack8(vb, f);
-    const uint2 codes_b = encode8(f, cb);
-    if (valid_a)
-        *reinterpret_cast<uint2 *>(q + ma * ldq + kba * GRP + l16 * 8) = codes_a;
-    if (valid_b)
-        *reinterpret_cast<uint2 *>(q + mb * ldq + kbb * GRP + l16 * 8) = codes_b;
+    const int src0 = lane & 16;
+#pragma unroll
+    for (int i = 0; i < QR_NV; ++i) {
+        if (i >= nv)
+            break;
+        Quot c;
+        c.r = __shfl_sync(0xFFFFFFFFu, own.r, src0 + 2 * i);
+        c.sd = __shfl_sync(0xFFFFFFFFu, own.sd, src0 + 2 * i);
+        c.f = kPrescale ? __shfl_sync(0xFFFFFFFFu, own.f, src0 + 2 * i) : 1.0f;
+        float f[8];
+        unpack8(v[i], f);
+        const uint2 codes = encode8_t<kPrescale>(f, c);
+        if (256 * i < kleft)
+            *reinterpret_cast<uint2 *>(qp + 256 * i) = codes;
+    }
 }
 
-// ---------------------------------------------------------------------------
-// 1x128 row-wise: each half-warp takes a group; a warp owns two consecutive
-// groups per slot and two slots per iteration (four 16-byte loads in flight
-// per lane pair).  Group g = m * KB + kb, advanced incrementally.
-// kNorm: x is a hidden state h, normalised on the fly (rmsnorm row factor rstd[m],
-// weight gamma[k]) before it is quantized.
 template <bool kNorm>
-__global__ void __launch_bounds__(256) k_quant_rows(const uint16_t *__restrict__ x, int64_t M, int KB,
-                                                    int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
-                                                    float *__restrict__ s, int64_t lds,
-                                                    const float *__restrict__ rstd,
-                                                    const uint16_t *__restrict__ gamma)
+__global__ void __launch_bounds__(256, 4) k_quant_rows_seg(const uint16_t *__restrict__ x, int64_t M, int64_t K,
+                                                        int segs, int nv, int64_t ldx, uint8_t *__restrict__ q,
+                                                        int64_t ldq, float *__restrict__ s, int64_t lds,
+                                                        const float *__restrict__ rstd,
+                                                        const uint16_t *__restrict__ gamma)
 {
+    static_assert(QR_NV == 8, "the exchange below reduces eight groups per half-warp");
     const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const bool b3 = l16 & 8, b2 = l16 & 4, b1 = l16 & 2;
+    const int jo = l16 >> 1;  // the load whose group this lane's scale belongs to
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t G = M * KB;
-    const int64_t step = 2 * nwarps;  // groups between the two slots
-    const int64_t dm = step / KB;
-    const int dkb = (int)(step % KB);
-    const int64_t g0 = 2 * warp + half;
-    int64_t m = g0 / KB;
-    int kb = (int)(g0 % KB);
-    // the next iteration's two groups are loaded before this iteration's are quantized
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    auto second = [&](int64_t mm, int kk, int64_t &m1, int &kb1) {
-        m1 = mm + dm;
-        kb1 = kk + dkb;
-        if (kb1 >= KB) {
-            kb1 -= KB;
-            ++m1;
-        }
-    };
-    int64_t m1;
-    int kb1;
-    second(m, kb, m1, kb1);
-    uint4 a = m < M ? ld_stream(x + m * ldx + (int64_t)kb * GRP + l16 * 8) : zero;
-    uint4 b = m1 < M ? ld_stream(x + m1 * ldx + (int64_t)kb1 * GRP + l16 * 8) : zero;
-    for (int64_t base = 2 * warp; base < G; base += 2 * step) {
-        int64_t mn = m1 + dm;
-        int kbn = kb1 + dkb;
-        if (kbn >= KB) {
-            kbn -= KB;
-            ++mn;
-        }
-        int64_t mn1;
-        int kbn1;
-        second(mn, kbn, mn1, kbn1);
-        const uint4 an = mn < M ? ld_stream(x + mn * ldx + (int64_t)kbn * GRP + l16 * 8) : zero;
-        const uint4 bn = mn1 < M ? ld_stream(x + mn1 * ldx + (int64_t)kbn1 * GRP + l16 * 8) : zero;
+    const int64_t items = M * segs;
+    for (int64_t it = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += nwarps) {
+        const int64_t m = it / segs;
+        const int64_t k0 = (it - m * segs) * 256 * nv;  // first element of the segment
+        const int64_t kleft = K - k0 - 8 * lane;        // load i is in range iff 256 i < kleft
+        const uint16_t *xp = x + m * ldx + k0 + 8 * lane;
+        uint4 v[QR_NV];
+#pragma unroll
+        for (int i = 0; i < QR_NV; ++i)
+            v[i] = (i < nv && 256 * i < kleft) ? ld_stream(xp + 256 * i) : make_uint4(0, 0, 0, 0);
         if (kNorm) {
-            const uint4 ga = *reinterpret_cast<const uint4 *>(gamma + (int64_t)kb * GRP + l16 * 8);
-            const uint4 gb = *reinterpret_cast<const uint4 *>(gamma + (int64_t)kb1 * GRP + l16 * 8);
-            a = norm8(a, m < M ? rstd[m] : 0.0f, ga);
-            b = norm8(b, m1 < M ? rstd[m1] : 0.0f, gb);
+            const float r = rstd[m];
+            const uint16_t *gp = gamma + k0 + 8 * lane;
+#pragma unroll
+            for (int i = 0; i < QR_NV; ++i)
+                if (i < nv && 256 * i < kleft)
+                    v[i] = norm8(v[i], r, *reinterpret_cast<const uint4 *>(gp + 256 * i));
         }
-        row_groups2(a, b, m < M, m1 < M, m, kb, m1, kb1, lane, q, ldq, s, lds);
-        a = an;
-        b = bn;
-        m = mn;
-        kb = kbn;
-        m1 = mn1;
-        kb1 = kbn1;
+        uint32_t pm[QR_NV], p1[4], p2[2];
+#pragma unroll
+        for (int i = 0; i < QR_NV; ++i)
+            pm[i] = bmaxabs2(bmaxabs2(v[i].x, v[i].y), bmaxabs2(v[i].z, v[i].w));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t keep = b3 ? pm[k + 4] : pm[k], send = b3 ? pm[k] : pm[k + 4];
+            p1[k] = bmaxabs2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 8));
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t keep = b2 ? p1[k + 2] : p1[k], send = b2 ? p1[k] : p1[k + 2];
+            p2[k] = bmaxabs2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 4));
+        }
+        uint32_t p3;
+        {
+            const uint32_t keep = b1 ? p2[1] : p2[0], send = b1 ? p2[0] : p2[1];
+            p3 = bmaxabs2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2));
+        }
+        p3 = bmaxabs2(p3, __shfl_xor_sync(0xFFFFFFFFu, p3, 1));
+        const float own_s = group_scale(bmax_final(babs2(p3)));
+        const Quot own = make_quot(own_s);
+        const int64_t kbo = (k0 >> 7) + 2 * jo + half;  // this lane's group
+        if ((l16 & 1) == 0 && jo < nv && kbo * GRP < K)
+            s[kbo * lds + m] = own_s;
+        uint8_t *qp = q + m * ldq + k0 + 8 * lane;
+        if (__any_sync(0xFFFFFFFFu, own.f != 1.0f))
+            rows_seg_codes<true>(v, own, lane, nv, kleft, qp);
+        else
+            rows_seg_codes<false>(v, own, lane, nv, kleft, qp);
     }
 }
 
@@ -479,68 +471,101 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
 //   acc = sum of h[m,k]^2 over k in index order, by fused multiply-adds in fp32
 //   rstd[m] = fl32(1 / fl32(sqrt(fl32(fl32(acc / K) + eps))))
 // The index order makes the sum, and so every code downstream, independent of
-// the launch shape.  One thread owns one row and runs its chain of K FMAs; a
-// one-warp CTA stages 32 rows x 128 columns per step in shared memory (16-byte
-// cp.async copies, a ring RMS_STAGES deep so that enough bytes are in flight to
-// keep HBM busy while the chains run).  Row pitch 272 bytes: the 16-byte reads
-// of each quarter-warp fall in distinct bank groups.
+// the launch shape.  One thread owns one row and runs its chain of K FMAs, so
+// the kernel's floor is K dependent FMA latencies, and everything else is kept
+// off that chain: a CTA of two warps takes 32 rows, warp 1 copies 32 rows x 128
+// columns per step into a ring of RMS_STAGES shared-memory slots (16-byte
+// cp.async copies) and warp 0 runs the chains.  Hardware named barriers pass
+// each slot between them (full: the producer's copies of the slot have landed;
+// empty: the consumer has read it), so no thread spins.  The FMAs take the bf16
+// halves of each word directly (mixed-precision FMA: the bf16 operands enter
+// exactly, one rounding to fp32, as fmaf on the widened values), so no
+// unpacking sits between them.  Row pitch 272 bytes: the 16-byte reads of each
+// quarter-warp fall in distinct bank groups.
 constexpr int RMS_ROWS = 32;
 constexpr int RMS_PITCH = GRP * 2 + 16;
 constexpr int RMS_STAGES = 6;
+constexpr int RMS_LOOKAHEAD = RMS_STAGES - 2;  // chunks in flight behind the one signalled full
 constexpr int RMS_SMEM = RMS_STAGES * RMS_ROWS * RMS_PITCH;
 
-__device__ __forceinline__ void cp_async16_q(uint32_t dst, const void *src, uint32_t src_bytes)
+__device__ __forceinline__ void cp_async16_q(uint32_t dst, const void *src)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-__global__ void __launch_bounds__(RMS_ROWS) k_rms_rstd(const uint16_t *__restrict__ h, int64_t M, int64_t K,
-                                                       int64_t ldh, float eps, float *__restrict__ rstd)
+// named barriers 1 .. RMS_STAGES (slot full) and RMS_STAGES + 1 .. 2 RMS_STAGES
+// (slot empty), each between the CTA's two warps
+__device__ __forceinline__ void nbar_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+__device__ __forceinline__ void nbar_arrive(int id) { asm volatile("bar.arrive %0, 64;" ::"r"(id) : "memory"); }
+
+// acc + lo * lo, then + hi * hi, for the two bf16 halves of w (lo = bits 0..15)
+__device__ __forceinline__ float fma_sq_bf16x2(uint32_t w, float acc)
+{
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "fma.rn.f32.bf16 %0, lo, lo, %0;\n\tfma.rn.f32.bf16 %0, hi, hi, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w));
+    return acc;
+}
+
+__global__ void __launch_bounds__(2 * RMS_ROWS) k_rms_rstd(const uint16_t *__restrict__ h, int64_t M, int64_t K,
+                                                           int64_t ldh, float eps, float *__restrict__ rstd)
 {
     extern __shared__ __align__(16) uint8_t rms_buf[];
-    const int t = threadIdx.x;
+    const int t = threadIdx.x & 31;
     const int64_t m0 = (int64_t)blockIdx.x * RMS_ROWS;
     const int rows = (int)((M - m0) < RMS_ROWS ? (M - m0) : RMS_ROWS);
     const int chunks = (int)(K / GRP);
-    const uint32_t base = (uint32_t)__cvta_generic_to_shared(rms_buf);
-    // chunk c of the CTA's rows into ring slot c % RMS_STAGES: 32 rows x 16 pieces
-    // of 16 bytes, thread t copying pieces t, t + 32, ...; rows beyond M read as 0
-    auto issue = [&](int c) {
-        if (c < chunks) {
-            const uint32_t slot = base + (uint32_t)((c % RMS_STAGES) * RMS_ROWS * RMS_PITCH);
-#pragma unroll 4
-            for (int i = t; i < RMS_ROWS * 16; i += RMS_ROWS) {
-                const int r = i >> 4, piece = i & 15;
-                const uint16_t *src = h + (m0 + r) * ldh + (int64_t)c * GRP + piece * 8;
-                cp_async16_q(slot + (uint32_t)(r * RMS_PITCH + piece * 16), r < rows ? src : h, r < rows ? 16u : 0u);
+    if (threadIdx.x >= 32) {
+        // producer: copy i of lane t moves piece t & 15 of row (t >> 4) + 2 i, so
+        // that each warp-wide copy reads 256 contiguous bytes of two rows; rows at
+        // or past M are not copied (their sums are not used)
+        const int r0 = t >> 4;
+        const uint32_t dst0 = (uint32_t)__cvta_generic_to_shared(rms_buf) + (uint32_t)(r0 * RMS_PITCH + (t & 15) * 16);
+        const char *src0 = reinterpret_cast<const char *>(h + m0 * ldh + (t & 15) * 8);
+        const int64_t rstride = ldh * (int64_t)sizeof(uint16_t);
+#pragma unroll 1
+        for (int c = 0; c < chunks + RMS_LOOKAHEAD; ++c) {
+            if (c < chunks) {
+                const int slot = c % RMS_STAGES;
+                if (c >= RMS_STAGES)
+                    nbar_sync(1 + RMS_STAGES + slot);  // chunk c - RMS_STAGES has been read
+                const uint32_t d = dst0 + (uint32_t)(slot * RMS_ROWS * RMS_PITCH);
+                const char *p = src0 + (int64_t)c * GRP * (int64_t)sizeof(uint16_t);
+#pragma unroll
+                for (int i = 0; i < RMS_ROWS / 2; ++i)
+                    if (r0 + 2 * i < rows)
+                        cp_async16_q(d + (uint32_t)(2 * i * RMS_PITCH), p + (r0 + 2 * i) * rstride);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");  // one group per step, empty past the end
+            const int cf = c - RMS_LOOKAHEAD;                   // the chunk that is now complete
+            if (cf >= 0) {
+                asm volatile("cp.async.wait_group %0;" ::"n"(RMS_LOOKAHEAD) : "memory");
+                nbar_arrive(1 + cf % RMS_STAGES);
             }
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");  // one group per chunk, empty past the end
-    };
-#pragma unroll 1
-    for (int c = 0; c < RMS_STAGES - 1; ++c)
-        issue(c);
+        return;
+    }
     float acc = 0.0f;
 #pragma unroll 1
     for (int c = 0; c < chunks; ++c) {
-        issue(c + RMS_STAGES - 1);
-        asm volatile("cp.async.wait_group %0;" ::"n"(RMS_STAGES - 1) : "memory");  // chunk c has landed
-        __syncwarp();
-        const uint8_t *row = rms_buf + (c % RMS_STAGES) * RMS_ROWS * RMS_PITCH + t * RMS_PITCH;
+        const int slot = c % RMS_STAGES;
+        nbar_sync(1 + slot);  // chunk c has landed
+        const uint8_t *row = rms_buf + slot * RMS_ROWS * RMS_PITCH + t * RMS_PITCH;
+        uint4 v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            v[j] = *reinterpret_cast<const uint4 *>(row + 16 * j);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * j);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float lo = bf_lo(w[i]), hi = bf_hi(w[i]);
-                acc = __fmaf_rn(lo, lo, acc);
-                acc = __fmaf_rn(hi, hi, acc);
-            }
+            acc = fma_sq_bf16x2(v[j].x, acc);
+            acc = fma_sq_bf16x2(v[j].y, acc);
+            acc = fma_sq_bf16x2(v[j].z, acc);
+            acc = fma_sq_bf16x2(v[j].w, acc);
         }
-        __syncwarp();  // every lane is done with the slot before it is refilled
+        if (c + RMS_STAGES < chunks)
+            nbar_arrive(1 + RMS_STAGES + slot);  // every read of the slot is done: it may be refilled
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
     if (t < rows) {
         const float ms = __fdiv_rn(acc, (float)K);
         rstd[m0 + t] = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
@@ -1088,19 +1113,22 @@ int sm_count()
 cudaError_t launch_quant_rows(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, int64_t ldq,
                               float *s, int64_t lds, cudaStream_t st, const float *rstd, const uint16_t *gamma)
 {
-    const int KB = (int)(K / GRP);
-    const int64_t groups = M * KB;
-    const int64_t warps_needed = (groups + 3) / 4;  // 4 groups per warp per iteration
-    int64_t blocks = (warps_needed + 7) / 8;
-    const int64_t cap = (int64_t)sm_count() * 8;
+    // segments of at most 256 * QR_NV elements, as few as cover the row, each the
+    // same number of loads per lane
+    const int64_t segs = (K + 256 * QR_NV - 1) / (256 * QR_NV);
+    const int64_t nv = (K + 256 * segs - 1) / (256 * segs);
+    int64_t blocks = (M * segs + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 64;
     if (blocks > cap)
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
     if (rstd)
-        k_quant_rows<true><<<(unsigned)blocks, 256, 0, st>>>(x, M, KB, ldx, q, ldq, s, lds, rstd, gamma);
+        k_quant_rows_seg<true><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, (int)segs, (int)nv, ldx, q, ldq, s, lds,
+                                                                 rstd, gamma);
     else
-        k_quant_rows<false><<<(unsigned)blocks, 256, 0, st>>>(x, M, KB, ldx, q, ldq, s, lds, nullptr, nullptr);
+        k_quant_rows_seg<false><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, (int)segs, (int)nv, ldx, q, ldq, s, lds,
+                                                                  nullptr, nullptr);
     return cudaGetLastError();
 }
 
@@ -1129,7 +1157,7 @@ cudaError_t launch_rms_rstd(const uint16_t *h, int64_t M, int64_t K, int64_t ldh
         attr = true;
     }
     const int64_t blocks = (M + RMS_ROWS - 1) / RMS_ROWS;
-    k_rms_rstd<<<(unsigned)blocks, RMS_ROWS, RMS_SMEM, st>>>(h, M, K, ldh, eps, rstd);
+    k_rms_rstd<<<(unsigned)blocks, 2 * RMS_ROWS, RMS_SMEM, st>>>(h, M, K, ldh, eps, rstd);
     return cudaGetLastError();
 }
 

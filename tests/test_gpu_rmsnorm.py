@@ -64,6 +64,23 @@ def test_rows_of_different_magnitude_and_crafted_rows():
     _check(h, g, 1e-5, True, "crafted, eps=1e-5")
 
 
+def test_tiny_rows_with_subnormal_partial_sums():
+    """Rows of magnitude 2^-64 .. 2^-75, whose squares and early partial sums are
+    fp32 subnormals (the sum of squares must not flush them), and rows of bf16
+    subnormals, whose squares all round to zero (then eps alone sets rstd)."""
+    K = 384
+    rng = np.random.default_rng(86)
+    rows = [rng.standard_normal(K) * 2.0 ** e for e in (-64, -66, -70, -75)]
+    rows.append(rng.standard_normal(K) * 2.0 ** -130)
+    mixed = rng.standard_normal(K) * 2.0 ** -70
+    mixed[200:] *= 2.0 ** 40
+    rows.append(mixed)
+    h = I.to_bf16_bits(np.stack(rows).astype(np.float32))
+    g = _gamma(K, 86)
+    _check(h[:3], g, 0.0, True, "tiny rows, eps=0")
+    _check(h, g, 1e-30, True, "tiny and subnormal rows, eps=1e-30")
+
+
 def test_pitched_hidden_state():
     M, K, pad = 130, 384, 40
     h = I.to_bf16_bits(I.normal(83, "x", (M, K), 1.0))
