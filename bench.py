@@ -560,7 +560,8 @@ def run_reference(args):
 # ----------------------------------------------------------------- sweep ---
 
 SWEEP_DOC = """Per-configuration report (--sweep): every kernel of each workload timed on
-its own (5 warm-ups, 20 repetitions, median; L2 flushed before each repetition),
+its own (5 warm-ups, 20 repetitions, median; L2 flushed before each repetition,
+then a short device-side wait so that the host's call overhead is not timed),
 against its binding roofline.  For a GEMM that is max(FLOP / FP8 peak,
 algorithmic bytes / HBM bandwidth): at small M the weight read dominates and the
 kernel is bound by HBM, not by the tensor cores."""
@@ -585,11 +586,16 @@ def _dev_normal(gen, shape, std, outlier_frac=0.0, factor=1.0, t_frac=0.0, dev="
 
 
 def _time_ms(fn, flush, reps=20, warm=5):
+    """Median device time of fn over `reps` calls, L2 flushed before each.  A short
+    device-side wait after the flush lets the host finish enqueueing fn (argument
+    marshalling, output allocation) before the start event runs, so the host's
+    call overhead stays out of the kernel's time."""
     for _ in range(warm):
         fn()
     ts = []
     for _ in range(reps):
         flush.zero_()
+        torch.cuda._sleep(1_000_000)  # about 0.5 ms of device time
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
