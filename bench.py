@@ -562,7 +562,9 @@ def run_reference(args):
 SWEEP_DOC = """Per-configuration report (--sweep): every kernel of each workload timed on
 its own (5 warm-ups, 20 repetitions, median; L2 flushed before each repetition,
 then a short device-side wait so that the host's call overhead is not timed),
-against its binding roofline.  For a GEMM that is max(FLOP / FP8 peak,
+against its binding roofline; the HBM-bound kernels also streamed (launched back to
+back over rotating input copies larger than 3x L2, per-launch time), as they run
+inside a step.  For a GEMM that is max(FLOP / FP8 peak,
 algorithmic bytes / HBM bandwidth): at small M the weight read dominates and the
 kernel is bound by HBM, not by the tensor cores."""
 
@@ -618,12 +620,15 @@ def run_sweep(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     rows = []
 
-    def emit(cfg, kernel, ms, nbytes=None, flop=None):
+    def emit(cfg, kernel, ms, nbytes=None, flop=None, ms_stream=None):
         r = {"sweep": True, "config": cfg, "kernel": kernel, "ms": round(ms, 4)}
         if flop is None:
             r["gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
             r["frac_hbm"] = round(r["gbs"] / bw, 3)
             r["bound"] = "hbm"
+            if ms_stream is not None:
+                r["ms_stream"] = round(ms_stream, 4)
+                r["frac_stream"] = round(nbytes / (ms_stream * 1e-3) / 1e9 / bw, 3)
         else:
             r["tflops"] = round(flop / (ms * 1e-3) / 1e12, 1)
             t_roof = max(flop / (fp8 * 1e12), nbytes / (bw * 1e9)) * 1e3
@@ -632,6 +637,33 @@ def run_sweep(args):
             r["frac_fp8_peak"] = round(r["tflops"] / fp8, 3)
         rows.append(r)
         print(json.dumps(r), flush=True)
+
+    def streamed_ms(fn, srcs):
+        """Per-launch device time of fn launched back to back over rotating copies of
+        its inputs (srcs: the tensors fn takes), the copies together larger than 3x
+        L2, so each launch reads from HBM without a flush in between; the launches
+        are enqueued behind a device-side wait, so the host's call overhead is not
+        timed.  The fixed cost of one event pair and one launch ramp is spread over
+        the launches, as inside a step."""
+        nb = sum(t.numel() * t.element_size() for t in srcs)
+        n = max(2, -(-(400 << 20) // nb))
+        sets = [srcs] + [[t.clone() for t in srcs] for _ in range(n - 1)]
+        reps = max(8, n)
+        for i in range(n):
+            fn(*sets[i])
+        ts = []
+        for _ in range(5):
+            torch.cuda._sleep(2_000_000)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for i in range(reps):
+                fn(*sets[i % n])
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / reps)
+        del sets
+        ts.sort()
+        return ts[len(ts) // 2]
 
     def _splitk_ws(kind, M, N, K):
         """Workspace for the split-K plan of this GEMM, None when it runs one pass
@@ -677,35 +709,41 @@ def run_sweep(args):
             st = torch.from_numpy(s).to(dev)
             inv = (1.0 / st).contiguous()
             wf, xf = w.clone(), x.clone()
-            par = [0]
+            par = {}
 
-            def fold():
-                # alternate s and 1/s so repeated folds keep the tensors stationary
-                rlq.uaq_fold_(wf, st if par[0] == 0 else inv, xf)
-                par[0] ^= 1
-            emit(cfg, "uaq_fold", _time_ms(fold, flush), nbytes=4 * (N * K + M * K))
+            def fold(wt, xt):
+                # alternate s and 1/s per tensor so repeated folds keep it stationary
+                p_ = par.get(wt.data_ptr(), 0)
+                rlq.uaq_fold_(wt, st if p_ == 0 else inv, xt)
+                par[wt.data_ptr()] = p_ ^ 1
+            emit(cfg, "uaq_fold", _time_ms(lambda: fold(wf, xf), flush), nbytes=4 * (N * K + M * K),
+                 ms_stream=streamed_ms(fold, [wf, xf]))
             if per_channel:
                 # AQN on a norm scale of K channels: read 2 + 4, write 2 bytes per channel
                 gam = torch.ones(K, dtype=torch.bfloat16, device=dev)
                 zz = torch.randn(K, generator=torch.Generator(device=dev).manual_seed(5), device=dev)
                 emit(cfg, "aqn_perturb", _time_ms(lambda: rlq.aqn_perturb_(gam, zz, 1e-3), flush), nbytes=8 * K)
-        emit(cfg, "quant_rows_x", _time_ms(lambda: rlq.quant_act_1x128(x), flush), nbytes=B_ROWS * M * K)
+        emit(cfg, "quant_rows_x", _time_ms(lambda: rlq.quant_act_1x128(x), flush), nbytes=B_ROWS * M * K,
+             ms_stream=streamed_ms(lambda t: rlq.quant_act_1x128(t), [x]))
         if norm:
             # RMSNorm of a hidden state of X's shape fused with the quantizer (x here
             # stands in for the hidden state): one read of h, the codes, the scales
             # and the per-row factors
             gam = torch.ones(K, dtype=torch.bfloat16, device=dev)
             emit(cfg, "rmsnorm_quant_rows_x", _time_ms(lambda: rlq.rmsnorm_quant_act_1x128(x, gam, 1e-5), flush),
-                 nbytes=B_ROWS * M * K + 4 * M)
+                 nbytes=B_ROWS * M * K + 4 * M,
+                 ms_stream=streamed_ms(lambda t: rlq.rmsnorm_quant_act_1x128(t, gam, 1e-5), [x]))
             emit(cfg, "rmsnorm_quant_dual_x",
                  _time_ms(lambda: rlq.rmsnorm_quant_act_1x128(x, gam, 1e-5, colwise=True), flush),
-                 nbytes=B_DUAL * M * K + 4 * M)
+                 nbytes=B_DUAL * M * K + 4 * M,
+                 ms_stream=streamed_ms(lambda t: rlq.rmsnorm_quant_act_1x128(t, gam, 1e-5, colwise=True), [x]))
         if full:
             emit(cfg, "quant_dual_x", _time_ms(lambda: rlq.quant_act_1x128(x, colwise=True), flush),
-                 nbytes=B_DUAL * M * K)
+                 nbytes=B_DUAL * M * K, ms_stream=streamed_ms(lambda t: rlq.quant_act_1x128(t, colwise=True), [x]))
         emit(cfg, "quant_weight" + ("_t" if full else ""),
              _time_ms(lambda: rlq.quant_weight_128x128(w, transposed=full), flush),
-             nbytes=(B_WEIGHT_T if full else B_WEIGHT) * N * K)
+             nbytes=(B_WEIGHT_T if full else B_WEIGHT) * N * K,
+             ms_stream=streamed_ms(lambda t: rlq.quant_weight_128x128(t, transposed=full), [w]))
         if nvfp4:
             nvfp4_gemm_row(cfg, x, w)
         qx, sx, qxT, sxc = rlq.quant_act_1x128(x, colwise=full)
@@ -721,11 +759,12 @@ def run_sweep(args):
         if per_channel:
             # read 2 + write 1 bytes per element, the row scale and its K/128 copies
             emit(cfg, "quant_per_row_x", _time_ms(lambda: rlq.quant_per_row(x), flush),
-                 nbytes=3 * M * K + 4 * M * (1 + K // 128))
+                 nbytes=3 * M * K + 4 * M * (1 + K // 128), ms_stream=streamed_ms(lambda t: rlq.quant_per_row(t), [x]))
             emit(cfg, "quant_per_row_w", _time_ms(lambda: rlq.quant_per_row(w), flush),
-                 nbytes=3 * N * K + 4 * N * (1 + K // 128))
+                 nbytes=3 * N * K + 4 * N * (1 + K // 128), ms_stream=streamed_ms(lambda t: rlq.quant_per_row(t), [w]))
             # NVFP4 weights: read 2, write 0.5 (codes) + 1/16 (block scales) bytes per element
-            emit(cfg, "quant_nvfp4_w", _time_ms(lambda: rlq.quant_nvfp4(w), flush), nbytes=2.5625 * N * K)
+            emit(cfg, "quant_nvfp4_w", _time_ms(lambda: rlq.quant_nvfp4(w), flush), nbytes=2.5625 * N * K,
+                 ms_stream=streamed_ms(lambda t: rlq.quant_nvfp4(t), [w]))
             pqx, _, psx = rlq.quant_per_row(x)
             pqw, _, psw = rlq.quant_per_row(w)
             emit(cfg, "gemm_fprop_per_channel",
@@ -740,7 +779,7 @@ def run_sweep(args):
             del pqx, pqw, psx, psw
         if full:
             emit(cfg, "quant_dual_dy", _time_ms(lambda: rlq.quant_act_1x128(dy, colwise=True), flush),
-                 nbytes=B_DUAL * M * N)
+                 nbytes=B_DUAL * M * N, ms_stream=streamed_ms(lambda t: rlq.quant_act_1x128(t, colwise=True), [dy]))
             qdy, sdy, qdyT, sdyc = rlq.quant_act_1x128(dy, colwise=True)
             dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
             dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
@@ -757,7 +796,8 @@ def run_sweep(args):
             emit(cfg, "gemm_wgrad", _time_ms(lambda: rlq.gemm_wgrad(qdyT, sdyc, qxT, sxc, out=dw), flush),
                  nbytes=gemm_bytes(N, K, M), flop=2.0 * M * N * K)
             if cfg.startswith("train_step_8b"):
-                emit(cfg, "quant_nvfp4_w", _time_ms(lambda: rlq.quant_nvfp4(w), flush), nbytes=2.5625 * N * K)
+                emit(cfg, "quant_nvfp4_w", _time_ms(lambda: rlq.quant_nvfp4(w), flush), nbytes=2.5625 * N * K,
+                     ms_stream=streamed_ms(lambda t: rlq.quant_nvfp4(t), [w]))
                 # fp32 accumulation (micro-batches): the operands, and the fp32 gradient
                 # read and written by the epilogue (no bf16 output)
                 acc = torch.zeros((N, K), dtype=torch.float32, device=dev)
@@ -809,11 +849,13 @@ def run_sweep(args):
         del w
     if args.sweep_md:
         with open(args.sweep_md, "w") as f:
-            f.write("| Config | Kernel | ms | TFLOP/s | GB/s | bound | fraction of roofline |\n|---|---|---:|---:|---:|---|---:|\n")
+            f.write("| Config | Kernel | ms | TFLOP/s | GB/s | bound | fraction of roofline | streamed ms (fraction) |\n"
+                    "|---|---|---:|---:|---:|---|---:|---:|\n")
             for r in rows:
                 frac = r.get("frac_roofline", r.get("frac_hbm"))
+                stream = f"{r['ms_stream']} ({r['frac_stream']})" if "ms_stream" in r else ""
                 f.write(f"| {r['config']} | {r['kernel']} | {r['ms']} | {r.get('tflops', '')} | {r.get('gbs', '')} | "
-                        f"{r['bound']} | {frac} |\n")
+                        f"{r['bound']} | {frac} | {stream} |\n")
 
 
 # ------------------------------------------------------------- one kernel ---
