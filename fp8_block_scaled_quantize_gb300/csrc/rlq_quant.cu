@@ -892,8 +892,9 @@ __global__ void __launch_bounds__(256) k_quant_per_row_reg_cta(const uint16_t *_
 //   element     q  = E2M1_RNsat(fl32(x / fl32(decode(sb) * st))), +-0 when that is 0.
 // Three launches: the tensor amax (packed maxima, one atomic max per warp, the
 // bits of a non-negative float ordering as unsigned integers), the block pass
-// (one thread per block: IEEE quotients, E2M1 codes by the hardware conversion
-// two at a time), and one thread that turns the amax into st.
+// (one thread per block; the codes of the IEEE quotients through a bracketing test
+// that divides only next to a rounding point, E2M1 codes by the hardware
+// conversion two at a time), and one thread that turns the amax into st.
 
 // E2M1 codes of two values (RN-even onto 0, 0.5, 1, 1.5, 2, 3, 4, 6, saturating at
 // +-6, sign of zero kept), `lo` in bits 0..3 and `hi` in bits 4..7: the hardware
@@ -907,25 +908,22 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
     return d;
 }
 
-// A quotient that gives the E2M1 code of the IEEE quotient fl32(x / S), for S a
-// normal fp32 value above 2^-100 and r = RN(1 / S).  q0 = RN(x * r) is within 2
-// ulps of x / S (one rounding of the product plus |x| times the reciprocal's half
-// ulp), and fl32(x / S) within half an ulp, so the two can fall on different sides
-// of a rounding point of the E2M1 code only if q0 lies within 3 ulps of one.  Those
-// points are the midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5 and 5 (codes saturate at
-// 6, so nothing above 5 decides anything): each has at most 3 significant bits, i.e.
-// its low 21 mantissa bits are 0 and its biased exponent lies in 125..129.  Every
-// q0 whose magnitude has an exponent in 124..129 and low 21 mantissa bits within 4
-// of a multiple of 2^21 takes the IEEE division instead (exact E2M1 values such as
-// 1.0 take it too, harmlessly); all other quotients keep q0.
-__device__ __forceinline__ float nv_quot(float x, float S, float r)
+// E2M1 codes of the pair fl32(x0 / S), fl32(x1 / S), for S a normal fp32 value above
+// 2^-100 and r = RN(1 / S).  q = RN(x * r) is within about 1.5 ulps of the IEEE
+// quotient, so q * (1 - 2^-20) and q * (1 + 2^-20) (each rounded) bracket it, and
+// since rounding to E2M1 is monotone, where the two ends give the same codes those
+// are the codes of the IEEE quotients; only pairs with a quotient within 2^-20 of a
+// rounding point (a few in 10^5) take the divisions.  Sign of zero kept (q has the
+// sign of x).
+__device__ __forceinline__ uint32_t nv_codes2(float x0, float x1, float S, float r)
 {
-    const float q0 = __fmul_rn(x, r);
-    const uint32_t u = __float_as_uint(q0) & 0x7FFFFFFFu;
-    const uint32_t ex = u >> 23;
-    if (ex >= 124u && ex <= 129u && ((u + 4u) & 0x1FFFFFu) <= 8u)
-        return __fdiv_rn(x, S);
-    return q0;
+    const float2 q = __fmul2_rn(make_float2(x0, x1), make_float2(r, r));
+    const float2 lo = __fmul2_rn(q, make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f));
+    const float2 hi = __fmul2_rn(q, make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f));
+    const uint32_t cl = e2m1x2(lo.x, lo.y), ch = e2m1x2(hi.x, hi.y);
+    if (cl == ch)
+        return cl;
+    return e2m1x2(__fdiv_rn(x0, S), __fdiv_rn(x1, S));
 }
 
 // Exact fp32 value of a finite E4M3 code.
@@ -977,6 +975,13 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const uint16_t *__restrict_
 {
     const float amax = __uint_as_float(*amax_bits);
     const float st = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);  // 6 * 448
+    // block codes by the bracketing test of nv_codes2: (amax_b * RN(1/6)) * RN(1/st) is
+    // within a few ulps of fl32(fl32(amax_b / 6) / st), and where the E4M3 codes of
+    // its two ends (x (1 -+ 2^-20)) agree they are the code; else both IEEE divisions.
+    // A tensor scale below 2^-100 (1 / st may overflow) always divides.
+    const bool st_fast = st >= 0x1p-100f;
+    const float rst = __frcp_rn(st);
+    constexpr float kR6 = 1.0f / 6.0f;  // RN(1/6)
     const int KB = (int)(K / 16);
     // CTAs walk whole rows, a thread per 16-element block; the next block's 32 bytes
     // are loaded before this one is encoded (two loads in flight per thread)
@@ -1004,16 +1009,18 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const uint16_t *__restrict_
             p1 = ld_stream(w + nn * ldw + (int64_t)kk * 16 + 8);
         }
         float f[16];
-        float lo8[8], hi8[8];
-        unpack8(c0, lo8);
-        unpack8(c1, hi8);
-        float ab = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            f[j] = lo8[j], f[j + 8] = hi8[j];
-            ab = fmaxf(ab, fmaxf(fabsf(lo8[j]), fabsf(hi8[j])));
+        unpack8(c0, *reinterpret_cast<float(*)[8]>(&f[0]));
+        unpack8(c1, *reinterpret_cast<float(*)[8]>(&f[8]));
+        const uint32_t pm = bmaxabs2(bmaxabs2(bmaxabs2(c0.x, c0.y), bmaxabs2(c0.z, c0.w)),
+                                     bmaxabs2(bmaxabs2(c1.x, c1.y), bmaxabs2(c1.z, c1.w)));
+        const float ab = bmax_final(babs2(pm));
+        uint32_t e;
+        {
+            const float qs = __fmul_rn(__fmul_rn(ab, kR6), rst);
+            const uint32_t ew = e4m3x2(__fmul_rn(qs, 1.0f - 0x1p-20f), __fmul_rn(qs, 1.0f + 0x1p-20f));
+            e = (st_fast && (ew & 0xFFu) == (ew >> 8)) ? (ew & 0xFFu)
+                                                     : (e4m3x2(__fdiv_rn(__fdiv_rn(ab, 6.0f), st), 0.0f) & 0xFFu);
         }
-        const uint32_t e = e4m3x2(__fdiv_rn(__fdiv_rn(ab, 6.0f), st), 0.0f) & 0xFFu;
         sb[n * ldsb + kb] = (uint8_t)e;
         const float S = __fmul_rn(e4m3_value(e), st);
         uint32_t word[2] = {0u, 0u};
@@ -1029,7 +1036,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const uint16_t *__restrict_
             const float r = __frcp_rn(S);
 #pragma unroll
             for (int j = 0; j < 16; j += 2)
-                word[j >> 3] |= e2m1x2(nv_quot(f[j], S, r), nv_quot(f[j + 1], S, r)) << (4 * (j & 7));
+                word[j >> 3] |= nv_codes2(f[j], f[j + 1], S, r) << (4 * (j & 7));
         }
         *reinterpret_cast<uint2 *>(q + n * ldq + kb * 8) = make_uint2(word[0], word[1]);
         c0 = p0, c1 = p1, n = nn, kb = kk;

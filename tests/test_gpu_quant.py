@@ -36,6 +36,16 @@ def test_rowwise_parity(M, K):
     _check_rows(x, q, s)
 
 
+@pytest.mark.parametrize("K", [640, 1152, 1920, 2176, 2304, 4224, 6272])
+def test_rowwise_segment_boundaries(K):
+    """Row lengths whose segments (up to 16 groups per warp) end inside the last
+    load or leave whole loads unused: 3, 5, 8 loads of one segment; 2, 3 and 4
+    segments per row with 5 to 7 loads each."""
+    x = normal_bits(11, (37, K))
+    q, s, _, _ = rlq.quant_act_1x128(to_dev(x))
+    _check_rows(x, q, s)
+
+
 @pytest.mark.parametrize("M,K", SHAPES)
 def test_dual_parity(M, K):
     x = normal_bits(11, (M, K), std=1e-3)

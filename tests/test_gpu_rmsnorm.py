@@ -44,6 +44,16 @@ def test_ragged_shapes(M, K, colwise):
     _check(h, _gamma(K, K), 1e-6, colwise, f"M={M} K={K}")
 
 
+@pytest.mark.parametrize("K", [256, 640, 768, 896, 1664])
+def test_row_factor_ring_boundaries(K):
+    """Row lengths of 2, 5, 6, 7 and 13 chunks of 128 columns around the row-factor
+    kernel's six-slot ring (fewer chunks than slots, exactly the lookahead, one
+    full ring, one past it, two wraps), on 70 rows (a partial last CTA)."""
+    h = I.to_bf16_bits(I.normal(87, "x", (70, K), 1.0, 70, K))
+    _check(h, _gamma(K, K + 1), 1e-6, True, f"K={K}")
+    _check(h, _gamma(K, K + 1), 1e-6, False, f"K={K}")
+
+
 def test_rows_of_different_magnitude_and_crafted_rows():
     """Rows spanning 2^-40 .. 2^20 (each row's factor must go to its own row),
     constant +-2^j rows (closed form, eps = 0 exact), the index-order row
