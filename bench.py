@@ -644,8 +644,11 @@ def run_sweep(args):
         L2, so each launch reads from HBM without a flush in between; the launches
         are enqueued behind a device-side wait, so the host's call overhead is not
         timed.  The fixed cost of one event pair and one launch ramp is spread over
-        the launches, as inside a step."""
+        the launches, as inside a step.  None for inputs under 16 MB (the host's
+        launch rate would set the time)."""
         nb = sum(t.numel() * t.element_size() for t in srcs)
+        if nb < (16 << 20):
+            return None  # too small to stream from HBM without the host's launch rate binding
         n = max(2, -(-(400 << 20) // nb))
         sets = [srcs] + [[t.clone() for t in srcs] for _ in range(n - 1)]
         reps = max(8, n)
@@ -653,7 +656,7 @@ def run_sweep(args):
             fn(*sets[i])
         ts = []
         for _ in range(5):
-            torch.cuda._sleep(2_000_000)
+            torch.cuda._sleep(4_000_000)  # about 2 ms: the host enqueues all launches behind it
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             for i in range(reps):

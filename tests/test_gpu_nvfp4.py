@@ -91,3 +91,31 @@ def test_nvfp4_midpoint_quotients_under_non_power_of_two_block_scales():
     q, sb, st = rlq.quant_nvfp4(to_dev(w))
     rlq.check()
     _check(w, q, sb, st)
+
+
+def test_nvfp4_block_scales_on_e4m3_grid_points_and_midpoints():
+    """Tensor scale 1 (tensor amax 2688) and block maxima 6 * c for c on the E4M3
+    grid and halfway between grid neighbours: amax_b / 6 / st is then exactly a code
+    or a rounding tie (to the even code), where the block scale's reciprocal-based
+    estimate brackets a rounding point and the kernel must fall back to the IEEE
+    divisions.  Block maxima that are not bf16-exact are skipped."""
+    codes = np.arange(0x08, 0x7F, dtype=np.uint8)  # normal positive E4M3 values up to 448
+    vals = oracle.e4m3_decode(codes).astype(np.float64)
+    cands = np.concatenate([vals, (vals[:-1] + vals[1:]) / 2]) * 6.0
+    bf = oracle.bf16_to_f32(I.to_bf16_bits(cands.astype(np.float32))).astype(np.float64)
+    cands = cands[bf == cands]  # block maxima exact in bf16
+    assert cands.size > 100
+    rng = np.random.default_rng(88)
+    blocks = []
+    for a in cands:
+        v = (rng.uniform(-1.0, 1.0, 16) * a).astype(np.float32)
+        v[int(rng.integers(0, 16))] = a * (1 if rng.random() < 0.5 else -1)
+        blocks.append(v)
+    row = np.concatenate(blocks)
+    pad = (-row.size) % 128
+    row = np.concatenate([row, np.zeros(pad, np.float32)])
+    row[-1] = 2688.0  # tensor amax 6 * 448: tensor scale exactly 1
+    w = I.to_bf16_bits(np.tile(row, (3, 1)))
+    q, sb, st = rlq.quant_nvfp4(to_dev(w))
+    rlq.check()
+    _check(w, q, sb, st)
