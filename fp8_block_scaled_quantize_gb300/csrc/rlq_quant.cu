@@ -300,12 +300,17 @@ __global__ void __launch_bounds__(256, 4) k_quant_rows_seg(const uint16_t *__res
 //
 // Column pass: 128 threads reduce the eight per-warp column maxima and compute
 // the 128 column scales once; then every thread encodes two adjacent columns
-// over 32 rows from the staged tile and writes their codes transposed.
+// over 32 rows from the staged tile, and the transposed codes go back through
+// the same buffer so that they leave as whole 128-byte lines of qT.
 //
 // Tiles are ordered with the row block fastest: CTAs that run together write
 // whole rows of the transposed codes (contiguous 128-byte pieces of one row)
 // rather than one piece of many rows.
 constexpr int TP = GRP + 8;  // staging row pitch in bf16 elements
+// pitch in bytes of the transposed codes staged in the same buffer (128 rows of 128
+// codes); it fits in the tile's 128 x TP bf16
+constexpr int TQ_PITCH = GRP + 16;
+static_assert(GRP * TQ_PITCH <= GRP * TP * 2, "the staged codes must fit in the tile buffer");
 
 // Row codes of the eight rows a lane holds, read back from the staged tile (each
 // lane reads the words it wrote itself); (r, s[, f]) of row group i come from
@@ -447,7 +452,25 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
         const int r0 = rq * 32;
         uint8_t *d0 = qT + k * ldqT + m0 + r0;
         uint8_t *d1 = d0 + ldqT;
-        if (r0 + 32 <= rows) {
+        if (rows == GRP) {
+            // full tile: the transposed codes are staged in the tile buffer (every thread
+            // has read its columns of it) and leave by whole 128-byte lines, each warp
+            // writing four rows of qT, rather than as 32-byte runs of 64 rows per warp
+            // (measured 11% faster on [8192, 14336])
+            __syncthreads();
+            uint8_t *tq = reinterpret_cast<uint8_t *>(tile);
+            *reinterpret_cast<uint4 *>(tq + (2 * c2) * TQ_PITCH + r0) = make_uint4(e[0], e[1], e[2], e[3]);
+            *reinterpret_cast<uint4 *>(tq + (2 * c2) * TQ_PITCH + r0 + 16) = make_uint4(e[4], e[5], e[6], e[7]);
+            *reinterpret_cast<uint4 *>(tq + (2 * c2 + 1) * TQ_PITCH + r0) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(tq + (2 * c2 + 1) * TQ_PITCH + r0 + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+            __syncthreads();
+#pragma unroll
+            for (int rd = 0; rd < 4; ++rd) {
+                const int cl = rd * 32 + (t >> 3), ch = t & 7;
+                const uint4 v = *reinterpret_cast<const uint4 *>(tq + cl * TQ_PITCH + ch * 16);
+                *reinterpret_cast<uint4 *>(qT + (kb * GRP + cl) * ldqT + m0 + ch * 16) = v;
+            }
+        } else if (r0 + 32 <= rows) {
             reinterpret_cast<uint4 *>(d0)[0] = make_uint4(e[0], e[1], e[2], e[3]);
             reinterpret_cast<uint4 *>(d0)[1] = make_uint4(e[4], e[5], e[6], e[7]);
             reinterpret_cast<uint4 *>(d1)[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -579,7 +602,8 @@ __global__ void __launch_bounds__(2 * RMS_ROWS) k_rms_rstd(const uint16_t *__res
 // is a packed bf16 maximum, a warp shuffle reduction and one exchange through
 // shared memory.  Each thread then encodes its 64 elements: one 32-bit word of
 // codes per row, and for the [K,N] copy four 4x4 byte transposes (byte
-// permutes) turn the sixteen row words into four 16-byte runs, one per column.
+// permutes) turn the sixteen row words into four 16-byte runs, one per column,
+// which go out through shared memory as whole 128-byte lines of the copy.
 // Blocks are ordered with the row block fastest, as in the fused quantizer.
 __device__ __forceinline__ uint2 ld_stream8(const uint16_t *p)
 {
@@ -625,6 +649,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_weight(const uint16_t *__restr
                                                          uint8_t *__restrict__ qT, int64_t ldqT, int64_t NB, int64_t KB)
 {
     __shared__ float red[8];
+    __shared__ __align__(16) uint8_t tqs[GRP * GRP];  // transposed codes: 128 rows of 128 bytes, swizzled
     const int t = threadIdx.x, j = t & 31, a = t >> 5;
 
     for (int64_t kb = blockIdx.y; kb < KB; kb += gridDim.y)
@@ -674,12 +699,23 @@ __global__ void __launch_bounds__(256, 4) k_quant_weight(const uint16_t *__restr
                 for (int k = 0; k < 4; ++k)
                     col[k][b] = cc[k];
             }
-            uint8_t *dT = qT + (kb * GRP + 4 * j) * ldqT + n0 + 16 * a;
+            // staged as row 4 j + k of the block, 16-byte chunk a (XOR-swizzled by
+            // (row / 4) % 8: conflict-free both ways), then written out as whole
+            // 128-byte lines, each warp four rows of qT (measured 13-15% faster than
+            // each warp writing 16 bytes into each of 128 rows)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(dT + k * ldqT) = make_uint4(col[k][0], col[k][1], col[k][2], col[k][3]);
+                *reinterpret_cast<uint4 *>(tqs + (4 * j + k) * GRP + ((a ^ (j & 7)) << 4)) =
+                    make_uint4(col[k][0], col[k][1], col[k][2], col[k][3]);
+            __syncthreads();
+#pragma unroll
+            for (int rd = 0; rd < 4; ++rd) {
+                const int cl = rd * 32 + (t >> 3), ch = t & 7;
+                const uint4 v = *reinterpret_cast<const uint4 *>(tqs + cl * GRP + ((ch ^ ((cl >> 2) & 7)) << 4));
+                *reinterpret_cast<uint4 *>(qT + (kb * GRP + cl) * ldqT + n0 + ch * 16) = v;
+            }
         }
-        __syncthreads();  // red is reused by the next block
+        __syncthreads();  // red and the staged codes are reused by the next block
     }
 }
 
