@@ -13,7 +13,8 @@ workload (X bf16 [8192, 4096], W bf16 [14336, 4096], dY bf16 [8192, 14336]):
   6. DGrad  dX = dY W
   7. WGrad  dW = dY^T X
 
-Every step launches only this library's kernels (8 launches).  L2 is flushed
+Every step launches only this library's kernels (7 launches; the fold of W and
+of the norm weight is one).  L2 is flushed
 (a 256 MB device write, outside the timed events) before every step; each
 step is timed with CUDA events on the launching stream, per kernel and whole.
 
@@ -200,7 +201,7 @@ class Step:
         self.w.copy_(host["w"])
         self.dy.copy_(host["dy"])
         self.parity = 0
-        self.launches_per_step = 8
+        self.launches_per_step = 7
 
     def run(self, stream: int, events=None):
         """Launch the step; if `events` (8 CUDA events) is given, record them

@@ -1104,20 +1104,15 @@ __global__ void __launch_bounds__(256) k_aqn_perturb(uint16_t *__restrict__ gamm
 // UAQ fold, in place: divide (w) or multiply (prev) column k by s[k] in fp32,
 // round to bf16.  8 elements per thread and vector; each thread handles FOLD_ROWS
 // rows per iteration with all their loads issued first (bytes in flight hide
-// the memory latency); row groups over blockIdx.y (grid-stride).
+// the memory latency).  One launch for both tensors: CTA rows blockIdx.y < gw
+// fold w (row groups grid-strided over gw), the rest fold prev.
 constexpr int FOLD_ROWS = 4;
 
 template <bool kDivide>
-__global__ void __launch_bounds__(256) k_uaq_fold(uint16_t *__restrict__ a, int64_t rows, int64_t K8,
-                                                  int64_t lda, const float *__restrict__ s)
+__device__ __forceinline__ void fold_rows(uint16_t *__restrict__ a, int64_t rows, int64_t lda, int64_t v,
+                                          const float (&sv)[8], int64_t y, int64_t gy)
 {
-    const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (v >= K8)
-        return;
-    const float4 s0 = __ldg(reinterpret_cast<const float4 *>(s) + 2 * v);
-    const float4 s1 = __ldg(reinterpret_cast<const float4 *>(s) + 2 * v + 1);
-    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-    for (int64_t r0 = (int64_t)blockIdx.y * FOLD_ROWS; r0 < rows; r0 += (int64_t)gridDim.y * FOLD_ROWS) {
+    for (int64_t r0 = y * FOLD_ROWS; r0 < rows; r0 += gy * FOLD_ROWS) {
         uint4 in[FOLD_ROWS];
 #pragma unroll
         for (int i = 0; i < FOLD_ROWS; ++i)
@@ -1141,6 +1136,22 @@ __global__ void __launch_bounds__(256) k_uaq_fold(uint16_t *__restrict__ a, int6
             *(reinterpret_cast<uint4 *>(a + (r0 + i) * lda) + v) = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
+}
+
+__global__ void __launch_bounds__(256) k_uaq_fold(uint16_t *__restrict__ w, int64_t N, int64_t ldw,
+                                                  uint16_t *__restrict__ prev, int64_t R, int64_t ldp, int64_t K8,
+                                                  const float *__restrict__ s, int gw)
+{
+    const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= K8)
+        return;
+    const float4 s0 = __ldg(reinterpret_cast<const float4 *>(s) + 2 * v);
+    const float4 s1 = __ldg(reinterpret_cast<const float4 *>(s) + 2 * v + 1);
+    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    if ((int)blockIdx.y < gw)
+        fold_rows<true>(w, N, ldw, v, sv, blockIdx.y, gw);
+    else
+        fold_rows<false>(prev, R, ldp, v, sv, blockIdx.y - gw, (int64_t)gridDim.y - gw);
 }
 
 int sm_count()
@@ -1292,19 +1303,14 @@ cudaError_t launch_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, cons
     const unsigned gx = (unsigned)((K8 + 255) / 256);
     auto gy = [](int64_t rows) {
         const int64_t g = (rows + FOLD_ROWS - 1) / FOLD_ROWS;
-        return (unsigned)(g < 65535 ? g : 65535);
+        return (int)(g < 32767 ? g : 32767);
     };
-    if (N > 0) {
-        k_uaq_fold<true><<<dim3(gx, gy(N)), 256, 0, st>>>(w, N, K8, ldw, s);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess)
-            return e;
-    }
-    if (prev && R > 0) {
-        k_uaq_fold<false><<<dim3(gx, gy(R)), 256, 0, st>>>(prev, R, K8, ldp, s);
-        return cudaGetLastError();
-    }
-    return cudaSuccess;
+    const int gw = N > 0 ? gy(N) : 0;
+    const int gp = (prev && R > 0) ? gy(R) : 0;
+    if (gw + gp == 0)
+        return cudaSuccess;
+    k_uaq_fold<<<dim3(gx, (unsigned)(gw + gp)), 256, 0, st>>>(w, N, ldw, prev, R, ldp, K8, s, gw);
+    return cudaGetLastError();
 }
 
 }  // namespace rlq
