@@ -669,10 +669,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 continue;
             }
-            // This thread's row, 128 columns, stored directly (512 or 256 contiguous
-            // bytes per thread); rows beyond R are skipped.
+            // Single CTAs: this thread's row, 128 columns, stored directly (512 or 256
+            // contiguous bytes per thread); rows beyond R are skipped.  (Pairs leave by
+            // TMA above; the host pairs CTAs only for unsplit GEMMs.)
             const int grow = mt * Cf::TILE_M + row_offset<kPair>() + row;
-            if (ok && half_ok && grow < p.R) {
+            if (!kPair && ok && half_ok && grow < p.R) {
                 if (p.out_mode == OUT_F32_PARTIAL) {
                     // fp32 partial of this contraction range, plane `split` of [splits][R][C]
                     float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)wu.split * p.R + grow) * p.C + col0);
