@@ -970,11 +970,15 @@ __device__ __forceinline__ float e4m3_value(uint32_t e)
     return (e & 0x80u) ? -v : v;
 }
 
-// Plain cached 16-byte load: the amax pass leaves W in L2 for the block pass.
+// 16-byte load that allocates in L2 (the amax pass leaves W there for the block
+// pass) but not in L1, through the read-only path (measured 3-5% faster than a
+// plain cached load for the amax pass).
 __device__ __forceinline__ uint4 ld_keep(const uint16_t *p)
 {
     uint4 v;
-    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
     return v;
 }
 
