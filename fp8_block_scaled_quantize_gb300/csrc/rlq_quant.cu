@@ -27,10 +27,13 @@ namespace {
 
 constexpr int GRP = 128;
 
+// Loads of a kernel's input, which no thread of the kernel writes: the read-only
+// path without L1 allocation (measured 2% faster for the dual quantizer than an
+// evict-first streaming load, the same elsewhere).
 __device__ __forceinline__ uint4 ld_stream(const uint16_t *p)
 {
     uint4 v;
-    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
@@ -608,7 +611,7 @@ __global__ void __launch_bounds__(2 * RMS_ROWS) k_rms_rstd(const uint16_t *__res
 __device__ __forceinline__ uint2 ld_stream8(const uint16_t *p)
 {
     uint2 v;
-    asm volatile("ld.global.cs.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
     return v;
 }
 
