@@ -290,6 +290,21 @@ def run_ours(args):
     _barrier(dist)
     rlq.check(sh)
 
+    # the same steps with only a start and an end event each: the per-kernel events
+    # above sit between the kernels in the stream and keep each kernel from being
+    # scheduled while the previous one drains (programmatic dependent launch)
+    plain = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        st.run(sh)
+        a1.record()
+        plain.append((a0, a1))
+    torch.cuda.synchronize()
+    rlq.check(sh)
+    plain_ms = _max_over_ranks(dist, statistics.mean(a0.elapsed_time(a1) for a0, a1 in plain))
+
     per_kernel = {k: [] for k in KERNELS}
     step_ms = []
     for e in evs:
@@ -346,6 +361,11 @@ def run_ours(args):
                        "parallelism": f"{world} independent replica(s)"},
             "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": st.launches_per_step * args.steps,
+            "step_without_kernel_events": {
+                "ms_per_step": round(plain_ms, 4),
+                "value": round(flop_step / (plain_ms * 1e-3) / 1e12, 1),
+                "note": "the same steps timed with a start and an end event only (informational; "
+                        "value and kernels come from the per-kernel-event loop)"},
             "clocks": clk.summary(),
         }
         print(json.dumps(line))

@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_block_scaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const Params p)
 {
+    pdl_begin();
     using Cf = Cfg<kPair>;
     constexpr int STAGES = Cf::STAGES;
     constexpr int STAGE_BYTES = Cf::STAGE_BYTES;
@@ -751,6 +752,7 @@ __global__ void k_diag_wait(uint64_t limit_ns)
 __global__ void __launch_bounds__(256) k_splitk_reduce(const float *__restrict__ ws, int splits, int R, int C,
                                                        uint16_t *__restrict__ out, int64_t ldo)
 {
+    pdl_begin();
     const int64_t per_row = C / 8;
     const int64_t total = (int64_t)R * per_row;
     const int64_t plane = (int64_t)R * C;
@@ -775,6 +777,7 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(const float *__restrict__
 __global__ void __launch_bounds__(256) k_splitk_reduce_acc(const float *__restrict__ ws, int splits, int R, int C,
                                                            float *__restrict__ acc, int64_t ld_acc)
 {
+    pdl_begin();
     const int64_t per_row = C / 4;
     const int64_t total = (int64_t)R * per_row;
     const int64_t plane = (int64_t)R * C;
@@ -980,22 +983,29 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
             return cuda_status(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         di.attr_set[variant] = true;
     }
-    cudaLaunchAttribute cluster_attr[1];
-    cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
-    cluster_attr[0].val.clusterDim.x = 2;
-    cluster_attr[0].val.clusterDim.y = 1;
-    cluster_attr[0].val.clusterDim.z = 1;
+    // [0] programmatic dependent launch (every kernel of the library begins with
+    // pdl_begin), [1] CTA pairs
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = 2;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
     cfg.stream = st;
+    cfg.attrs = attrs;
+    cfg.numAttrs = kPair ? 2 : 1;
     if constexpr (kPair) {
-        cfg.attrs = cluster_attr;
-        cfg.numAttrs = 1;
         if (di.max_clusters[variant] == 0) {
-            cfg.gridDim = dim3(2 * (di.sms / 2), 1, 1);
+            cudaLaunchConfig_t q = cfg;  // the occupancy query sees the cluster shape only
+            q.gridDim = dim3(2 * (di.sms / 2), 1, 1);
+            q.attrs = attrs + 1;
+            q.numAttrs = 1;
             int n = 0;
-            e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&n, kernel, &q);
             if (e != cudaSuccess)
                 return cuda_status(e, "cudaOccupancyMaxActiveClusters");
             di.max_clusters[variant] = n < 1 ? -1 : n;  // -1: no pair fits, use single CTAs
@@ -1055,9 +1065,9 @@ rlq_status launch_impl(const GemmArgs &a, int splits, cudaStream_t st, bool with
     if (rgrid > (int64_t)di.sms * 8)
         rgrid = (int64_t)di.sms * 8;
     if (a.acc)
-        k_splitk_reduce_acc<<<(int)rgrid, 256, 0, st>>>(a.ws, p.splits, p.R, p.C, a.acc, a.ld_acc);
+        (void)launch_pdl(k_splitk_reduce_acc, dim3((int)rgrid), dim3(256), 0, st, a.ws, p.splits, p.R, p.C, a.acc, a.ld_acc);
     else
-        k_splitk_reduce<<<(int)rgrid, 256, 0, st>>>(a.ws, p.splits, p.R, p.C, a.out, a.ldo);
+        (void)launch_pdl(k_splitk_reduce, dim3((int)rgrid), dim3(256), 0, st, a.ws, p.splits, p.R, p.C, a.out, a.ldo);
     return cuda_status(cudaGetLastError(), "split-K reduction launch");
 }
 
@@ -1136,7 +1146,7 @@ rlq_status launch_splitk_reduce(const float *ws, int splits, int64_t R, int64_t 
     int64_t rgrid = (total + 255) / 256;
     if (rgrid > (int64_t)sms * 8)
         rgrid = (int64_t)sms * 8;
-    k_splitk_reduce<<<(int)rgrid, 256, 0, st>>>(ws, splits, (int)R, (int)C, out, ldo);
+    (void)launch_pdl(k_splitk_reduce, dim3((int)rgrid), dim3(256), 0, st, ws, splits, (int)R, (int)C, out, ldo);
     return cuda_status(cudaGetLastError(), "split-K reduction launch");
 }
 

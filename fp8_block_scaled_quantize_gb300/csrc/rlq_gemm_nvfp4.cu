@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
     k_gemm_nvfp4w(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmS, const NvParams p)
 {
+    pdl_begin();
     extern __shared__ uint8_t nv_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(nv_smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NV_OFF_BARS);
@@ -618,7 +619,7 @@ rlq_status launch_gemm_nvfp4w(const uint16_t *x, int64_t ldx, const uint8_t *wq,
     p.num_units = p.num_tiles * p.splits;
     p.timeout_ns = nv_wait_limit_ns();
     const int grid = p.num_units < sms ? p.num_units : sms;
-    k_gemm_nvfp4w<<<grid, NV_THREADS, NV_SMEM, stream>>>(tmX, tmQ, tmS, p);
+    (void)launch_pdl(k_gemm_nvfp4w, dim3(grid), dim3(NV_THREADS), NV_SMEM, stream, tmX, tmQ, tmS, p);
     e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1)
         return cuda_status(e, "NVFP4 GEMM launch");

@@ -8,6 +8,39 @@
 
 namespace rlq {
 
+// Programmatic dependent launch: every kernel of the library is launched with
+// programmatic stream serialization allowed and begins with pdl_begin(), which
+// first waits until the grids it depends on (the previous kernels in the stream)
+// have completed and their memory is visible, and then lets the next kernel in
+// the stream be scheduled as soon as every block of this grid has started.  The
+// next kernel's blocks can then be resident and waiting when this grid ends,
+// instead of being launched only afterwards.  No kernel touches global memory
+// before the wait, so the ordering of the stream is unchanged.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_begin()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Records a failure description for rlq_last_error() and returns `st`.
 rlq_status fail(rlq_status st, const char *fmt, ...);
 

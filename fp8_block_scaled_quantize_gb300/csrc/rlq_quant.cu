@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_rows_seg(const uint16_t *__res
                                                         const float *__restrict__ rstd,
                                                         const uint16_t *__restrict__ gamma)
 {
+    pdl_begin();
     static_assert(QR_NV == 8, "the exchange below reduces eight groups per half-warp");
     const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
     const bool b3 = l16 & 8, b2 = l16 & 4, b1 = l16 & 2;
@@ -347,6 +348,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_dual(const uint16_t *__restric
                                                     const float *__restrict__ rstd,
                                                     const uint16_t *__restrict__ gamma)
 {
+    pdl_begin();
     __shared__ __align__(16) uint16_t tile[GRP * TP];
     __shared__ __align__(16) uint32_t ccm[8][GRP / 2];  // per-warp column-pair maxima
     __shared__ __align__(8) float col_r[GRP], col_nsd[GRP], col_f[GRP];
@@ -537,6 +539,7 @@ __device__ __forceinline__ float fma_sq_bf16x2(uint32_t w, float acc)
 __global__ void __launch_bounds__(2 * RMS_ROWS) k_rms_rstd(const uint16_t *__restrict__ h, int64_t M, int64_t K,
                                                            int64_t ldh, float eps, float *__restrict__ rstd)
 {
+    pdl_begin();
     extern __shared__ __align__(16) uint8_t rms_buf[];
     const int t = threadIdx.x & 31;
     const int64_t m0 = (int64_t)blockIdx.x * RMS_ROWS;
@@ -651,6 +654,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_weight(const uint16_t *__restr
                                                          float *__restrict__ s, int64_t lds,
                                                          uint8_t *__restrict__ qT, int64_t ldqT, int64_t NB, int64_t KB)
 {
+    pdl_begin();
     __shared__ float red[8];
     __shared__ __align__(16) uint8_t tqs[GRP * GRP];  // transposed codes: 128 rows of 128 bytes, swizzled
     const int t = threadIdx.x, j = t & 31, a = t >> 5;
@@ -751,6 +755,7 @@ __global__ void __launch_bounds__(256) k_quant_per_row(const uint16_t *__restric
                                                        float *__restrict__ s, float *__restrict__ s_rep,
                                                        int64_t ld_rep)
 {
+    pdl_begin();
     __shared__ uint32_t red[8];
     __shared__ float sh[4];  // s, r, s*f, f of the CTA's row
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -818,6 +823,7 @@ __global__ void __launch_bounds__(256) k_quant_per_row_reg(const uint16_t *__res
                                                            float *__restrict__ s, float *__restrict__ s_rep,
                                                            int64_t ld_rep)
 {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int64_t team = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nteams = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -871,6 +877,7 @@ __global__ void __launch_bounds__(256) k_quant_per_row_reg_cta(const uint16_t *_
                                                                float *__restrict__ s, float *__restrict__ s_rep,
                                                                int64_t ld_rep)
 {
+    pdl_begin();
     __shared__ uint32_t red[8];
     __shared__ float sh[4];  // s, r, s*f, f of the CTA's row
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -990,6 +997,7 @@ __device__ __forceinline__ uint4 ld_keep(const uint16_t *p)
 __global__ void __launch_bounds__(256) k_nvfp4_amax(const uint16_t *__restrict__ w, int64_t N, int64_t K, int64_t ldw,
                                                     unsigned int *__restrict__ amax_bits)
 {
+    pdl_begin();
     const int K8 = (int)(K / 8);
     uint32_t pm = 0;
     for (int64_t n = blockIdx.x; n < N; n += gridDim.x) {
@@ -1016,6 +1024,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const uint16_t *__restrict_
                                                      uint8_t *__restrict__ sb, int64_t ldsb,
                                                      const unsigned int *__restrict__ amax_bits)
 {
+    pdl_begin();
     const float amax = __uint_as_float(*amax_bits);
     const float st = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);  // 6 * 448
     // block codes by the bracketing test of nv_codes2: (amax_b * RN(1/6)) * RN(1/st) is
@@ -1088,6 +1097,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const uint16_t *__restrict_
 
 __global__ void k_nvfp4_tensor_scale(float *st)
 {
+    pdl_begin();
     const float amax = *st;  // the amax pass left its bits here
     *st = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
 }
@@ -1099,6 +1109,7 @@ __global__ void k_nvfp4_tensor_scale(float *st)
 __global__ void __launch_bounds__(256) k_aqn_perturb(uint16_t *__restrict__ gamma, int64_t K,
                                                      const float *__restrict__ z, float sigma)
 {
+    pdl_begin();
     for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < K; k += (int64_t)gridDim.x * blockDim.x) {
         const float v = __fadd_rn(bf_lo(gamma[k]), __fmul_rn(sigma, z[k]));
         uint16_t h;
@@ -1149,6 +1160,7 @@ __global__ void __launch_bounds__(256) k_uaq_fold(uint16_t *__restrict__ w, int6
                                                   uint16_t *__restrict__ prev, int64_t R, int64_t ldp, int64_t K8,
                                                   const float *__restrict__ s, int gw)
 {
+    pdl_begin();
     const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (v >= K8)
         return;
@@ -1185,11 +1197,11 @@ cudaError_t launch_quant_rows(const uint16_t *x, int64_t M, int64_t K, int64_t l
     if (blocks < 1)
         blocks = 1;
     if (rstd)
-        k_quant_rows_seg<true><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, (int)segs, (int)nv, ldx, q, ldq, s, lds,
-                                                                 rstd, gamma);
+        (void)launch_pdl(k_quant_rows_seg<true>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, (int)segs, (int)nv,
+                         ldx, q, ldq, s, lds, rstd, gamma);
     else
-        k_quant_rows_seg<false><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, (int)segs, (int)nv, ldx, q, ldq, s, lds,
-                                                                  nullptr, nullptr);
+        (void)launch_pdl(k_quant_rows_seg<false>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, (int)segs, (int)nv,
+                         ldx, q, ldq, s, lds, nullptr, nullptr);
     return cudaGetLastError();
 }
 
@@ -1200,10 +1212,11 @@ cudaError_t launch_quant_dual(const uint16_t *x, int64_t M, int64_t K, int64_t l
     const int64_t MB = (M + GRP - 1) / GRP, KB = K / GRP;
     const dim3 grid((unsigned)(MB < 0x7FFFFFFF ? MB : 0x7FFFFFFF), (unsigned)(KB < 65535 ? KB : 65535));
     if (rstd)
-        k_quant_dual<true><<<grid, 256, 0, st>>>(x, M, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, MB, KB, rstd, gamma);
+        (void)launch_pdl(k_quant_dual<true>, dim3(grid), dim3(256), 0, st, x, M, ldx, q, ldq, s, lds, qT, ldqT, sc,
+                         ldsc, MB, KB, rstd, gamma);
     else
-        k_quant_dual<false><<<grid, 256, 0, st>>>(x, M, ldx, q, ldq, s, lds, qT, ldqT, sc, ldsc, MB, KB, nullptr,
-                                                  nullptr);
+        (void)launch_pdl(k_quant_dual<false>, dim3(grid), dim3(256), 0, st, x, M, ldx, q, ldq, s, lds, qT, ldqT, sc,
+                         ldsc, MB, KB, nullptr, nullptr);
     return cudaGetLastError();
 }
 
@@ -1218,7 +1231,7 @@ cudaError_t launch_rms_rstd(const uint16_t *h, int64_t M, int64_t K, int64_t ldh
         attr = true;
     }
     const int64_t blocks = (M + RMS_ROWS - 1) / RMS_ROWS;
-    k_rms_rstd<<<(unsigned)blocks, 2 * RMS_ROWS, RMS_SMEM, st>>>(h, M, K, ldh, eps, rstd);
+    (void)launch_pdl(k_rms_rstd, dim3((unsigned)blocks), dim3(2 * RMS_ROWS), RMS_SMEM, st, h, M, K, ldh, eps, rstd);
     return cudaGetLastError();
 }
 
@@ -1227,7 +1240,7 @@ cudaError_t launch_quant_weight(const uint16_t *w, int64_t N, int64_t K, int64_t
 {
     const int64_t NB = N / GRP, KB = K / GRP;
     const dim3 grid((unsigned)(NB < 0x7FFFFFFF ? NB : 0x7FFFFFFF), (unsigned)(KB < 65535 ? KB : 65535));
-    k_quant_weight<<<grid, 256, 0, st>>>(w, ldw, q, ldq, s, lds, qT, ldqT, NB, KB);
+    (void)launch_pdl(k_quant_weight, dim3(grid), dim3(256), 0, st, w, ldw, q, ldq, s, lds, qT, ldqT, NB, KB);
     return cudaGetLastError();
 }
 
@@ -1240,39 +1253,50 @@ cudaError_t launch_quant_per_row(const uint16_t *x, int64_t M, int64_t K, int64_
         if (blocks > sms * 2 * 16)
             blocks = sms * 2 * 16;
         if (K <= 256 * 4)
-            k_quant_per_row_reg<4><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg<4>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q, ldq, s,
+                             s_rep, ld_rep);
         else if (K <= 256 * 8)
-            k_quant_per_row_reg<8><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg<8>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q, ldq, s,
+                             s_rep, ld_rep);
         else if (K <= 256 * 12)
-            k_quant_per_row_reg<12><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg<12>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q, ldq, s,
+                             s_rep, ld_rep);
         else
-            k_quant_per_row_reg<16><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg<16>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q, ldq, s,
+                             s_rep, ld_rep);
     } else if (K <= 2048 * 16) {  // longer rows: a CTA per row, held in registers
         // as few loads per thread as cover the row (fewer registers, more resident CTAs;
         // measured: K = 18944 at 10 loads 0.81 of HBM, at 16 loads 0.66)
         const int64_t blocks = M < sms * 16 ? M : sms * 16;
         const int64_t nv = (K + 2047) / 2048;
         if (nv <= 4)
-            k_quant_per_row_reg_cta<4><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg_cta<4>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q, ldq,
+                             s, s_rep, ld_rep);
         else if (nv <= 6)
-            k_quant_per_row_reg_cta<6><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg_cta<6>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q, ldq,
+                             s, s_rep, ld_rep);
         else if (nv <= 8)
-            k_quant_per_row_reg_cta<8><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg_cta<8>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q, ldq,
+                             s, s_rep, ld_rep);
         else if (nv <= 10)
-            k_quant_per_row_reg_cta<10><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg_cta<10>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q,
+                             ldq, s, s_rep, ld_rep);
         else if (nv <= 12)
-            k_quant_per_row_reg_cta<12><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg_cta<12>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q,
+                             ldq, s, s_rep, ld_rep);
         else if (nv <= 14)
-            k_quant_per_row_reg_cta<14><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg_cta<14>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q,
+                             ldq, s, s_rep, ld_rep);
         else
-            k_quant_per_row_reg_cta<16><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+            (void)launch_pdl(k_quant_per_row_reg_cta<16>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q,
+                             ldq, s, s_rep, ld_rep);
     } else if (M >= sms * 64) {  // enough rows for every resident warp: a warp per row
         int64_t blocks = (M + 7) / 8;
         if (blocks > sms * 8 * 16)
             blocks = sms * 8 * 16;
-        k_quant_per_row<32><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+        (void)launch_pdl(k_quant_per_row<32>, dim3((unsigned)blocks), dim3(256), 0, st, x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
     } else {  // few, long rows: a CTA per row
-        k_quant_per_row<256><<<(unsigned)M, 256, 0, st>>>(x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
+        (void)launch_pdl(k_quant_per_row<256>, dim3((unsigned)M), dim3(256), 0, st, x, M, K, ldx, q, ldq, s, s_rep, ld_rep);
     }
     return cudaGetLastError();
 }
@@ -1287,10 +1311,10 @@ cudaError_t launch_quant_nvfp4(const uint16_t *w, int64_t N, int64_t K, int64_t 
     // one CTA per row while rows are few, else a grid-stride over rows
     const int64_t cap = (int64_t)sm_count() * 8;
     const int64_t g1 = N > cap ? cap : (N < 1 ? 1 : N);
-    k_nvfp4_amax<<<(unsigned)g1, 256, 0, st_stream>>>(w, N, K, ldw, amax_bits);
+    (void)launch_pdl(k_nvfp4_amax, dim3((unsigned)g1), dim3(256), 0, st_stream, w, N, K, ldw, amax_bits);
     const int64_t g2 = N > cap * 4 ? cap * 4 : (N < 1 ? 1 : N);
-    k_nvfp4_quant<<<(unsigned)g2, 256, 0, st_stream>>>(w, N, K, ldw, q, ldq, sb, ldsb, amax_bits);
-    k_nvfp4_tensor_scale<<<1, 1, 0, st_stream>>>(st);
+    (void)launch_pdl(k_nvfp4_quant, dim3((unsigned)g2), dim3(256), 0, st_stream, w, N, K, ldw, q, ldq, sb, ldsb, amax_bits);
+    (void)launch_pdl(k_nvfp4_tensor_scale, dim3(1), dim3(1), 0, st_stream, st);
     return cudaGetLastError();
 }
 
@@ -1299,7 +1323,7 @@ cudaError_t launch_aqn_perturb(uint16_t *gamma, int64_t K, const float *z, float
     int64_t blocks = (K + 255) / 256;
     if (blocks > (int64_t)sm_count() * 8)
         blocks = (int64_t)sm_count() * 8;
-    k_aqn_perturb<<<(unsigned)blocks, 256, 0, st>>>(gamma, K, z, sigma);
+    (void)launch_pdl(k_aqn_perturb, dim3((unsigned)blocks), dim3(256), 0, st, gamma, K, z, sigma);
     return cudaGetLastError();
 }
 
@@ -1316,7 +1340,7 @@ cudaError_t launch_uaq_fold(uint16_t *w, int64_t N, int64_t K, int64_t ldw, cons
     const int gp = (prev && R > 0) ? gy(R) : 0;
     if (gw + gp == 0)
         return cudaSuccess;
-    k_uaq_fold<<<dim3(gx, (unsigned)(gw + gp)), 256, 0, st>>>(w, N, ldw, prev, R, ldp, K8, s, gw);
+    (void)launch_pdl(k_uaq_fold, dim3(dim3(gx, (unsigned)(gw + gp))), dim3(256), 0, st, w, N, ldw, prev, R, ldp, K8, s, gw);
     return cudaGetLastError();
 }
 
