@@ -462,6 +462,229 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Decode-sized batches (up to NV_GEMV_MAX_M tokens) on the CUDA cores.  With a
+// handful of tokens the tensor-core kernel's time per weight stage does not
+// depend on M and is several times the time to stream the weights from HBM.
+// Here a warp owns R weight rows at a time and its lanes split the contraction:
+// per step a lane takes a pair of 16-element blocks (16 bytes of codes and two
+// scale bytes per row), U steps' loads issued together, so a warp reads 512
+// contiguous bytes of each row per step.  Where the layer has too few rows to
+// give every SM enough warps (down projections: long contractions, few output
+// rows) a row group is shared by ks warps of a CTA, each taking every ks-th
+// chunk of the contraction.  An E2M1 pair becomes an f16 pair (hardware
+// conversion), its product with the block scale is taken in f16 (exact: at most
+// 6 significant bits within [2^-10, 2688], f16 normals), widened to fp32 and
+// multiplied with the bf16 activations by fp32 FMAs.  A lane's partial sums are
+// added across its warp by a halving butterfly, the ks warps' sums in warp order
+// through shared memory, st applied once and the result rounded to bf16.  The
+// fp32 additions run in a fixed order, so results repeat bit for bit.
+
+constexpr int NV_GEMV_MAX_M = 4;        // tokens the CUDA-core kernel takes
+constexpr int NV_GEMV_SPLIT_MAX_M = 2;  // ... also when a split-K workspace is offered
+constexpr int NV_GEMV_THREADS = 256;
+constexpr int NV_GEMV_TASKS_PER_SM = 32;  // warp tasks per SM below which a row group is split across warps
+
+// Eight E2M1 codes (element 2j in the low nibble of byte j) times a block scale
+// held as an f16 pair: h[j] holds elements 2j (low half) and 2j + 1 (high half).
+__device__ __forceinline__ void nv_e2m1x8_scaled(uint32_t codes, uint32_t scale2, uint32_t *h)
+{
+    asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+        "mov.b32 {c0, c1, c2, c3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, c0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, c2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, c3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(codes));
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[j]) : "r"(scale2));
+}
+
+// An E4M3 code as an f16 pair (both halves), exact.
+__device__ __forceinline__ uint32_t nv_e4m3_f16x2(uint32_t code)
+{
+    uint32_t h;
+    const uint16_t two = (uint16_t)(code | (code << 8));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+    return h;
+}
+
+__device__ __forceinline__ float2 nv_f16x2_f32(uint32_t h)
+{
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
+    return make_float2(lo, hi);
+}
+
+__device__ __forceinline__ uint4 nv_ld_stream16(const uint8_t *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t nv_ld_stream_u16(const uint8_t *p)
+{
+    uint16_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+// Halving butterfly over a warp: afterwards lane l holds the warp's sum of
+// v[l >> (5 - log2 NVAL)] (the other lanes of that value's group hold it too).
+template <int NVAL>
+__device__ __forceinline__ float nv_warp_sums(float (&v)[NVAL], int lane)
+{
+    static_assert(NVAL >= 1 && NVAL <= 32 && (NVAL & (NVAL - 1)) == 0, "a power of two up to 32");
+#pragma unroll
+    for (int n = NVAL, off = 16; n > 1; n >>= 1, off >>= 1) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+        }
+    }
+    float s = v[0];
+#pragma unroll
+    for (int off = 16 / NVAL; off > 0; off >>= 1)
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+    return s;
+}
+
+// MT tokens (M <= MT), R weight rows per warp, U steps of a pair of blocks per
+// lane and chunk, MINB CTAs per SM (the register budget).  The CTA's 8 warps work on 8 / ks row groups at a time, ks
+// warps per group, each taking every ks-th chunk of the group's contraction; the
+// ks partial sums of a group are added through shared memory in warp order.
+template <int MT, int R, int U, int MINB>
+__global__ void __launch_bounds__(NV_GEMV_THREADS, MINB)
+    k_gemv_nvfp4(const uint16_t *__restrict__ x, int64_t ldx, const uint8_t *__restrict__ wq, int64_t ldwq,
+                 const uint8_t *__restrict__ wsb, int64_t ldwsb, const float *__restrict__ st,
+                 uint16_t *__restrict__ y, int64_t ldy, int M, int N, int K, int ks)
+{
+    pdl_begin();
+    constexpr int WARPS = NV_GEMV_THREADS / 32;
+    constexpr int NVAL = R * MT;
+    constexpr int LOG_NVAL = NVAL >= 32 ? 5 : NVAL >= 16 ? 4 : NVAL >= 8 ? 3 : NVAL >= 4 ? 2 : NVAL >= 2 ? 1 : 0;
+    __shared__ float red[WARPS][NVAL];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gpc = WARPS / ks;                             // row groups per CTA round
+    const int npairs = K >> 5;                              // pairs of 16-element blocks per row (K % 64 == 0)
+    const int nchunks = (npairs + 32 * U - 1) / (32 * U);  // chunks per row group
+    const int groups = (N + R - 1) / R;
+    const float stv = *st;
+    for (int round = blockIdx.x; round * gpc < groups; round += gridDim.x) {
+        const int g = round * gpc + warp / ks;
+        const int slice = warp % ks;
+        float2 acc[R][MT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                acc[r][m] = make_float2(0.0f, 0.0f);
+        if (g < groups) {
+            const uint8_t *qrow[R];
+            const uint8_t *srow[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int n = min(g * R + r, N - 1);  // (rows past N repeat the last row; their sums are not stored)
+                qrow[r] = wq + (int64_t)n * ldwq;
+                srow[r] = wsb + (int64_t)n * ldwsb;
+            }
+            for (int ci = slice; ci < nchunks; ci += ks) {
+                uint4 c[U][R];
+                uint32_t sc2[U][R];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int p = ci * 32 * U + 32 * u + lane;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        if (p < npairs) {
+                            c[u][r] = nv_ld_stream16(qrow[r] + 16 * (int64_t)p);
+                            sc2[u][r] = nv_ld_stream_u16(srow[r] + 2 * (int64_t)p);
+                        } else {
+                            c[u][r] = make_uint4(0, 0, 0, 0);
+                            sc2[u][r] = 0;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int p = ci * 32 * U + 32 * u + lane;
+                    if (p >= npairs)
+                        break;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {  // the two blocks of the pair
+                        // the block's 16 activations per token as fp32 pairs (L1-allocating: every warp reads them)
+                        float2 xf[MT][8];
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+                            if (m < M) {
+                                const uint4 *xp =
+                                    reinterpret_cast<const uint4 *>(x + (int64_t)m * ldx + 32 * (int64_t)p + 16 * j);
+                                x0 = __ldg(xp);
+                                x1 = __ldg(xp + 1);
+                            }
+                            const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                xf[m][i] =
+                                    make_float2(__uint_as_float(xw[i] << 16), __uint_as_float(xw[i] & 0xFFFF0000u));
+                        }
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t sc = nv_e4m3_f16x2((sc2[u][r] >> (8 * j)) & 0xFFu);
+                            uint32_t h[8];
+                            nv_e2m1x8_scaled(j ? c[u][r].z : c[u][r].x, sc, h);
+                            nv_e2m1x8_scaled(j ? c[u][r].w : c[u][r].y, sc, h + 4);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float2 w = nv_f16x2_f32(h[i]);
+#pragma unroll
+                                for (int m = 0; m < MT; ++m)
+                                    acc[r][m] = __ffma2_rn(w, xf[m][i], acc[r][m]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        float v[NVAL];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                v[r * MT + m] = acc[r][m].x + acc[r][m].y;
+        const float sum = nv_warp_sums<NVAL>(v, lane);
+        if ((lane & ((32 >> LOG_NVAL) - 1)) == 0)
+            red[warp][lane >> (5 - LOG_NVAL)] = sum;
+        __syncthreads();
+        if (threadIdx.x < gpc * NVAL) {
+            const int gi = threadIdx.x / NVAL, idx = threadIdx.x - gi * NVAL;
+            const int gg = round * gpc + gi;
+            const int r = idx / MT, m = idx - (idx / MT) * MT;
+            float t = red[gi * ks][idx];
+            for (int k = 1; k < ks; ++k)
+                t += red[gi * ks + k][idx];
+            if (gg < groups && m < M && gg * R + r < N) {
+                const float o = __fmul_rn(t, stv);
+                uint16_t bits;
+                asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(bits) : "f"(o));
+                y[(int64_t)m * ldy + gg * R + r] = bits;
+            }
+        }
+        __syncthreads();  // red is reused by the next round
+    }
+}
+
 // ---------------------------------------------------------------- host ---
 
 PFN_cuTensorMapEncodeTiled_v12000 nv_encode_fn()
@@ -564,17 +787,55 @@ rlq_status plan_nvfp4_splitk(int64_t M, int64_t N, int64_t K, int64_t ws_cap, in
     if (rs != RLQ_OK)
         return rs;
     int s = 1;
-    if (M > 0 && N > 0 && K > 0)
+    if (M > NV_GEMV_SPLIT_MAX_M && N > 0 && K > 0)  // (one or two tokens run one pass on the CUDA cores)
         nv_plan(M, N, K, sms, ws_cap, &s, &kps);
     *splits = s;
     *ws_bytes = s > 1 ? (int64_t)s * M * N * 4 : 0;
     return RLQ_OK;
 }
 
+namespace {
+
+template <int MT, int R, int U, int MINB>
+rlq_status launch_gemv(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq, const uint8_t *wsb,
+                       int64_t ldwsb, const float *st, uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                       cudaStream_t stream)
+{
+    int sms = 0;
+    const rlq_status rs = nv_sms(&sms);
+    if (rs != RLQ_OK)
+        return rs;
+    constexpr int WARPS = NV_GEMV_THREADS / 32;
+    const int64_t groups = (N + R - 1) / R;
+    const int64_t nchunks = (K / 32 + 32 * U - 1) / (32 * U);
+    // warps per row group: enough warp tasks to fill the GPU when the layer has few
+    // output rows (a long contraction and few rows: down projections)
+    int ks = 1;
+    while (ks < WARPS && ks < nchunks && groups * ks < (int64_t)sms * NV_GEMV_TASKS_PER_SM)
+        ks *= 2;
+    const int64_t rounds = (groups + WARPS / ks - 1) / (WARPS / ks);
+    int64_t grid = rounds < (int64_t)sms * 16 ? rounds : (int64_t)sms * 16;
+    (void)launch_pdl(k_gemv_nvfp4<MT, R, U, MINB>, dim3((unsigned)grid), dim3(NV_GEMV_THREADS), 0, stream, x, ldx, wq,
+                     ldwq, wsb, ldwsb, st, y, ldy, (int)M, (int)N, (int)K, ks);
+    return cuda_status(cudaGetLastError(), "NVFP4 decode GEMM launch");
+}
+
+}  // namespace
+
 rlq_status launch_gemm_nvfp4w(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq, const uint8_t *wsb,
                               int64_t ldwsb, const float *st, uint16_t *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
                               void *workspace, int64_t workspace_bytes, cudaStream_t stream)
 {
+    // A handful of tokens: the CUDA-core kernel, one pass.  Three or four tokens
+    // with a split-K workspace take the split tensor-core path instead (faster for
+    // long contractions over few output rows, about even elsewhere).
+    if (M <= NV_GEMV_SPLIT_MAX_M || (M <= NV_GEMV_MAX_M && workspace == nullptr)) {
+        if (M == 1)
+            return launch_gemv<1, 2, 4, 3>(x, ldx, wq, ldwq, wsb, ldwsb, st, y, ldy, M, N, K, stream);
+        if (M == 2)
+            return launch_gemv<2, 4, 2, 2>(x, ldx, wq, ldwq, wsb, ldwsb, st, y, ldy, M, N, K, stream);
+        return launch_gemv<4, 4, 2, 2>(x, ldx, wq, ldwq, wsb, ldwsb, st, y, ldy, M, N, K, stream);
+    }
     CUtensorMap tmX, tmQ, tmS;
     rlq_status rs = nv_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, NV_BK, NV_BM,
                            CU_TENSOR_MAP_SWIZZLE_128B, "bf16 activations");

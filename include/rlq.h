@@ -305,7 +305,10 @@ rlq_status rlq_quant_nvfp4(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
  * with the operands rlq_quant_nvfp4 writes.  Each weight value e2m1 * e4m3 is exact
  * in bf16 (at most 6 significant bits, within [2^-10, 2688] or 0); the products with
  * x and their sum over K are accumulated in fp32 by the tensor cores, then multiplied
- * once by st and rounded to bf16.  The activations are not quantized.
+ * once by st and rounded to bf16.  The activations are not quantized.  Batches of
+ * up to 4 tokens run on the CUDA cores instead (fp32 FMAs of the same exact products,
+ * summed in a fixed order): the result is the same up to the order of the fp32
+ * additions, and repeats bit for bit from call to call.
  *
  *   x    bf16 [M, K], pitch ldx >= K (elements, a multiple of 8), 16-byte aligned
  *   wq   packed E2M1 codes [N, K/2] as rlq_quant_nvfp4 writes them (low nibble =
@@ -337,7 +340,8 @@ rlq_status rlq_gemm_nvfp4_weight_only(const uint16_t *x, int64_t ldx, const uint
  * split-K calls (caller-owned, 16-byte aligned or NULL for one pass; the plan
  * is lowered until splits * M * N * 4 bytes fit); the unconstrained plan's
  * size comes from rlq_gemm_splitk_workspace_bytes(RLQ_GEMM_NVFP4_WEIGHT_ONLY,
- * M, N, K).  Other arguments, shapes and errors as for
+ * M, N, K), which is 0 for M <= 2: one or two tokens run the single-pass CUDA-core
+ * path whatever the workspace, with the bits of rlq_gemm_nvfp4_weight_only.  Other arguments, shapes and errors as for
  * rlq_gemm_nvfp4_weight_only.
  */
 rlq_status rlq_gemm_nvfp4_weight_only_splitk(const uint16_t *x, int64_t ldx, const uint8_t *wq, int64_t ldwq,

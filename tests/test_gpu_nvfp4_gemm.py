@@ -22,6 +22,9 @@ from gpu_util import assert_gemm_close, idx, normal_bits, np_, strata, to_dev, u
 
 pytestmark = pytest.mark.gpu
 
+DECODE_MAX_M = 4        # batches of up to this many tokens run the CUDA-core kernel ...
+DECODE_SPLIT_MAX_M = 2  # ... also through the split-K entry point (no workspace planned)
+
 
 def _unpack(qp: np.ndarray) -> np.ndarray:
     lo, hi = qp & 0xF, qp >> 4
@@ -166,7 +169,7 @@ def _ws(M, N, K):
     return nb, (torch.empty(nb, dtype=torch.uint8, device="cuda") if nb else None)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 128, 4096), (16, 256, 8192), (130, 384, 2048), (1, 128, 4288),
+@pytest.mark.parametrize("M,N,K", [(5, 128, 4096), (16, 256, 8192), (130, 384, 2048), (5, 128, 4288),
                                    (7, 640, 3392)])
 def test_splitk_parity(M, N, K):
     """Shapes whose output has far fewer tiles than the GPU has SMs: the plan
@@ -185,7 +188,7 @@ def test_splitk_parity(M, N, K):
     assert_gemm_close(y1, ref, f"NVFP4 GEMM {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(3, 128, 4288), (64, 256, 8192)])
+@pytest.mark.parametrize("M,N,K", [(5, 128, 4288), (64, 256, 8192)])
 def test_splitk_integer_case_bit_exact(M, N, K):
     """The exact integer case of test_integer_case_bit_exact under a split plan:
     every split sum and their total are exact, so the split and single-pass
@@ -211,7 +214,8 @@ def test_splitk_integer_case_bit_exact(M, N, K):
 @pytest.mark.parametrize("case", ["32b_down_m1", "32b_down_m16", "qwen7b_down_m64"])
 def test_splitk_down_projections(case):
     """The down projections at decode sizes (few output tiles, long contraction:
-    the case the split plan is for)."""
+    the case the split plan is for; a single token runs the CUDA-core kernel in
+    one pass, with no workspace)."""
     if case.startswith("32b"):
         M = int(case.split("_m")[1])
         d = I.sweep_32b(M, "down", with_dy=False)
@@ -220,7 +224,7 @@ def test_splitk_down_projections(case):
         d = I.qwen7b_layer(M, "down")
     N, K = d["w"].shape
     nb, ws = _ws(M, N, K)
-    assert nb > 0
+    assert (nb == 0) if M <= DECODE_SPLIT_MAX_M else (nb > 0)
     (q, sb, st), (oq, osb, ost) = _quantized_weight(d["w"])
     y = rlq.gemm_nvfp4_weight_only(to_dev(d["x"]), q, sb, st, split_k=True, workspace=ws)
     rlq.check()
@@ -258,3 +262,82 @@ def test_splitk_workspace_limits():
                                               ws.data_ptr() + 4, nb - 16, torch.cuda.current_stream().cuda_stream)
     assert e.value.status == 3
     rlq.check()
+
+
+def _integer_case(M, N, K, seed):
+    """Operands whose fp32 sums are exact in any order (see test_integer_case_bit_exact)."""
+    rng = np.random.default_rng(seed)
+    x = I.to_bf16_bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
+    q = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    sb = rng.choice(np.array([0x30, 0x38, 0x40], np.uint8), size=(N, K // 16))
+    ref = oracle.gemm_nvfp4_weight_only(x, q, sb, 1.0)
+    assert np.all(ref * 4 == np.round(ref * 4)) and np.all(np.abs(ref) < 2 ** 17)
+    return x, q, sb, ref
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("N,K", [(128, 64), (256, 1088), (384, 4288), (128, 27648)])
+def test_decode_kernel_parity(M, N, K):
+    """Batches of up to four tokens (the CUDA-core kernel): contractions of 2 block
+    pairs (two lanes busy), 34 pairs (past one warp's 32 lanes), 134 pairs (a
+    ragged last step of loads) and the 32B down projection's 864 on 128 rows (the
+    row group then shared by several warps); M = 3 leaves one token of the
+    four-token kernel unused.  Through the split-K entry point one or two tokens
+    plan no workspace and return the same bits; three or four take the split
+    tensor-core path, within the same tolerance."""
+    x = normal_bits(95 + M, (M, K), 1.0, "x")
+    w = normal_bits(95, (N, K), 0.02, "w")
+    (q, sb, st), (oq, osb, ost) = _quantized_weight(w)
+    nb, ws = _ws(M, N, K)
+    xd = to_dev(x)
+    y = rlq.gemm_nvfp4_weight_only(xd, q, sb, st)
+    y2 = rlq.gemm_nvfp4_weight_only(xd, q, sb, st, split_k=True, workspace=ws)
+    rlq.check()
+    ref = oracle.gemm_nvfp4_weight_only(x, oq, osb, ost)
+    assert_gemm_close(y, ref, f"decode NVFP4 GEMM {M}x{N}x{K}")
+    if M <= DECODE_SPLIT_MAX_M:
+        assert nb == 0
+        assert torch.equal(y, y2)
+    else:
+        assert_gemm_close(y2, ref, f"split-K NVFP4 GEMM {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 4096), (2, 256, 1088), (3, 128, 4288), (4, 384, 2048)])
+def test_decode_kernel_integer_case_bit_exact(M, N, K):
+    """The exact integer case through the CUDA-core kernel: its fp32 sums run in
+    another order than the tensor cores', and must still give the exact result
+    rounded to bf16, bit for bit."""
+    x, q, sb, ref = _integer_case(M, N, K, 17 * M + K)
+    st = torch.ones(1, dtype=torch.float32, device="cuda")
+    y = rlq.gemm_nvfp4_weight_only(to_dev(x), _padded(_pack(q)), _padded(sb), st)
+    rlq.check()
+    assert np.array_equal(u16(y), I.to_bf16_bits(ref.astype(np.float32)))
+
+
+def test_decode_kernel_pitched_and_repeatable():
+    """Pitched activations, codes, scales and output through the CUDA-core kernel
+    (guard bands untouched), and a second call equal bit for bit (its additions run
+    in a fixed order)."""
+    M, N, K = 3, 256, 1024
+    x = normal_bits(96, (M, K), 1.0, "x")
+    w = normal_bits(96, (N, K), 0.02, "w")
+    oq, osb, ost = oracle.quant_nvfp4(w)
+    dev = "cuda"
+    xb = torch.zeros((M, K + 40), dtype=torch.bfloat16, device=dev)
+    xb[:, :K] = to_dev(x)
+    qb = torch.zeros((N, K // 2 + 32), dtype=torch.uint8, device=dev)
+    qb[:, :K // 2] = torch.from_numpy(_pack(oq)).cuda()
+    sbb = torch.zeros((N, K // 16 + 32), dtype=torch.uint8, device=dev)
+    sbb[:, :K // 16] = torch.from_numpy(osb).cuda()
+    st = torch.tensor([ost], dtype=torch.float32, device=dev)
+    outs = []
+    for _ in range(2):
+        yb = torch.full((M, N + 24), 3.0, dtype=torch.bfloat16, device=dev)
+        rlq.rlq_gemm_nvfp4_weight_only(xb.data_ptr(), K + 40, qb.data_ptr(), K // 2 + 32, sbb.data_ptr(),
+                                       K // 16 + 32, st.data_ptr(), yb.data_ptr(), N + 24, M, N, K,
+                                       torch.cuda.current_stream().cuda_stream)
+        rlq.check()
+        assert torch.all(yb[:, N:] == 3.0)
+        outs.append(yb[:, :N].clone())
+    assert torch.equal(outs[0], outs[1])
+    assert_gemm_close(outs[0], oracle.gemm_nvfp4_weight_only(x, oq, osb, ost), "pitched decode NVFP4 GEMM")
