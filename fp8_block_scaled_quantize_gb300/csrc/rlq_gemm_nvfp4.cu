@@ -37,6 +37,9 @@
 // Every mbarrier wait is bounded as in the FP8 GEMM: a wait that runs out records
 // an error word (this translation unit's) and raises the CTA's abort flag; the
 // CTA drains its TMA copies, frees TMEM and exits.
+//
+// Batches of up to 4 tokens take k_gemv_nvfp4 (below) instead: the same exact
+// weight values on the CUDA cores, streaming the codes with no shared-memory ring.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
