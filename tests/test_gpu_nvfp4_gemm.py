@@ -341,3 +341,18 @@ def test_decode_kernel_pitched_and_repeatable():
         outs.append(yb[:, :N].clone())
     assert torch.equal(outs[0], outs[1])
     assert_gemm_close(outs[0], oracle.gemm_nvfp4_weight_only(x, oq, osb, ost), "pitched decode NVFP4 GEMM")
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_decode_kernel_qwen7b_down(M):
+    """The Qwen2.5-7B down projection (N 3584, K 18944) at one and three tokens:
+    few row groups for the GPU's warps, so each group is shared by 4 (M = 1) or 8
+    (M = 3) warps of a CTA whose partial sums meet in shared memory."""
+    d = I.qwen7b_layer(M, "down")
+    (q, sb, st), (oq, osb, ost) = _quantized_weight(d["w"])
+    y = rlq.gemm_nvfp4_weight_only(to_dev(d["x"]), q, sb, st)
+    rlq.check()
+    N = d["w"].shape[0]
+    cols = strata(N, 32, np.random.default_rng(M + 7))
+    ref = oracle.gemm_nvfp4_weight_only(d["x"], oq, osb, ost, cols=cols)
+    assert_gemm_close(y[:, idx(cols)], ref, f"decode NVFP4 GEMM qwen7b down M={M}")
