@@ -350,6 +350,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
+            // the tile order walks the smaller operand fastest and re-reads it: keep it in L2
+            const uint64_t pol_a = l2_policy(p.m_fastest != 0), pol_b = l2_policy(p.m_fastest == 0);
             for (int u = unit0; ok && u < p.num_units; u += unit_step) {
                 const Unit w = unit_of(p, u);
                 const int mt = w.mt, nt = w.nt;
@@ -366,11 +368,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t fb = cluster_addr(full_bar(s), 0);
                         if (cta_rank() == 0)
                             mbar_arrive_expect_tx(full_bar(s), 2 * STAGE_BYTES);
-                        tma_load_2d_pair(a_stage(s), &tmA, fb, kb * BK, mt * Cf::TILE_M + row_offset<kPair>());
+                        tma_load_2d_pair_hint(a_stage(s), &tmA, fb, kb * BK, mt * Cf::TILE_M + row_offset<kPair>(),
+                                              pol_a);
                         if (kBMajorMN)  // this CTA's 128 output columns: one 128 x 128 box
-                            tma_load_2d_pair(b_stage(s), &tmB, fb, nt * BN + row_offset<kPair>(), kb * BK);
+                            tma_load_2d_pair_hint(b_stage(s), &tmB, fb, nt * BN + row_offset<kPair>(), kb * BK, pol_b);
                         else
-                            tma_load_2d_pair(b_stage(s), &tmB, fb, kb * BK, nt * BN + row_offset<kPair>());
+                            tma_load_2d_pair_hint(b_stage(s), &tmB, fb, kb * BK, nt * BN + row_offset<kPair>(), pol_b);
                     } else {
                         if (p.withhold_first_load && it == 0)
                             continue;  // nothing arrives on this stage's barrier
@@ -662,9 +665,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> TMA reads
                     __syncwarp();
                     if (lane == 0 && ok && half_ok) {
-                        tma_store_2d(&tmOut, stg, col0 + rd * STG_COLS, y);
+                        const uint64_t pol = l2_policy(false);  // the output is not read again here
+                        tma_store_2d_hint(&tmOut, stg, col0 + rd * STG_COLS, y, pol);
                         if (STG_COLS == 128)
-                            tma_store_2d(&tmOut, stg + 32 * 128, col0 + rd * STG_COLS + 64, y);
+                            tma_store_2d_hint(&tmOut, stg + 32 * 128, col0 + rd * STG_COLS + 64, y, pol);
                         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                     }
                 }

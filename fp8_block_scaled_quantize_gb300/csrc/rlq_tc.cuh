@@ -174,6 +174,35 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// L2 eviction priorities for bulk copies: the operand a tile order re-reads stays
+// (evict_last), streamed data goes first (evict_first).
+__device__ __forceinline__ uint64_t l2_policy(bool keep)
+{
+    uint64_t pol;
+    if (keep)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
+                                                      uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%3, %4}], [%2], %5;"
+        ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, uint32_t src, int x, int y, uint64_t pol)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;"
+                 ::"l"((uint64_t)map), "r"(src), "r"(x), "r"(y), "l"(pol)
+                 : "memory");
+}
+
 // shared::cluster address of the variable at shared::cta address `a` in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank)
 {
